@@ -1,0 +1,151 @@
+"""CPU oracle for the linear-layer hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (``linear_layer_gb300``)
+never imports it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, double / int64 accumulation);
+this module only marshals numpy arrays into it through ctypes.
+
+Functions and the passages they follow:
+
+* ``decode_f16`` / ``decode_bf16`` / ``decode_e4m3`` -- "Tensor Core" chapter,
+  table "精度：FP16、BF16、TF32、FP8" (bit splits 1/5/10, 1/8/7, 1/4/3).
+* ``gemm`` -- same chapter, section "Tensor Core 做什么": D = A x B + C with
+  low-precision inputs and a wide accumulator; here alpha*A*B + beta*C in double.
+* ``gemm_fp8_blockscaled`` -- same chapter, "精度" section: FP8 needs scaling
+  factors per tensor, row or block; 1x128 blocks of A, 128x128 blocks of B.
+* ``gemv_w8a8`` -- "NVIDIA A100: chip to SIMT", sections 5.1-5.2: int8 x int8
+  summed exactly, then y = fp16(float(z) * s_x * s_W[o]).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.orc_decode_f16.restype = ctypes.c_double
+        L.orc_decode_f16.argtypes = [ctypes.c_uint16]
+        L.orc_decode_bf16.restype = ctypes.c_double
+        L.orc_decode_bf16.argtypes = [ctypes.c_uint16]
+        L.orc_decode_e4m3.restype = ctypes.c_double
+        L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
+        L.orc_encode_f16_rn.restype = ctypes.c_uint16
+        L.orc_encode_f16_rn.argtypes = [ctypes.c_double]
+        vp = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        L.orc_gemm.restype = ctypes.c_int
+        L.orc_gemm.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_double, vp, i64, vp, i64, ctypes.c_double, vp, i64,
+                               vp, ctypes.c_int, vp, vp]
+        L.orc_gemm_fp8_blockscaled.restype = ctypes.c_int
+        L.orc_gemm_fp8_blockscaled.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double, vp, i64, vp, i64, vp, i64,
+                                               vp, i64, ctypes.c_double, vp, i64, vp,
+                                               ctypes.c_int, vp, vp]
+        L.orc_gemv_w8a8.restype = ctypes.c_int
+        L.orc_gemv_w8a8.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_float, vp, i64,
+                                    vp, vp, vp]
+        _lib = L
+    return _lib
+
+
+KIND = {"f16": 0, "bf16": 1, "e4m3": 2}
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def decode_f16(bits: int) -> float:
+    return lib().orc_decode_f16(int(bits) & 0xFFFF)
+
+
+def decode_bf16(bits: int) -> float:
+    return lib().orc_decode_bf16(int(bits) & 0xFFFF)
+
+
+def decode_e4m3(bits: int) -> float:
+    return lib().orc_decode_e4m3(int(bits) & 0xFF)
+
+
+def encode_f16_rn(v: float) -> int:
+    return lib().orc_encode_f16_rn(float(v))
+
+
+def _rows(M, rows):
+    if rows is None:
+        rows = np.arange(M, dtype=np.int32)
+    return np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+
+
+def gemm(kind, M, N, K, alpha, A, lda, B, ldb, beta=0.0, C=None, ldc=0, rows=None,
+         want_absab=True):
+    """Reference D (double, len(rows) x N) and sum_k |A||B| for the selected rows.
+
+    ``A``/``B`` are flat numpy arrays holding the raw element bits (uint16 for
+    f16/bf16, uint8 for e4m3) with leading dimensions ``lda``/``ldb``; ``C`` is
+    float32 with ``ldc`` and is not read when ``beta == 0``.
+    """
+    rows = _rows(M, rows)
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    C = None if C is None else np.ascontiguousarray(C, dtype=np.float32)
+    D = np.zeros((len(rows), N), dtype=np.float64)
+    S = np.zeros((len(rows), N), dtype=np.float64) if want_absab else None
+    rc = lib().orc_gemm(KIND[kind], M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb,
+                        float(beta), _ptr(C), ldc, _ptr(rows), len(rows), _ptr(D), _ptr(S))
+    if rc != 0:
+        raise ValueError("orc_gemm failed with code %d" % rc)
+    return D, S
+
+
+def gemm_fp8_blockscaled(M, N, K, alpha, A, lda, sA, ld_sa, B, ldb, sB, ld_sb, beta=0.0,
+                         C=None, ldc=0, rows=None, want_absab=True):
+    rows = _rows(M, rows)
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    sA = np.ascontiguousarray(sA, dtype=np.float32)
+    sB = np.ascontiguousarray(sB, dtype=np.float32)
+    C = None if C is None else np.ascontiguousarray(C, dtype=np.float32)
+    D = np.zeros((len(rows), N), dtype=np.float64)
+    S = np.zeros((len(rows), N), dtype=np.float64) if want_absab else None
+    rc = lib().orc_gemm_fp8_blockscaled(M, N, K, float(alpha), _ptr(A), lda, _ptr(sA), ld_sa,
+                                        _ptr(B), ldb, _ptr(sB), ld_sb, float(beta), _ptr(C),
+                                        ldc, _ptr(rows), len(rows), _ptr(D), _ptr(S))
+    if rc != 0:
+        raise ValueError("orc_gemm_fp8_blockscaled failed with code %d" % rc)
+    return D, S
+
+
+def gemv_w8a8(N, K, x, s_x, W, ldw, s_W):
+    """Return (z int64 [N], y float16 [N]) for the batch-1 W8A8 linear layer."""
+    x = np.ascontiguousarray(x, dtype=np.int8)
+    W = np.ascontiguousarray(W, dtype=np.int8)
+    s_W = np.ascontiguousarray(s_W, dtype=np.float32)
+    z = np.zeros(N, dtype=np.int64)
+    y = np.zeros(N, dtype=np.uint16)
+    rc = lib().orc_gemv_w8a8(N, K, _ptr(x), float(np.float32(s_x)), _ptr(W), ldw, _ptr(s_W),
+                             _ptr(z), _ptr(y))
+    if rc == 5:
+        raise OverflowError("W8A8 dot product exceeds the INT32 range")
+    if rc != 0:
+        raise ValueError("orc_gemv_w8a8 failed with code %d" % rc)
+    return z, y.view(np.float16)
+
+
+def threads_used() -> int:
+    """Threads OpenMP will use (OMP_NUM_THREADS, else the usable cores)."""
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env:
+        return int(env)
+    return len(os.sched_getaffinity(0))

@@ -1,0 +1,250 @@
+/*
+ * CPU oracle for the linear-layer hot path.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may load
+ * this library.  It shares no code, header, table or helper with the CUDA path
+ * in linear_layer_gb300/csrc; it is written from the definitions on the pages:
+ *
+ *   "Tensor Core" chapter (anrans ai-infra-handbooks), section "Tensor Core 做什么":
+ *       D = A x B + C with low-precision inputs and an FP32 (here: wider) accumulator.
+ *   same chapter, table "精度：FP16、BF16、TF32、FP8": bit splits FP16 1/5/10,
+ *       BF16 1/8/7, FP8 E4M3 1/4/3; FP8 GEMMs need scaling factors per tensor,
+ *       row or block (fine-grained block scaling as in DeepSeek-V3).
+ *   "NVIDIA A100: chip to SIMT", section 5.1: symmetric W8A8, per-token activation
+ *       scale s_x, per-output-channel weight scale s_W[o], zero point 0, integer dot
+ *       product over the whole K into INT32, then dequantise once in the epilogue.
+ *   same page, section 5.2 (kernel epilogue): y[o] = half(float(z) * s_x * s_W[o]),
+ *       evaluated left to right in FP32, then rounded to FP16.
+ *
+ * Arithmetic: every floating-point input is decoded exactly to double from its bit
+ * fields and every sum is a plain double loop (int64 for the integer path).  The
+ * W8A8 dequantisation is the one place where the result is defined in FP32: it is
+ * computed with C float multiplies (this file is compiled with -ffp-contract=off so
+ * no fused multiply-add can change the rounding) and an FP16 encoder written here
+ * from the IEEE binary16 definition (round to nearest, ties to even).
+ *
+ * The W8A8 GEMV path, the GEMM paths and the decoders are pinned by the CPU tests
+ * (closed forms, brute force with exact rationals, library decoders, the printed
+ * INT32 bound of the A100 page section 5.1).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ decoders */
+
+/* IEEE binary16: sign 1, exponent 5 (bias 15), mantissa 10. */
+double orc_decode_f16(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 10) & 0x1F;
+  int m = h & 0x3FF;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -24); /* subnormal: m * 2^(1-15-10) */
+  } else if (e == 31) {
+    v = (m == 0) ? INFINITY : NAN;
+  } else {
+    v = ldexp((double)(1024 + m), e - 25); /* (1 + m/2^10) * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* bfloat16: sign 1, exponent 8 (bias 127), mantissa 7. */
+double orc_decode_bf16(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 0xFF;
+  int m = h & 0x7F;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -133); /* m * 2^(1-127-7) */
+  } else if (e == 255) {
+    v = (m == 0) ? INFINITY : NAN;
+  } else {
+    v = ldexp((double)(128 + m), e - 134); /* (1 + m/2^7) * 2^(e-127) */
+  }
+  return sign ? -v : v;
+}
+
+/* FP8 E4M3 in its finite-only form: sign 1, exponent 4 (bias 7), mantissa 3; no
+ * infinities; the only NaN codes are S.1111.111; largest finite value 448. */
+double orc_decode_e4m3(uint8_t b) {
+  int sign = (b >> 7) & 1;
+  int e = (b >> 3) & 0xF;
+  int m = b & 0x7;
+  double v;
+  if (e == 15 && m == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)m, -9); /* m * 2^(1-7-3) */
+  } else {
+    v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+  }
+  return sign ? -v : v;
+}
+
+/* Round a double to the nearest binary16 (ties to even) and return its bits.
+ * Written from the binary16 definition: quantum 2^-24 below 2^-14, otherwise
+ * 2^(e-10) for |v| in [2^e, 2^(e+1)); magnitudes that round past 65504 become inf. */
+uint16_t orc_encode_f16_rn(double v) {
+  uint16_t sign = (uint16_t)(signbit(v) ? 0x8000 : 0);
+  double a = fabs(v);
+  if (isnan(v)) return (uint16_t)(sign | 0x7E00);
+  if (isinf(a)) return (uint16_t)(sign | 0x7C00);
+  if (a < ldexp(1.0, -14)) {
+    double q = nearbyint(a / ldexp(1.0, -24)); /* exact division; ties to even */
+    return (uint16_t)(sign | (uint16_t)q);      /* q == 1024 encodes 2^-14 itself */
+  }
+  int e2;
+  (void)frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1) */
+  int e = e2 - 1;      /* a in [2^e, 2^(e+1)) */
+  double q = nearbyint(a / ldexp(1.0, e - 10));
+  if (q == 2048.0) { q = 1024.0; e += 1; }
+  if (e > 15) return (uint16_t)(sign | 0x7C00);
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)((int)q - 1024));
+}
+
+static double decode_in(int kind, const void* base, int64_t idx) {
+  switch (kind) {
+    case 0: return orc_decode_f16(((const uint16_t*)base)[idx]);
+    case 1: return orc_decode_bf16(((const uint16_t*)base)[idx]);
+    case 2: return orc_decode_e4m3(((const uint8_t*)base)[idx]);
+    default: return NAN;
+  }
+}
+
+/* ------------------------------------------------------------------ GEMM */
+
+/*
+ * D_ref[r][j] = alpha * sum_k dec(A[i][k]) * dec(B[k][j]) + beta * C[i][j],  i = rows[r]
+ *
+ * kind: 0 = FP16, 1 = BF16, 2 = FP8 E4M3 (unscaled).  A row-major M x K (lda),
+ * B row-major K x N (ldb), C FP32 row-major (ldc), not read when beta == 0.
+ * absab[r][j] = sum_k |dec A[i][k]| * |dec B[k][j]| (the tolerance scale).
+ * D_ref and absab are nrows x N, row-major, double.  Either output may be NULL.
+ */
+int orc_gemm(int kind, int M, int N, int K, double alpha, const void* A, int64_t lda,
+             const void* B, int64_t ldb, double beta, const float* C, int64_t ldc,
+             const int32_t* rows, int nrows, double* D_ref, double* absab) {
+  if (M < 0 || N < 0 || K < 0 || nrows < 0) return 1;
+  for (int r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= M) return 2;
+  if (beta != 0.0 && C == NULL) return 3;
+  /* decode B once: Bd[k][j] */
+  double* Bd = (double*)malloc(sizeof(double) * ((size_t)K * (size_t)N + 1));
+  if (!Bd) return 4;
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j) Bd[k * N + j] = decode_in(kind, B, k * ldb + j);
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    const int64_t i = rows[r];
+    double* acc = (double*)calloc((size_t)N + 1, sizeof(double));
+    double* aab = (double*)calloc((size_t)N + 1, sizeof(double));
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = decode_in(kind, A, i * lda + k);
+      const double* brow = Bd + k * N;
+      for (int64_t j = 0; j < N; ++j) {
+        acc[j] += a * brow[j];
+        aab[j] += fabs(a) * fabs(brow[j]);
+      }
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      double d = alpha * acc[j];
+      if (beta != 0.0) d += beta * (double)C[i * ldc + j];
+      if (D_ref) D_ref[(int64_t)r * N + j] = d;
+      if (absab) absab[(int64_t)r * N + j] = aab[j];
+    }
+    free(acc);
+    free(aab);
+  }
+  free(Bd);
+  return 0;
+}
+
+/*
+ * FP8 E4M3 GEMM with FP32 block scales, following the block structure:
+ *   D_ref[i][j] = alpha * sum_kb sA[i][kb] * sB[kb][j/128] * P_kb[i][j] + beta * C[i][j]
+ *   P_kb[i][j]  = sum_{k in [128 kb, min(128 kb + 128, K))} dec8(A[i][k]) * dec8(B[k][j])
+ * sA is M x ceil(K/128) (ld_sa), one scale per row and 128-wide K block;
+ * sB is ceil(K/128) x ceil(N/128) (ld_sb), one scale per 128 x 128 block of B.
+ * absab[i][j] = sum_k |dec8(A[i][k]) sA[i][k/128]| * |dec8(B[k][j]) sB[k/128][j/128]|.
+ */
+int orc_gemm_fp8_blockscaled(int M, int N, int K, double alpha, const uint8_t* A, int64_t lda,
+                             const float* sA, int64_t ld_sa, const uint8_t* B, int64_t ldb,
+                             const float* sB, int64_t ld_sb, double beta, const float* C,
+                             int64_t ldc, const int32_t* rows, int nrows, double* D_ref,
+                             double* absab) {
+  if (M < 0 || N < 0 || K < 0 || nrows < 0) return 1;
+  for (int r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= M) return 2;
+  if (beta != 0.0 && C == NULL) return 3;
+  const int64_t KB = ((int64_t)K + 127) / 128;
+  double* Bd = (double*)malloc(sizeof(double) * ((size_t)K * (size_t)N + 1));
+  if (!Bd) return 4;
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j) Bd[k * N + j] = orc_decode_e4m3(B[k * ldb + j]);
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    const int64_t i = rows[r];
+    double* acc = (double*)calloc((size_t)N + 1, sizeof(double));
+    double* part = (double*)calloc((size_t)N + 1, sizeof(double));
+    double* aab = (double*)calloc((size_t)N + 1, sizeof(double));
+    for (int64_t kb = 0; kb < KB; ++kb) {
+      const int64_t k_end = (kb + 1) * 128 < K ? (kb + 1) * 128 : K;
+      for (int64_t j = 0; j < N; ++j) part[j] = 0.0;
+      const double sa = (double)sA[i * ld_sa + kb];
+      for (int64_t k = kb * 128; k < k_end; ++k) {
+        const double a = orc_decode_e4m3(A[i * lda + k]);
+        const double* brow = Bd + k * N;
+        for (int64_t j = 0; j < N; ++j) {
+          part[j] += a * brow[j];
+          aab[j] += fabs(a * sa) * fabs(brow[j] * (double)sB[kb * ld_sb + j / 128]);
+        }
+      }
+      for (int64_t j = 0; j < N; ++j) acc[j] += sa * (double)sB[kb * ld_sb + j / 128] * part[j];
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      double d = alpha * acc[j];
+      if (beta != 0.0) d += beta * (double)C[i * ldc + j];
+      if (D_ref) D_ref[(int64_t)r * N + j] = d;
+      if (absab) absab[(int64_t)r * N + j] = aab[j];
+    }
+    free(acc);
+    free(part);
+    free(aab);
+  }
+  free(Bd);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ W8A8 GEMV */
+
+/*
+ * Batch-1 symmetric W8A8 linear layer (A100 page, sections 5.1 and 5.2):
+ *   z[o] = sum_k x[k] * W[o][k]                      (exact, int64; must fit INT32)
+ *   y[o] = fp16_rn( (float(z[o]) * s_x) * s_W[o] )    (two FP32 products, left to right)
+ * x int8 [K]; W int8 row-major qweight[N][ldw] (output channel o is row o); s_x is
+ * one FP32 scalar; s_W FP32 [N].  z (int64 [N]) and y (FP16 bits [N]) may be NULL.
+ * Returns 0, or 5 if some |z[o]| does not fit a signed 32-bit integer.
+ */
+int orc_gemv_w8a8(int N, int K, const int8_t* x, float s_x, const int8_t* W, int64_t ldw,
+                  const float* s_W, int64_t* z, uint16_t* y) {
+  if (N < 0 || K < 0) return 1;
+  int bad = 0;
+#pragma omp parallel for reduction(| : bad)
+  for (int o = 0; o < N; ++o) {
+    int64_t acc = 0;
+    for (int64_t k = 0; k < K; ++k) acc += (int64_t)x[k] * (int64_t)W[(int64_t)o * ldw + k];
+    if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;
+    if (z) z[o] = acc;
+    if (y) {
+      float f = (float)(int32_t)acc; /* int -> float, round to nearest even */
+      float t = f * s_x;             /* FP32 product, rounded */
+      float u = t * s_W[o];          /* FP32 product, rounded */
+      y[o] = orc_encode_f16_rn((double)u);
+    }
+  }
+  return bad ? 5 : 0;
+}

@@ -1,0 +1,166 @@
+"""Seeded synthetic inputs for the linear-layer hot path.
+
+This module only draws random inputs and lays them out in memory; it holds none
+of the method's arithmetic.  Both the CUDA path (tests, bench) and the CPU oracle
+consume exactly the bytes produced here.
+
+Generator: numpy ``default_rng(seed)`` (PCG64), values drawn in row-major order.
+Seeds: A = 1, B = 2, C = 3, scales = 4, x = 5, s_x = 6 (the GEMM seeds 1 and 2 are the ones
+the "Tensor Core" chapter's WMMA host harness uses for A and B).
+
+Distributions (the workload shapes of the pages' linear layer):
+
+* FP16 operands: U[-1, 1] in float64, rounded to FP16 (round to nearest even).
+* BF16 operands: N(0, 1) drawn in float32, rounded to BF16 (nearest even).
+* FP32 C: N(0, 1) in float32.
+* int8 activations and weights: integers uniform on [-127, 127] (so -128 never occurs).
+* FP32 scales: U(0.001, 0.02).
+* FP8 E4M3 operands: N(0, 1) in float32, one FP32 scale per block
+  s = amax(|block|) / 448 (s = 1 for an all-zero block), code = e4m3(x / s) rounded
+  to nearest even; blocks are 1 x 128 for A and 128 x 128 for B.  Turning the FP32
+  values into E4M3 bytes uses torch's float8_e4m3fn conversion.
+
+Leading dimensions larger than the row width leave padding columns; they are
+filled with a NaN code so that a kernel which reads padding poisons its result.
+"""
+import numpy as np
+
+SEED_A, SEED_B, SEED_C, SEED_SCALE, SEED_X, SEED_SX = 1, 2, 3, 4, 5, 6
+
+NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "e4m3": 0x7F}
+
+# The five workloads of the linear layer (named by what they are, with sizes).
+WORKLOADS = {
+    "f16_gemm_256": dict(op="gemm", kind="f16", M=256, N=256, K=256, alpha=1.0, beta=0.0,
+                         out="f32"),
+    "bf16_gemm_4096": dict(op="gemm", kind="bf16", M=4096, N=4096, K=4096, alpha=1.0, beta=1.0,
+                           out="bf16"),
+    "w8a8_gemv_4096x11008": dict(op="gemv", N=11008, K=4096),
+    "f16_gemm_4093x5003x2056": dict(op="gemm", kind="f16", M=4093, N=5003, K=2056, alpha=0.5,
+                                    beta=-1.25, out="f32"),
+    "e4m3_gemm_8192": dict(op="fp8", kind="e4m3", M=8192, N=8192, K=8192, alpha=1.0, beta=0.0,
+                           out="bf16"),
+}
+
+
+def _pad(vals, ld, fill, dtype):
+    rows, cols = vals.shape
+    if ld < cols:
+        raise ValueError("leading dimension smaller than the row width")
+    out = np.full((rows, ld), fill, dtype=dtype)
+    out[:, :cols] = vals
+    return out
+
+
+def f16_uniform(rows, cols, seed, ld=None):
+    """FP16 bits (uint16, rows x ld) of U[-1, 1] draws."""
+    ld = cols if ld is None else ld
+    v = np.random.default_rng(seed).uniform(-1.0, 1.0, size=(rows, cols))
+    bits = v.astype(np.float16).view(np.uint16)
+    return _pad(bits, ld, NAN_BITS["f16"], np.uint16)
+
+
+def bf16_normal(rows, cols, seed, ld=None):
+    """BF16 bits (uint16, rows x ld) of N(0, 1) draws."""
+    import torch
+    ld = cols if ld is None else ld
+    v = np.random.default_rng(seed).standard_normal(size=(rows, cols), dtype=np.float32)
+    bits = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return _pad(bits, ld, NAN_BITS["bf16"], np.uint16)
+
+
+def operand(kind, rows, cols, seed, ld=None):
+    if kind == "f16":
+        return f16_uniform(rows, cols, seed, ld)
+    if kind == "bf16":
+        return bf16_normal(rows, cols, seed, ld)
+    raise ValueError(kind)
+
+
+def f32_normal(rows, cols, seed, ld=None):
+    ld = cols if ld is None else ld
+    v = np.random.default_rng(seed).standard_normal(size=(rows, cols), dtype=np.float32)
+    return _pad(v, ld, np.float32(np.nan), np.float32)
+
+
+def int8_uniform(shape, seed):
+    return np.random.default_rng(seed).integers(-127, 128, size=shape, dtype=np.int8)
+
+
+def scales_uniform(n, seed, lo=0.001, hi=0.02):
+    return np.random.default_rng(seed).uniform(lo, hi, size=n).astype(np.float32)
+
+
+def _to_e4m3_bits(v32):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def e4m3_blockquant(rows, cols, seed, block_rows, block_cols, ld=None):
+    """Quantise N(0, 1) float32 draws to E4M3 per block of block_rows x block_cols.
+
+    Returns (codes uint8 rows x ld, scales float32 ceil(rows/br) x ceil(cols/bc)).
+    """
+    ld = cols if ld is None else ld
+    v = np.random.default_rng(seed).standard_normal(size=(rows, cols), dtype=np.float32)
+    nbr = -(-rows // block_rows)
+    nbc = -(-cols // block_cols)
+    scales = np.ones((nbr, nbc), dtype=np.float32)
+    q = np.empty((rows, cols), dtype=np.float32)
+    for bi in range(nbr):
+        r0, r1 = bi * block_rows, min(rows, (bi + 1) * block_rows)
+        blk = v[r0:r1]
+        for bj in range(nbc):
+            c0, c1 = bj * block_cols, min(cols, (bj + 1) * block_cols)
+            amax = np.float32(np.max(np.abs(blk[:, c0:c1]))) if (r1 > r0 and c1 > c0) else 0
+            s = np.float32(amax) / np.float32(448.0) if amax > 0 else np.float32(1.0)
+            scales[bi, bj] = s
+            q[r0:r1, c0:c1] = blk[:, c0:c1] / s
+    codes = _to_e4m3_bits(q)
+    return _pad(codes, ld, NAN_BITS["e4m3"], np.uint8), scales
+
+
+def e4m3_blockquant_rowblocks(rows, cols, seed, ld=None):
+    """A operand: 1 x 128 blocks (one scale per row and 128-wide K block)."""
+    ld = cols if ld is None else ld
+    v = np.random.default_rng(seed).standard_normal(size=(rows, cols), dtype=np.float32)
+    nbc = -(-cols // 128)
+    pad = nbc * 128 - cols
+    vp = np.pad(v, ((0, 0), (0, pad))) if pad else v
+    blocks = vp.reshape(rows, nbc, 128)
+    amax = np.max(np.abs(blocks), axis=2).astype(np.float32)
+    scales = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q = (blocks / scales[:, :, None]).reshape(rows, nbc * 128)[:, :cols]
+    codes = _to_e4m3_bits(q.astype(np.float32))
+    return _pad(codes, ld, NAN_BITS["e4m3"], np.uint8), scales
+
+
+def gemm_inputs(kind, M, N, K, beta, lda=None, ldb=None, ldc=None):
+    """Operands of a 16-bit GEMM workload: A (M x lda), B (K x ldb), C (M x ldc) or None."""
+    A = operand(kind, M, K, SEED_A, lda)
+    B = operand(kind, K, N, SEED_B, ldb)
+    C = f32_normal(M, N, SEED_C, ldc) if beta != 0.0 else None
+    return A, B, C
+
+
+def fp8_inputs(M, N, K, beta=0.0, lda=None, ldb=None, ldc=None):
+    """E4M3 operands with block scales: (A, sA, B, sB, C or None)."""
+    A, sA = e4m3_blockquant_rowblocks(M, K, SEED_A, lda)
+    B, sB = e4m3_blockquant(K, N, SEED_B, 128, 128, ldb)
+    C = f32_normal(M, N, SEED_C, ldc) if beta != 0.0 else None
+    return A, sA, B, sB, C
+
+
+def gemv_inputs(N, K, ldw=None):
+    """(x int8 [K], s_x float32 scalar, W int8 [N x ldw], s_W float32 [N])."""
+    ldw = K if ldw is None else ldw
+    x = int8_uniform(K, SEED_X)
+    s_x = scales_uniform(1, SEED_SX)[0]
+    W = int8_uniform((N, K), SEED_B)
+    if ldw != K:
+        Wp = np.full((N, ldw), 77, dtype=np.int8)  # padding a kernel must not read
+        Wp[:, :K] = W
+        W = Wp
+    s_W = scales_uniform(N, SEED_SCALE)
+    return x, s_x, W, s_W
