@@ -1,0 +1,188 @@
+/*
+ * linear_layer_gb300 -- C ABI of the GB300 (sm_103a) linear-layer hot path.
+ *
+ * The library computes, on one GPU, the tiled matrix multiply-accumulate
+ *
+ *     D = alpha * A x B + beta * C          (FP32 accumulation)
+ *
+ * for FP16, BF16 and block-scaled FP8 E4M3 inputs, and its batch-1 W8A8 special
+ * case (int8 x int8 -> int32, per-token x per-channel dequantisation to FP16).
+ *
+ * Conventions shared by every entry point
+ *   - All matrices are row-major.  A leading dimension (ld*) is the distance, in
+ *     ELEMENTS, between the starts of consecutive rows; ld >= the row width.
+ *   - Every pointer except the ones named "host" is caller-owned DEVICE memory on
+ *     the current CUDA device.  The library allocates no device memory per call;
+ *     its only device state is one status word per device (see ll_get_device_status).
+ *   - Every entry point is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  Argument errors are detected on the host and
+ *     returned before anything is launched; nothing is written in that case.
+ *   - Calls are deterministic: identical inputs give bit-identical outputs.
+ *   - A wait inside a kernel that exceeds its time limit does not hang the GPU: the
+ *     kernel records LL_ERR_DEVICE_TIMEOUT in the status word and exits.
+ *
+ * Scope: one GPU; no collective; no CPU fallback.
+ */
+#ifndef LINEAR_LAYER_GB300_LL_H
+#define LINEAR_LAYER_GB300_LL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the type behind cudaStream_t */
+typedef struct CUstream_st* ll_stream_t;
+
+typedef enum {
+  LL_OK = 0,
+  LL_ERR_INVALID_ARG = 1,    /* a size, leading dimension or pointer is invalid       */
+  LL_ERR_MISALIGNED = 2,     /* reserved: misaligned operands are repacked instead    */
+  LL_ERR_UNSUPPORTED = 3,    /* a valid request this build does not implement         */
+  LL_ERR_WORKSPACE = 4,      /* workspace too small for the operand repack it needs   */
+  LL_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed         */
+  LL_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait ran out (device status word)  */
+  LL_ERR_NO_DEVICE = 7       /* no sm_103 device is current                            */
+} ll_status;
+
+/* Element type of the A and B operands. */
+typedef enum { LL_IN_F16 = 0, LL_IN_BF16 = 1, LL_IN_E4M3 = 2 } ll_in_type;
+
+/* Element type of the output D. */
+typedef enum { LL_OUT_F32 = 0, LL_OUT_BF16 = 1, LL_OUT_F16 = 2 } ll_out_type;
+
+/* ------------------------------------------------------------------ dense GEMM */
+
+/*
+ * Bytes of workspace a GEMM with these sizes and leading dimensions needs
+ * (0 when both operands can be read in place).  An operand is read in place when
+ * its base pointer is 16-byte aligned and its row pitch (ld * element size) is a
+ * multiple of 16 bytes; otherwise the call first repacks it into the workspace
+ * (row pitch rounded up to 16 bytes) inside the same stream, and that copy is part
+ * of the call.  The figure assumes 16-byte-aligned base pointers; a misaligned base
+ * pointer is repacked too and needs at most ll_gemm_workspace_size(...,lda=1,ldb=1).
+ */
+size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int in_type);
+
+/*
+ * D = alpha * A x B + beta * C for FP16 (ll_gemm_f16) or BF16 (ll_gemm_bf16) A, B.
+ *
+ * Defined by: "Tensor Core" chapter (anrans ai-infra-handbooks), section
+ * "Tensor Core 做什么" (D = A x B + C, low-precision inputs) and table
+ * "精度：FP16、BF16、TF32、FP8" (FP16/BF16 inputs, FP32 accumulation), with the
+ * BLAS alpha/beta scaling.
+ *
+ *   A : M x K, lda >= K (FP16 or BF16)          B : K x N, ldb >= N (same type as A)
+ *   C : M x N FP32, ldc >= N; not read when beta == 0 (may then be NULL)
+ *   D : M x N, ldd >= N, element type d_type; D may alias C only when
+ *       d_type == LL_OUT_F32 and ldd == ldc (each element is read before it is written)
+ *   workspace : device scratch of ws_bytes (see ll_gemm_workspace_size); may be NULL if 0.
+ * Every product is accumulated in FP32 over the whole K; alpha * acc + beta * C is
+ * evaluated in FP32 and rounded once to d_type (round to nearest even).
+ * M == 0 or N == 0: nothing is done.  K == 0: D = beta * C (alpha is not used).
+ * Errors: LL_ERR_INVALID_ARG for negative sizes, ld < width, NULL operands, or
+ * beta != 0 with C == NULL; LL_ERR_WORKSPACE if a repack is needed and ws_bytes is
+ * smaller than ll_gemm_workspace_size; LL_ERR_CUDA if a launch fails.
+ */
+ll_status ll_gemm_f16(int M, int N, int K, float alpha, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+                      void* D, int64_t ldd, int d_type, void* workspace, size_t ws_bytes,
+                      ll_stream_t stream);
+ll_status ll_gemm_bf16(int M, int N, int K, float alpha, const void* A, int64_t lda,
+                       const void* B, int64_t ldb, float beta, const float* C, int64_t ldc,
+                       void* D, int64_t ldd, int d_type, void* workspace, size_t ws_bytes,
+                       ll_stream_t stream);
+
+/*
+ * FP8 E4M3 GEMM with FP32 block scales:
+ *
+ *   D[i][j] = alpha * sum_kb scale_a[i][kb] * scale_b[kb][j / 128]
+ *                          * sum_{k in block kb} A[i][k] * B[k][j]  + beta * C[i][j]
+ *
+ * Defined by: "Tensor Core" chapter, table "精度：FP16、BF16、TF32、FP8" and the text
+ * under it (FP8 E4M3 1/4/3; FP8 GEMMs need scaling factors per tensor, row or block;
+ * fine-grained block scaling as used for DeepSeek-V3 training).
+ *
+ *   A       : M x K E4M3 codes (1 byte), lda >= K
+ *   scale_a : M x ceil(K/128) FP32, ld_sa >= ceil(K/128); one scale per row and 128-wide K block
+ *   B       : K x N E4M3 codes, ldb >= N
+ *   scale_b : ceil(K/128) x ceil(N/128) FP32, ld_sb >= ceil(N/128); one per 128 x 128 block
+ *   C, D, workspace, stream: as for ll_gemm_f16.
+ * E4M3 is the finite-only form (bias 7, max 448, NaN = S.1111.111).  Each 128-K
+ * block is accumulated in FP32 by the tensor cores, then scaled by
+ * scale_a * scale_b and added into an FP32 accumulator (block-wise promotion).
+ * Errors: as for ll_gemm_f16; scale pointers must be non-NULL when M, N, K > 0.
+ */
+ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_t* A, int64_t lda,
+                                  const float* scale_a, int64_t ld_sa, const uint8_t* B,
+                                  int64_t ldb, const float* scale_b, int64_t ld_sb, float beta,
+                                  const float* C, int64_t ldc, void* D, int64_t ldd, int d_type,
+                                  void* workspace, size_t ws_bytes, ll_stream_t stream);
+
+/* ------------------------------------------------------------------ W8A8 GEMV */
+
+/*
+ * Batch-1 symmetric W8A8 linear layer:
+ *
+ *   z[o] = sum_k x[k] * W[o][k]                    (int32, exact)
+ *   y[o] = fp16_rn( (float(z[o]) * x_scale) * w_scale[o] )   (two FP32 products, in order)
+ *
+ * Defined by: "NVIDIA A100: chip to SIMT", section 5.1 (symmetric W8A8: per-token
+ * activation scale, per-output-channel weight scale, zero point 0, qweight[N,K]
+ * stored output-channel-major; integer dot product over the whole K into INT32,
+ * dequantised once in the epilogue) and section 5.2 (epilogue order).
+ *
+ *   x       : K int8 codes (the quantised activation of one token)
+ *   x_scale : device pointer to ONE FP32 value (per-token scale s_x)
+ *   W       : N x K int8, row o = output channel o, ldw >= K
+ *   w_scale : N FP32 per-output-channel scales
+ *   y       : N FP16 outputs (written)
+ *   z_out   : N int32 raw dot products (written when not NULL)
+ * |z| <= K * 128^2 must fit INT32, i.e. K <= 131071 (checked: LL_ERR_INVALID_ARG).
+ * N == 0: nothing is done.  K == 0: z = 0 and y = fp16(0 * s_x * s_W[o]).
+ * Errors: LL_ERR_INVALID_ARG for negative sizes, ldw < K or NULL pointers.
+ */
+ll_status ll_linear_w8a8_gemv(int N, int K, const int8_t* x, const float* x_scale,
+                              const int8_t* W, int64_t ldw, const float* w_scale, void* y,
+                              int32_t* z_out, ll_stream_t stream);
+
+/* ------------------------------------------------------------------ status */
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word.
+ * Returns LL_OK, LL_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out since the
+ * last call, or LL_ERR_CUDA if the synchronisation itself failed.
+ * `detail` (host, may be NULL) receives the raw word: bits 0-7 the status code,
+ * bits 8-15 the kernel role that gave up (1 producer, 2 MMA, 3 epilogue, 4 test wait).
+ */
+ll_status ll_get_device_status(ll_stream_t stream, uint32_t* detail);
+
+/*
+ * Set the time limit, in nanoseconds, of every bounded wait in this library's
+ * kernels on the current device (default 2e9 = 2 s).  Applies to kernels launched
+ * after this call returns (the limit travels with each launch as a parameter).
+ * Returns LL_ERR_INVALID_ARG for ns == 0.
+ */
+ll_status ll_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Launch one CTA that waits, with the bounded wait the GEMM kernels use, on an
+ * mbarrier phase that nothing completes.  The wait runs out after the configured
+ * limit, the kernel records LL_ERR_DEVICE_TIMEOUT (role 4) and returns.  Used to
+ * test failure detection without a GPU fault; the paper has no counterpart.
+ */
+ll_status ll_debug_timeout_probe(ll_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* ll_status_string(ll_status s);
+
+/* Library version string, e.g. "linear_layer_gb300 0.1 sm_103a". */
+const char* ll_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINEAR_LAYER_GB300_LL_H */

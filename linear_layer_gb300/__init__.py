@@ -1,0 +1,160 @@
+"""linear_layer_gb300: GB300 (sm_103a) linear-layer hot path behind a C ABI.
+
+This module is a thin ctypes binding over ``lib/liblinear_layer_gb300.so``: it
+turns torch tensors (or raw integer device pointers) into pointers and calls the
+C entry points declared in ``include/ll.h``.  Every step of the computation runs
+in the library's CUDA kernels; there is no Python or CPU fallback.  If the
+library has not been built, importing this package raises ImportError.
+
+Python name          C entry point
+------------------   -------------------------
+gemm_f16             ll_gemm_f16
+gemm_bf16            ll_gemm_bf16
+gemm_fp8_blockscaled ll_gemm_fp8_blockscaled
+linear_w8a8_gemv     ll_linear_w8a8_gemv
+gemm_workspace_size  ll_gemm_workspace_size
+get_device_status    ll_get_device_status
+set_wait_timeout_ns  ll_set_wait_timeout_ns
+debug_timeout_probe  ll_debug_timeout_probe
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "liblinear_layer_gb300.so")
+
+LL_OK, LL_ERR_INVALID_ARG, LL_ERR_MISALIGNED, LL_ERR_UNSUPPORTED = 0, 1, 2, 3
+LL_ERR_WORKSPACE, LL_ERR_CUDA, LL_ERR_DEVICE_TIMEOUT, LL_ERR_NO_DEVICE = 4, 5, 6, 7
+IN_F16, IN_BF16, IN_E4M3 = 0, 1, 2
+OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+
+# every symbol the header declares
+EXPORTS = ["ll_gemm_workspace_size", "ll_gemm_f16", "ll_gemm_bf16", "ll_gemm_fp8_blockscaled",
+           "ll_linear_w8a8_gemv", "ll_get_device_status", "ll_set_wait_timeout_ns",
+           "ll_debug_timeout_probe", "ll_status_string", "ll_version"]
+
+
+class LLError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("linear_layer_gb300: the CUDA library is not built (%s missing); "
+                          "run `python -m linear_layer_gb300.build`" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    L.ll_gemm_workspace_size.restype = ctypes.c_size_t
+    L.ll_gemm_workspace_size.argtypes = [i32, i32, i32, i64, i64, i32]
+    dense = [i32, i32, i32, f32, vp, i64, vp, i64, f32, vp, i64, vp, i64, i32, vp, ctypes.c_size_t, vp]
+    for name in ("ll_gemm_f16", "ll_gemm_bf16"):
+        getattr(L, name).restype = i32
+        getattr(L, name).argtypes = dense
+    L.ll_gemm_fp8_blockscaled.restype = i32
+    L.ll_gemm_fp8_blockscaled.argtypes = [i32, i32, i32, f32, vp, i64, vp, i64, vp, i64, vp, i64,
+                                          f32, vp, i64, vp, i64, i32, vp, ctypes.c_size_t, vp]
+    L.ll_linear_w8a8_gemv.restype = i32
+    L.ll_linear_w8a8_gemv.argtypes = [i32, i32, vp, vp, vp, i64, vp, vp, vp, vp]
+    L.ll_get_device_status.restype = i32
+    L.ll_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.ll_set_wait_timeout_ns.restype = i32
+    L.ll_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.ll_debug_timeout_probe.restype = i32
+    L.ll_debug_timeout_probe.argtypes = [vp]
+    L.ll_status_string.restype = ctypes.c_char_p
+    L.ll_status_string.argtypes = [i32]
+    L.ll_version.restype = ctypes.c_char_p
+    L.ll_version.argtypes = []
+    return L
+
+
+lib = _load()
+
+
+def status_string(status):
+    return lib.ll_status_string(int(status)).decode()
+
+
+def version():
+    return lib.ll_version().decode()
+
+
+def _p(x):
+    """Pointer of a torch tensor (data_ptr), an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status, where):
+    if status != LL_OK:
+        raise LLError(status, where)
+    return status
+
+
+def gemm_workspace_size(M, N, K, lda, ldb, in_type):
+    return lib.ll_gemm_workspace_size(M, N, K, lda, ldb, in_type)
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    if isinstance(workspace, tuple):
+        return workspace
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def gemm_f16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, workspace=None,
+             stream=None):
+    w, wb = _ws(workspace)
+    return _check(lib.ll_gemm_f16(M, N, K, alpha, _p(A), lda, _p(B), ldb, beta, _p(C), ldc, _p(D),
+                                  ldd, d_type, w, wb, _stream(stream)), "ll_gemm_f16")
+
+
+def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, workspace=None,
+              stream=None):
+    w, wb = _ws(workspace)
+    return _check(lib.ll_gemm_bf16(M, N, K, alpha, _p(A), lda, _p(B), ldb, beta, _p(C), ldc, _p(D),
+                                   ldd, d_type, w, wb, _stream(stream)), "ll_gemm_bf16")
+
+
+def gemm_fp8_blockscaled(M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb, scale_b, ld_sb, beta, C,
+                         ldc, D, ldd, d_type, workspace=None, stream=None):
+    w, wb = _ws(workspace)
+    return _check(lib.ll_gemm_fp8_blockscaled(M, N, K, alpha, _p(A), lda, _p(scale_a), ld_sa, _p(B),
+                                              ldb, _p(scale_b), ld_sb, beta, _p(C), ldc, _p(D), ldd,
+                                              d_type, w, wb, _stream(stream)),
+                  "ll_gemm_fp8_blockscaled")
+
+
+def linear_w8a8_gemv(N, K, x, x_scale, W, ldw, w_scale, y, z_out=None, stream=None):
+    return _check(lib.ll_linear_w8a8_gemv(N, K, _p(x), _p(x_scale), _p(W), ldw, _p(w_scale), _p(y),
+                                          _p(z_out), _stream(stream)), "ll_linear_w8a8_gemv")
+
+
+def get_device_status(stream=None):
+    """(status, raw word): synchronises the stream, reads and clears the status word."""
+    word = ctypes.c_uint32(0)
+    st = lib.ll_get_device_status(_stream(stream), ctypes.byref(word))
+    return st, word.value
+
+
+def set_wait_timeout_ns(ns):
+    return _check(lib.ll_set_wait_timeout_ns(int(ns)), "ll_set_wait_timeout_ns")
+
+
+def debug_timeout_probe(stream=None):
+    return _check(lib.ll_debug_timeout_probe(_stream(stream)), "ll_debug_timeout_probe")

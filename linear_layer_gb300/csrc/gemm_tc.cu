@@ -1,0 +1,515 @@
+// Dense GEMM on the 5th-generation tensor cores of sm_103a:
+//
+//   D = alpha * A x B + beta * C,   FP32 accumulation
+//
+// ("Tensor Core" chapter, section "Tensor Core 做什么" and table "精度": low-precision
+// inputs, FP32 accumulator; FP8 with per-block scaling factors.)
+//
+// One persistent CTA per SM walks a static list of 128 x BN output tiles in a
+// grouped (L2-friendly) order.  Warp roles:
+//   warp 0      TMA producer: A (128 x BK, K-major) and B (BK x BN, N-major) tiles,
+//               128-byte swizzle, into a STAGES-deep shared-memory ring (mbarrier
+//               full/empty pairs).  The K tail is zero-filled by TMA out-of-bounds fill.
+//   warp 1      TMEM allocator and MMA issuer: one thread issues tcgen05.mma
+//               (M = 128, N = BN) into a TMEM accumulator; tcgen05.commit releases
+//               smem stages and hands finished accumulators to the epilogue.
+//   warps 2..   epilogue.  16-bit inputs: 4 warps read the accumulator with
+//               tcgen05.ld while the next tile's MMAs run into the other of two TMEM
+//               accumulators, then apply alpha/beta, cast and store.
+//               FP8 inputs: 8 warps promote each 128-K block: the MMAs accumulate one
+//               block into a TMEM partial buffer (two, alternating), the warps read it
+//               and add scale_a[m][kb] * scale_b[kb][n/128] * partial into FP32
+//               registers; at the end of the tile they apply alpha/beta and store.
+// Every wait is bounded: on expiry the CTA records LL_ERR_DEVICE_TIMEOUT, drains the
+// copies and MMAs it has in flight, frees TMEM and exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ll {
+
+struct GemmParams {
+  int M, N, K;
+  float alpha, beta;
+  const float* C;
+  int64_t ldc;
+  void* D;
+  int64_t ldd;
+  int d_type;
+  int c_vec, d_vec;  // rows of C / D may be accessed with 16-byte vectors
+  const float* sA;
+  int64_t ld_sa;
+  const float* sB;
+  int64_t ld_sb;
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int group_m;
+};
+
+template <int BN_, bool FP8_>
+struct TileCfg {
+  static constexpr int BN = BN_;
+  static constexpr bool FP8 = FP8_;
+  static constexpr int BM = 128;
+  static constexpr int ELT = FP8 ? 1 : 2;
+  static constexpr int BK = 128 / ELT;        // K elements per stage: one 128-byte swizzle row
+  static constexpr int UMMA_K = 32 / ELT;     // K of one tcgen05.mma (32 bytes)
+  static constexpr int KSTEPS = BK / UMMA_K;  // MMAs per stage
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BOX_N = 128 / ELT;  // N elements in one 128-byte swizzle row
+  static constexpr int B_BOXES = BN / B_BOX_N;
+  static constexpr int B_BOX_BYTES = BK * 128;
+  static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) < 8 ? (196608 / STAGE_BYTES) : 8;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int EPI_WARPS = FP8 ? 8 : 4;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 256 + 1024;
+  static_assert(B_BOXES >= 1 && BN % B_BOX_N == 0, "tile N must cover whole swizzle rows");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                "TMEM allocation must be a power of two in [32, 512]");
+  static_assert(STAGES >= 2, "need at least two stages");
+};
+
+// tcgen05 instruction descriptor (kind::f16 / kind::f8f6f4): D = F32 (bits 4-5 = 1),
+// A/B format (bits 7-9 / 10-12), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
+// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_fmt, int n, int m) {
+  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | (1u << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mb,
+                                            int& nb) {
+  const int span = group_m * num_n;
+  const int g = t / span;
+  const int first_m = g * group_m;
+  const int gsz = min(num_m - first_m, group_m);
+  const int r = t - g * span;
+  mb = first_m + r % gsz;
+  nb = r / gsz;
+}
+
+// Epilogue of 32 consecutive columns of one output row: D = alpha * v + beta * C.
+__device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n, const float* v) {
+  if (m >= p.M) return;
+  const bool full = (n + 32 <= p.N);
+  float o[32];
+  if (p.beta != 0.0f) {
+    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
+    if (full && p.c_vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(crow + j);
+        o[j + 0] = p.alpha * v[j + 0] + p.beta * c4.x;
+        o[j + 1] = p.alpha * v[j + 1] + p.beta * c4.y;
+        o[j + 2] = p.alpha * v[j + 2] + p.beta * c4.z;
+        o[j + 3] = p.alpha * v[j + 3] + p.beta * c4.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = (n + j < p.N) ? p.alpha * v[j] + p.beta * crow[j] : 0.0f;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = p.alpha * v[j];
+  }
+  if (p.d_type == LL_OUT_F32) {
+    float* drow = static_cast<float*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
+    if (full && p.d_vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(drow + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < p.N) drow[j] = o[j];
+    }
+  } else if (p.d_type == LL_OUT_BF16) {
+    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
+    if (full && p.d_vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        uint4 u;
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(o[j + 0], o[j + 1]);
+        __nv_bfloat162 h1 = __floats2bfloat162_rn(o[j + 2], o[j + 3]);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(o[j + 4], o[j + 5]);
+        __nv_bfloat162 h3 = __floats2bfloat162_rn(o[j + 6], o[j + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&h0);
+        u.y = *reinterpret_cast<uint32_t*>(&h1);
+        u.z = *reinterpret_cast<uint32_t*>(&h2);
+        u.w = *reinterpret_cast<uint32_t*>(&h3);
+        *reinterpret_cast<uint4*>(drow + j) = u;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < p.N) drow[j] = __float2bfloat16_rn(o[j]);
+    }
+  } else {
+    __half* drow = static_cast<__half*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
+    if (full && p.d_vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        uint4 u;
+        __half2 h0 = __floats2half2_rn(o[j + 0], o[j + 1]);
+        __half2 h1 = __floats2half2_rn(o[j + 2], o[j + 3]);
+        __half2 h2 = __floats2half2_rn(o[j + 4], o[j + 5]);
+        __half2 h3 = __floats2half2_rn(o[j + 6], o[j + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&h0);
+        u.y = *reinterpret_cast<uint32_t*>(&h1);
+        u.z = *reinterpret_cast<uint32_t*>(&h2);
+        u.w = *reinterpret_cast<uint32_t*>(&h3);
+        *reinterpret_cast<uint4*>(drow + j) = u;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < p.N) drow[j] = __float2half_rn(o[j]);
+    }
+  }
+}
+
+template <class Cfg, uint32_t AB_FMT>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  constexpr int S = Cfg::STAGES;
+  constexpr int BN = Cfg::BN;
+  constexpr uint32_t IDESC = make_idesc(AB_FMT, BN, 128);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return smem_addr(bars + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + S + s); };
+  auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * S + b); };
+  auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * S + 2 + b); };
+  const uint32_t drain_bar = smem_addr(bars + 2 * S + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), Cfg::EPI_THREADS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  WaitCtx wctx{p.status, p.timeout_ns, abort_flag};
+  const int num_m = (p.M + 127) / 128;
+  const int num_n = (p.N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, num_m, num_n, p.group_m, mb, nb);
+        for (int kb = 0; kb < KB; ++kb) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, wctx, kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a_s = smem + s * Cfg::STAGE_BYTES;
+          uint8_t* b_s = a_s + Cfg::A_BYTES;
+          mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
+          tma_load_2d(smem_addr(a_s), &tmA, full_bar(s), kb * Cfg::BK, mb * 128);
+#pragma unroll
+          for (int j = 0; j < Cfg::B_BOXES; ++j)
+            tma_load_2d(smem_addr(b_s + j * Cfg::B_BOX_BYTES), &tmB, full_bar(s),
+                        nb * BN + j * Cfg::B_BOX_N, kb * Cfg::BK);
+          ++it;
+        }
+      }
+      if (!ok) {
+        // wait for the copies still in flight before the CTA can exit
+        for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0u); j < it; ++j)
+          wait_drain(full_bar(j % S), (j / S) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        uint32_t d_tmem = 0;
+        if (!Cfg::FP8) {
+          const uint32_t ab = acc_it & 1u;
+          if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          d_tmem = tmem_base + ab * BN;
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+          if (Cfg::FP8) {  // one TMEM partial buffer per 128-K block, alternating
+            const uint32_t pb = acc_it & 1u;
+            if (!wait_bounded(tempty_bar(pb), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + pb * BN;
+          }
+          const int s = it % S;
+          if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_addr(smem + s * Cfg::STAGE_BYTES);
+          const uint32_t b_base = a_base + Cfg::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc =
+                smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BOX_BYTES, 1024);
+            const uint32_t accum = Cfg::FP8 ? (kk > 0) : (kb > 0 || kk > 0);
+            if (Cfg::FP8)
+              mma_f8(d_tmem, adesc, bdesc, IDESC, accum);
+            else
+              mma_f16(d_tmem, adesc, bdesc, IDESC, accum);
+          }
+          mma_commit(empty_bar(s));
+          ++it;
+          if (Cfg::FP8) {
+            mma_commit(tfull_bar(acc_it & 1u));
+            ++acc_it;
+          }
+        }
+        if (!ok) break;
+        if (!Cfg::FP8) {
+          mma_commit(tfull_bar(acc_it & 1u));
+          ++acc_it;
+        }
+      }
+      // every MMA issued by this thread must finish before TMEM is freed
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0u, p.timeout_ns);
+    }
+  } else if (!Cfg::FP8) {
+    // ---------------------------------------------------------------- epilogue (16-bit)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc_it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, num_m, num_n, p.group_m, mb, nb);
+      const uint32_t ab = acc_it & 1u;
+      bool ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int m = mb * 128 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        store_chunk32(p, m, nb * BN + c * 32, v);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(ab));
+      ++acc_it;
+    }
+  } else {
+    // ---------------------------------------------------------------- promotion + epilogue (FP8)
+    constexpr int HALF = BN / 2;  // columns per thread
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int h = ew >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t pit = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, num_m, num_n, p.group_m, mb, nb);
+      const int m = mb * 128 + q * 32 + lane;
+      const bool row_ok = m < p.M;
+      const int ncol0 = nb * BN + h * HALF;
+      const bool col_ok = ncol0 < p.N;
+      const int nblk = ncol0 / 128;
+      const float* sa_row = p.sA + static_cast<int64_t>(row_ok ? m : 0) * p.ld_sa;
+      float acc[HALF];
+#pragma unroll
+      for (int j = 0; j < HALF; ++j) acc[j] = 0.0f;
+      float sa_next = row_ok ? sa_row[0] : 0.0f;
+      float sb_next = col_ok ? p.sB[nblk] : 0.0f;
+      for (int kb = 0; kb < KB; ++kb) {
+        const float s = sa_next * sb_next;
+        if (kb + 1 < KB) {
+          sa_next = row_ok ? sa_row[kb + 1] : 0.0f;
+          sb_next = col_ok ? p.sB[static_cast<int64_t>(kb + 1) * p.ld_sb + nblk] : 0.0f;
+        }
+        const uint32_t pb = pit & 1u;
+        bool w = wait_bounded(tfull_bar(pb), (pit >> 1) & 1u, wctx, kRoleEpilogue);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_x32(tmem_base + lane_base + pb * BN + h * HALF + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), s, acc[c * 32 + j]);
+        }
+        tc_fence_before();
+        mbar_arrive(tempty_bar(pb));
+        ++pit;
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int c = 0; c < HALF / 32; ++c) store_chunk32(p, m, ncol0 + c * 32, acc + c * 32);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D row-major matrix rows x cols (pitch in elements) with a box of box_cols x box_rows.
+static bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
+                     int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch * esize)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <class Cfg, uint32_t AB_FMT>
+static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
+  auto kern = gemm_tc_kernel<Cfg, AB_FMT>;
+  // the attribute is per device; setting it on every call is cheap and always correct
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+      cudaSuccess)
+    return LL_ERR_CUDA;
+  const CUtensorMapDataType dt =
+      Cfg::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+               : (AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
+  if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
+
+  GemmParams p;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.D = a.D;
+  p.ldd = a.ldd;
+  p.d_type = a.d_type;
+  const int dsize = a.d_type == LL_OUT_F32 ? 4 : 2;
+  p.c_vec = a.C != nullptr && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * 4) % 16 == 0);
+  p.d_vec = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * dsize) % 16 == 0);
+  p.sA = a.scale_a;
+  p.ld_sa = a.ld_sa;
+  p.sB = a.scale_b;
+  p.ld_sb = a.ld_sb;
+  p.status = ctx.status;
+  p.timeout_ns = ctx.timeout_ns;
+  p.group_m = 8;
+
+  const int num_tiles = ((a.M + 127) / 128) * ((a.N + Cfg::BN - 1) / Cfg::BN);
+  const int grid = num_tiles < ctx.num_sms ? num_tiles : ctx.num_sms;
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM, ctx.stream>>>(tmA, tmB, p);
+  return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
+  const int tiles_m = (a.M + 127) / 128;
+  auto tiles = [&](int bn) { return tiles_m * ((a.N + bn - 1) / bn); };
+  if (a.in_type == LL_IN_E4M3) {
+    if (tiles(256) >= ctx.num_sms || a.N > 128) return run<TileCfg<256, true>, 0>(a, ctx);
+    return run<TileCfg<128, true>, 0>(a, ctx);
+  }
+  const bool bf = a.in_type == LL_IN_BF16;
+  int bn = 64;
+  if (tiles(256) >= ctx.num_sms)
+    bn = 256;
+  else if (tiles(128) >= ctx.num_sms)
+    bn = 128;
+  if (bn == 256) return bf ? run<TileCfg<256, false>, 1>(a, ctx) : run<TileCfg<256, false>, 0>(a, ctx);
+  if (bn == 128) return bf ? run<TileCfg<128, false>, 1>(a, ctx) : run<TileCfg<128, false>, 0>(a, ctx);
+  return bf ? run<TileCfg<64, false>, 1>(a, ctx) : run<TileCfg<64, false>, 0>(a, ctx);
+}
+
+}  // namespace ll

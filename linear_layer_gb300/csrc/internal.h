@@ -1,0 +1,55 @@
+// Host-side interfaces shared between the C ABI (abi.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ll.h"
+
+namespace ll {
+
+// Per-call context the ABI hands to every launcher.
+struct LaunchCtx {
+  cudaStream_t stream;
+  uint32_t* status;     // device status word of the current device
+  uint64_t timeout_ns;  // limit of one bounded wait
+  int num_sms;          // SM count of the current device
+};
+
+struct GemmArgs {
+  int in_type;  // ll_in_type
+  int M, N, K;
+  float alpha, beta;
+  const void* A;
+  int64_t lda;  // operand pitches as the kernel reads them (after any repack)
+  const void* B;
+  int64_t ldb;
+  const float* C;
+  int64_t ldc;
+  void* D;
+  int64_t ldd;
+  int d_type;  // ll_out_type
+  const float* scale_a;
+  int64_t ld_sa;
+  const float* scale_b;
+  int64_t ld_sb;
+};
+
+// tcgen05 GEMM (gemm_tc.cu).  Requires A, B 16-byte aligned with 16-byte-multiple pitches.
+ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx);
+
+// D = beta * C (or 0) for K == 0 (aux.cu).
+ll_status launch_scale_c(const GemmArgs& a, const LaunchCtx& ctx);
+
+// Row-pitch repack of a rows x cols matrix of esize-byte elements (aux.cu).
+ll_status launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int rows,
+                        int cols, int esize, const LaunchCtx& ctx);
+
+// Bounded-wait probe (aux.cu).
+ll_status launch_timeout_probe(const LaunchCtx& ctx);
+
+// W8A8 GEMV (gemv_w8a8.cu).
+ll_status launch_gemv_w8a8(int N, int K, const int8_t* x, const float* x_scale, const int8_t* W,
+                           int64_t ldw, const float* w_scale, void* y, int32_t* z_out,
+                           const LaunchCtx& ctx);
+
+}  // namespace ll

@@ -1,0 +1,175 @@
+"""GPU parity of the FP16 / BF16 tcgen05 GEMM against the CPU oracle, through the C ABI.
+
+Small cases are compared on every element; the full-size workloads (BF16 4096^3 and
+the ragged FP16 4093 x 5003 x 2056 with tight leading dimensions) on sampled rows
+that cover the first and last rows of tiles and the M tail, in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import check_close, out_code, out_tensor, up
+
+pytestmark = pytest.mark.gpu
+
+
+def _dec_out(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_gemm(orc, kind, M, N, K, alpha, beta, out, lda=None, ldb=None, ldc=None, ldd=None,
+             rows=None, seed_shift=0, A=None, B=None, C=None, workspace=True):
+    import linear_layer_gb300 as ll
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    ldd = N if ldd is None else ldd
+    if A is None:
+        A = wl.operand(kind, M, K, wl.SEED_A + seed_shift, ld=lda)
+        B = wl.operand(kind, K, N, wl.SEED_B + seed_shift, ld=ldb)
+        C = wl.f32_normal(M, N, wl.SEED_C + seed_shift, ld=ldc) if beta != 0.0 else None
+    tA, tB, tC = up(A), up(B), up(C)
+    tD = out_tensor(M, ldd, out)
+    in_type = ll.IN_F16 if kind == "f16" else ll.IN_BF16
+    ws = None
+    need = ll.gemm_workspace_size(M, N, K, lda, ldb, in_type)
+    if need and workspace:
+        ws = torch.empty(need, dtype=torch.uint8, device=tA.device)
+    fn = ll.gemm_f16 if kind == "f16" else ll.gemm_bf16
+    fn(M, N, K, alpha, tA, lda, tB, ldb, beta, tC, ldc, tD, ldd, out_code(out), workspace=ws)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, "device status %s (word %#x)" % (ll.status_string(st), word)
+    D = _dec_out(tD)
+    if rows is None:
+        rows = np.arange(M)
+    ref, absab = orc.gemm(kind, M, N, K, alpha, A.ravel(), lda, B.ravel(), ldb, beta,
+                          None if C is None else C.ravel(), ldc, rows=rows)
+    check_close(D[rows, :N], ref, absab, K, out, kind, what="%s %dx%dx%d" % (kind, M, N, K))
+    if ldd > N:  # padding columns of D are never written
+        assert torch.isnan(tD[:, N:].float()).all()
+    return D
+
+
+def test_f16_256_cube_f32_out(orc):
+    """The FP16 256^3 workload: C not read (beta = 0), FP32 output."""
+    cfg = wl.WORKLOADS["f16_gemm_256"]
+    run_gemm(orc, "f16", cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"], cfg["out"])
+
+
+@pytest.mark.parametrize("kind", ["f16", "bf16"])
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
+def test_small_tails_all_outputs(orc, kind, out):
+    # several tiles in M and N, ragged M / N / K tails, beta != 0
+    run_gemm(orc, kind, 300, 520, 200, 0.75, -0.5, out)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 1, 16), (5, 7, 3), (129, 65, 64), (128, 256, 65),
+                                   (64, 1000, 8), (700, 300, 1)])
+def test_odd_shapes(orc, M, N, K):
+    run_gemm(orc, "bf16", M, N, K, 1.0, 1.0, "f32")
+
+
+def test_many_tiles_every_bn(orc):
+    # shapes that pick the 64-, 128- and 256-wide tile variants
+    for (M, N) in [(256, 256), (2048, 1280), (4096, 2304)]:
+        run_gemm(orc, "f16", M, N, 128, 1.0, 0.0, "f32", rows=[0, 127, 128, M - 1])
+
+
+def test_padded_leading_dims(orc):
+    run_gemm(orc, "f16", 200, 300, 136, 1.5, 0.25, "f32", lda=152, ldb=328, ldc=301, ldd=310)
+
+
+def test_unaligned_pitch_needs_workspace(orc):
+    import linear_layer_gb300 as ll
+    with pytest.raises(ll.LLError) as e:
+        run_gemm(orc, "f16", 64, 77, 40, 1.0, 0.0, "f32", ldb=77, workspace=False)
+    assert e.value.status == ll.LL_ERR_WORKSPACE
+    run_gemm(orc, "f16", 64, 77, 40, 1.0, 0.0, "f32", lda=41, ldb=77)
+
+
+def test_k_zero_is_beta_c(orc):
+    run_gemm(orc, "bf16", 70, 90, 0, 2.0, -1.25, "f32")
+    run_gemm(orc, "bf16", 70, 90, 0, 2.0, 0.0, "bf16")
+
+
+def test_in_place_c_equals_d(orc):
+    import linear_layer_gb300 as ll
+    M, N, K = 130, 144, 72  # 16-byte row pitches: read in place, no workspace
+    A = wl.operand("f16", M, K, 7)
+    B = wl.operand("f16", K, N, 8)
+    C = wl.f32_normal(M, N, 9)
+    tC = up(C)
+    ll.gemm_f16(M, N, K, 1.0, up(A), K, up(B), N, 2.0, tC, N, tC, N, ll.OUT_F32)
+    ref, absab = orc.gemm("f16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, 2.0, C.ravel(), N)
+    check_close(tC.cpu().numpy(), ref, absab, K, "f32", "f16", "in place")
+
+
+def test_deterministic(orc):
+    import linear_layer_gb300 as ll
+    M, N, K = 512, 768, 512
+    A, B, C = wl.gemm_inputs("bf16", M, N, K, 1.0)
+    tA, tB, tC = up(A), up(B), up(C)
+    outs = []
+    for _ in range(3):
+        tD = out_tensor(M, N, "bf16")
+        ll.gemm_bf16(M, N, K, 1.0, tA, K, tB, N, 1.0, tC, N, tD, N, ll.OUT_BF16)
+        outs.append(tD.view(torch.int16).cpu().numpy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_invalid_args_rejected_before_launch():
+    import linear_layer_gb300 as ll
+    t = torch.zeros(64, dtype=torch.float16, device="cuda")
+    D = torch.zeros(64, dtype=torch.float32, device="cuda")
+    cases = [
+        dict(M=-1, N=4, K=4, lda=4, ldb=4, C=None, beta=0.0, ldd=4),
+        dict(M=4, N=4, K=4, lda=3, ldb=4, C=None, beta=0.0, ldd=4),
+        dict(M=4, N=4, K=4, lda=4, ldb=4, C=None, beta=1.0, ldd=4),
+        dict(M=4, N=4, K=4, lda=4, ldb=4, C=None, beta=0.0, ldd=3),
+    ]
+    for c in cases:
+        with pytest.raises(ll.LLError) as e:
+            ll.gemm_f16(c["M"], c["N"], c["K"], 1.0, t, c["lda"], t, c["ldb"], c["beta"], c["C"], 4,
+                        D, c["ldd"], ll.OUT_F32)
+        assert e.value.status == ll.LL_ERR_INVALID_ARG
+    # M == 0 / N == 0 are no-ops
+    ll.gemm_f16(0, 4, 4, 1.0, t, 4, t, 4, 0.0, None, 4, D, 4, ll.OUT_F32)
+    ll.gemm_f16(4, 0, 4, 1.0, t, 4, t, 4, 0.0, None, 4, D, 4, ll.OUT_F32)
+
+
+def _sample_rows(M, extra, seed):
+    rng = np.random.default_rng(seed)
+    base = {0, 1, 127, 128, 255, 256, M // 2, M - 2, M - 1}
+    base |= set(int(r) for r in rng.integers(0, M, extra))
+    return np.array(sorted(r for r in base if 0 <= r < M))
+
+
+def test_bf16_4096_full_size_sampled(orc):
+    cfg = wl.WORKLOADS["bf16_gemm_4096"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    run_gemm(orc, "bf16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"],
+             rows=_sample_rows(M, 12, 17))
+
+
+def test_bf16_4096_fp32_output_strict_bar(orc):
+    # the same workload and kernel with an FP32 epilogue: the 1e-3 Frobenius bar
+    # applies to the accumulator before any cast, with no allowance for it
+    cfg = wl.WORKLOADS["bf16_gemm_4096"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    run_gemm(orc, "bf16", M, N, K, cfg["alpha"], cfg["beta"], "f32", rows=_sample_rows(M, 6, 31))
+
+
+def test_f16_ragged_tight_lds_full_size_sampled(orc):
+    cfg = wl.WORKLOADS["f16_gemm_4093x5003x2056"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    run_gemm(orc, "f16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"],
+             rows=_sample_rows(M, 12, 19))
+
+
+def test_f16_ragged_padded_lds_sampled(orc):
+    cfg = wl.WORKLOADS["f16_gemm_4093x5003x2056"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    run_gemm(orc, "f16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"], lda=2064, ldb=5008,
+             ldc=5008, ldd=5008, rows=_sample_rows(M, 6, 23))
