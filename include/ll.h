@@ -121,6 +121,35 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
                                   const float* C, int64_t ldc, void* D, int64_t ldd, int d_type,
                                   void* workspace, size_t ws_bytes, ll_stream_t stream);
 
+/*
+ * ll_gemm_f16 for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this entry point exists for integration, not for the method.
+ *
+ * Some callers cannot provide the workspace ll_gemm_f16 needs for an operand whose
+ * row pitch or base address is not a multiple of 16 bytes: code that runs while a
+ * stream is being captured into a CUDA graph (cudaMalloc is not allowed there), code
+ * in a host callback, or a runtime whose allocator owns all device memory.  This
+ * variant takes the same arguments minus the workspace and repacks such operands
+ * into a fixed scratch array inside the library: 16 MiB of device memory that every
+ * GPU which loads the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   - Limit: the repacked operands must fit the 16 MiB scratch, i.e.
+ *     (A repacked ? roundup(M * roundup(K, 8) * 2, 256) : 0)
+ *       + (B repacked ? K * roundup(N, 8) * 2 : 0)  <=  16 MiB;
+ *     larger requests return LL_ERR_WORKSPACE before anything is launched.
+ *     Operands that are already 16-byte aligned use no scratch and have no limit.
+ *   - The first call on a device that needs the scratch looks up its device address
+ *     (once per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one scratch array and overwrites what it reads, so calls
+ *     that overlap on the GPU (different streams, concurrent graph replays) race:
+ *     serialise them.
+ * Results equal those of ll_gemm_f16 with workspace; errors as for ll_gemm_f16.
+ */
+ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const void* A, int64_t lda,
+                              const void* B, int64_t ldb, float beta, const float* C,
+                              int64_t ldc, void* D, int64_t ldd, int d_type, ll_stream_t stream);
+
 /* ------------------------------------------------------------------ W8A8 GEMV */
 
 /*

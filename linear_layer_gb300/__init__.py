@@ -12,6 +12,7 @@ gemm_f16             ll_gemm_f16
 gemm_bf16            ll_gemm_bf16
 gemm_fp8_blockscaled ll_gemm_fp8_blockscaled
 linear_w8a8_gemv     ll_linear_w8a8_gemv
+gemm_f16_noalloc     ll_gemm_f16_noalloc
 gemm_workspace_size  ll_gemm_workspace_size
 get_device_status    ll_get_device_status
 set_wait_timeout_ns  ll_set_wait_timeout_ns
@@ -30,6 +31,7 @@ OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 
 # every symbol the header declares
 EXPORTS = ["ll_gemm_workspace_size", "ll_gemm_f16", "ll_gemm_bf16", "ll_gemm_fp8_blockscaled",
+           "ll_gemm_f16_noalloc",
            "ll_linear_w8a8_gemv", "ll_get_device_status", "ll_set_wait_timeout_ns",
            "ll_debug_timeout_probe", "ll_status_string", "ll_version"]
 
@@ -52,6 +54,8 @@ def _load():
     for name in ("ll_gemm_f16", "ll_gemm_bf16"):
         getattr(L, name).restype = i32
         getattr(L, name).argtypes = dense
+    L.ll_gemm_f16_noalloc.restype = i32
+    L.ll_gemm_f16_noalloc.argtypes = dense[:14] + [vp]
     L.ll_gemm_fp8_blockscaled.restype = i32
     L.ll_gemm_fp8_blockscaled.argtypes = [i32, i32, i32, f32, vp, i64, vp, i64, vp, i64, vp, i64,
                                           f32, vp, i64, vp, i64, i32, vp, ctypes.c_size_t, vp]
@@ -129,6 +133,15 @@ def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, work
     w, wb = _ws(workspace)
     return _check(lib.ll_gemm_bf16(M, N, K, alpha, _p(A), lda, _p(B), ldb, beta, _p(C), ldc, _p(D),
                                    ldd, d_type, w, wb, _stream(stream)), "ll_gemm_bf16")
+
+
+def gemm_f16_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, stream=None):
+    """ll_gemm_f16 without workspace: unaligned operands are repacked into the library's
+    fixed 16 MiB device scratch (for callers that cannot allocate; calls must not
+    overlap on the GPU)."""
+    return _check(lib.ll_gemm_f16_noalloc(M, N, K, alpha, _p(A), lda, _p(B), ldb, beta, _p(C), ldc,
+                                          _p(D), ldd, d_type, _stream(stream)),
+                  "ll_gemm_f16_noalloc")
 
 
 def gemm_fp8_blockscaled(M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb, scale_b, ld_sb, beta, C,

@@ -126,6 +126,10 @@ ll_status gemm_common(ll::GemmArgs a, void* workspace, size_t ws_bytes, ll_strea
 
 }  // namespace
 
+ll_status ll::current_launch_ctx(ll_stream_t stream, ll::LaunchCtx& ctx) {
+  return current_ctx(stream, ctx);
+}
+
 extern "C" {
 
 size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int in_type) {

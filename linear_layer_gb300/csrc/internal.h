@@ -34,6 +34,10 @@ struct GemmArgs {
   int64_t ld_sb;
 };
 
+// Launch context of the current device (status word, SM count, wait limit) for `stream`;
+// LL_ERR_NO_DEVICE unless an sm_103 device is current (abi.cu).
+ll_status current_launch_ctx(ll_stream_t stream, LaunchCtx& ctx);
+
 // tcgen05 GEMM (gemm_tc.cu).  Requires A, B 16-byte aligned with 16-byte-multiple pitches.
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx);
 
