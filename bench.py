@@ -480,11 +480,15 @@ def oracle_sample(target_s, min_rows=1):
 
 
 def cpu_baseline(target_s=12.0):
-    rows, _, cores, (M, N, K), secs = oracle_sample(target_s)
-    tflops = 2.0 * rows * N * K / secs / 1e12
+    rows, run, cores, (M, N, K), secs = oracle_sample(target_s)
+    reps = 1
+    if rows >= M and secs < 0.8 * target_s:  # the whole workload is shorter: repeat it
+        reps = max(1, int(math.ceil(target_s / max(secs, 1e-3))))
+        secs = sum(run(rows) for _ in range(reps))
+    tflops = 2.0 * rows * N * K * reps / secs / 1e12
     return {"value": tflops, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-            "sample": "%d of %d rows of the BF16 %dx%dx%d GEMM (double accumulation), %.1f s" % (
-                rows, M, M, N, K, secs)}
+            "sample": "%d x %d of %d rows of the BF16 %dx%dx%d GEMM (double accumulation), %.1f s" % (
+                reps, rows, M, M, N, K, secs)}
 
 
 def run_reference(args):

@@ -11,18 +11,26 @@
 
 namespace ll {
 
+// Each thread writes one 16-byte vector of a destination row (the destination pitch is a
+// multiple of 16 bytes); columns past `cols` are the pad and are written as zero.
 template <class T>
 __global__ void repack_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst,
                               int64_t ld_dst, int rows, int cols) {
-  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
-    const T* s = src + static_cast<int64_t>(r) * ld_src;
-    T* d = dst + static_cast<int64_t>(r) * ld_dst;
-    for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < cols; c += gridDim.x * blockDim.x)
-      d[c] = s[c];
-    // zero the pad so that the repacked pitch never exposes stale bytes
-    for (int64_t c = cols + blockIdx.x * blockDim.x + threadIdx.x; c < ld_dst;
-         c += static_cast<int64_t>(gridDim.x) * blockDim.x)
-      d[c] = T(0);
+  constexpr int V = 16 / sizeof(T);
+  const int64_t vec_per_row = ld_dst / V;
+  const int64_t total = static_cast<int64_t>(rows) * vec_per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / vec_per_row;
+    const int64_t c0 = (i - r * vec_per_row) * V;
+    const T* s = src + r * ld_src + c0;
+    union {
+      T e[V];
+      uint4 u;
+    } buf;
+#pragma unroll
+    for (int v = 0; v < V; ++v) buf.e[v] = (c0 + v < cols) ? s[v] : T(0);
+    *reinterpret_cast<uint4*>(dst + r * ld_dst + c0) = buf.u;
   }
 }
 
@@ -30,15 +38,14 @@ ll_status launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_d
                         int cols, int esize, const LaunchCtx& ctx) {
   if (rows <= 0 || cols <= 0) return LL_OK;
   const int threads = 256;
-  int gx = (cols + threads - 1) / threads;
-  if (gx > 64) gx = 64;
-  const int gy = rows < 65535 ? rows : 65535;
-  dim3 grid(gx, gy);
+  const int64_t vecs = static_cast<int64_t>(rows) * (ld_dst * esize / 16);
+  int64_t blocks = (vecs + threads - 1) / threads;
+  if (blocks > 16 * ctx.num_sms) blocks = 16 * ctx.num_sms;
   if (esize == 2)
-    repack_kernel<uint16_t><<<grid, threads, 0, ctx.stream>>>(
+    repack_kernel<uint16_t><<<static_cast<int>(blocks), threads, 0, ctx.stream>>>(
         static_cast<const uint16_t*>(src), ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
   else
-    repack_kernel<uint8_t><<<grid, threads, 0, ctx.stream>>>(
+    repack_kernel<uint8_t><<<static_cast<int>(blocks), threads, 0, ctx.stream>>>(
         static_cast<const uint8_t*>(src), ld_src, static_cast<uint8_t*>(dst), ld_dst, rows, cols);
   return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }

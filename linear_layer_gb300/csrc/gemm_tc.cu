@@ -15,7 +15,9 @@
 //               smem stages and hands finished accumulators to the epilogue.
 //   warps 2..   epilogue.  16-bit inputs: 4 warps read the accumulator with
 //               tcgen05.ld while the next tile's MMAs run into the other of two TMEM
-//               accumulators, then apply alpha/beta, cast and store.
+//               accumulators, then apply alpha/beta, cast and store; each 32 x 32
+//               chunk is transposed through shared memory so that global C loads and
+//               D stores are row segments (coalesced for any leading dimension).
 //               FP8 inputs: 8 warps promote each 128-K block: the MMAs accumulate one
 //               block into a TMEM partial buffer (two, alternating), the warps read it
 //               and add scale_a[m][kb] * scale_b[kb][n/128] * partial into FP32
@@ -40,7 +42,7 @@ struct GemmParams {
   void* D;
   int64_t ldd;
   int d_type;
-  int c_vec, d_vec;  // rows of C / D may be accessed with 16-byte vectors
+  int c_vec, d_vec;  // rows of C / D may be accessed with 4-element vectors
   const float* sA;
   int64_t ld_sa;
   const float* sB;
@@ -69,8 +71,11 @@ struct TileCfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int EPI_WARPS = FP8 ? 8 : 4;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static constexpr int THREADS = 64 + EPI_THREADS;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 256 + 1024;
+  static constexpr int EPI_WARP0 = 2;  // first epilogue warp
+  static constexpr int THREADS = 32 * EPI_WARP0 + EPI_THREADS;
+  static constexpr int EPI_STAGE_BYTES = EPI_WARPS * 32 * 32 * 4;  // one 32x32 FP32 chunk per warp
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 256 + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(B_BOXES >= 1 && BN % B_BOX_N == 0, "tile N must cover whole swizzle rows");
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
@@ -97,84 +102,110 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   nb = r / gsz;
 }
 
-// Epilogue of 32 consecutive columns of one output row: D = alpha * v + beta * C.
-__device__ __forceinline__ void store_chunk32(const GemmParams& p, int m, int n, const float* v) {
-  if (m >= p.M) return;
-  const bool full = (n + 32 <= p.N);
-  float o[32];
-  if (p.beta != 0.0f) {
-    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
-    if (full && p.c_vec) {
+// Epilogue of one 32 x 32 chunk owned by a warp: rows m_base .. m_base + 31 (lane t holds
+// row m_base + t in v[0..31]), columns n0 .. n0 + 31:
+//   D[m][n] = alpha * acc[m][n] + beta * C[m][n]   (C not read when beta == 0)
+// The chunk is transposed through the warp's 32 x 32 FP32 staging buffer; float4 slot
+// c of row r is stored at slot c ^ (r & 7), which keeps the row-per-lane writes and
+// the segment-per-8-lanes reads free of bank conflicts.  Afterwards lane l handles
+// columns 4*(l%8) .. 4*(l%8)+3 of rows 4*i + l/8 (i = 0..7): each warp access is four
+// 128-byte row segments, for any leading dimension.  C loads are issued G rows at a
+// time before the stores of those rows (C may alias D, so a later load cannot move
+// above an earlier store).
+template <int G>  // rows handled per batch of C loads (8 or 4; smaller = fewer registers)
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, float* st, int m_base, int n0,
+                                               const float (&v)[32], int lane) {
+  static_assert(8 % G == 0, "G must divide 8");
+  float4* st4 = reinterpret_cast<float4*>(st);
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(crow + j);
-        o[j + 0] = p.alpha * v[j + 0] + p.beta * c4.x;
-        o[j + 1] = p.alpha * v[j + 1] + p.beta * c4.y;
-        o[j + 2] = p.alpha * v[j + 2] + p.beta * c4.z;
-        o[j + 3] = p.alpha * v[j + 3] + p.beta * c4.w;
+  for (int c = 0; c < 8; ++c)
+    st4[lane * 8 + (c ^ (lane & 7))] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  __syncwarp();
+  const int c4 = lane & 7;
+  const int n = n0 + 4 * c4;
+  const int ncols = min(4, p.N - n);  // valid columns of this lane (<= 0: none)
+  const bool full_cols = ncols == 4;
+#pragma unroll
+  for (int g = 0; g < 8; g += G) {
+    float4 cv[G];
+    if (p.beta != 0.0f) {
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const int m = m_base + 4 * (g + i) + (lane >> 3);
+        cv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < p.M && ncols > 0) {
+          const float* cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
+          if (full_cols && p.c_vec) {
+            cv[i] = *reinterpret_cast<const float4*>(cp);
+          } else {
+            cv[i].x = cp[0];
+            if (ncols > 1) cv[i].y = cp[1];
+            if (ncols > 2) cv[i].z = cp[2];
+            if (ncols > 3) cv[i].w = cp[3];
+          }
+        }
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = (n + j < p.N) ? p.alpha * v[j] + p.beta * crow[j] : 0.0f;
     }
-  } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) o[j] = p.alpha * v[j];
+    for (int i = 0; i < G; ++i) {
+      const int r = 4 * (g + i) + (lane >> 3);
+      const int m = m_base + r;
+      if (m >= p.M || ncols <= 0) continue;
+      const float4 a = st4[r * 8 + (c4 ^ (r & 7))];
+      float4 o;
+      o.x = p.alpha * a.x;
+      o.y = p.alpha * a.y;
+      o.z = p.alpha * a.z;
+      o.w = p.alpha * a.w;
+      if (p.beta != 0.0f) {
+        o.x += p.beta * cv[i].x;
+        o.y += p.beta * cv[i].y;
+        o.z += p.beta * cv[i].z;
+        o.w += p.beta * cv[i].w;
+      }
+      const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
+      if (p.d_type == LL_OUT_F32) {
+        float* dp = static_cast<float*>(p.D) + off;
+        if (full_cols && p.d_vec) {
+          *reinterpret_cast<float4*>(dp) = o;
+        } else {
+          dp[0] = o.x;
+          if (ncols > 1) dp[1] = o.y;
+          if (ncols > 2) dp[2] = o.z;
+          if (ncols > 3) dp[3] = o.w;
+        }
+      } else if (p.d_type == LL_OUT_BF16) {
+        __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(p.D) + off;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+        if (full_cols && p.d_vec) {
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&lo);
+          u.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(dp) = u;
+        } else {
+          dp[0] = lo.x;
+          if (ncols > 1) dp[1] = lo.y;
+          if (ncols > 2) dp[2] = hi.x;
+          if (ncols > 3) dp[3] = hi.y;
+        }
+      } else {
+        __half* dp = static_cast<__half*>(p.D) + off;
+        __half2 lo = __floats2half2_rn(o.x, o.y), hi = __floats2half2_rn(o.z, o.w);
+        if (full_cols && p.d_vec) {
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&lo);
+          u.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(dp) = u;
+        } else {
+          dp[0] = lo.x;
+          if (ncols > 1) dp[1] = lo.y;
+          if (ncols > 2) dp[2] = hi.x;
+          if (ncols > 3) dp[3] = hi.y;
+        }
+      }
+    }
   }
-  if (p.d_type == LL_OUT_F32) {
-    float* drow = static_cast<float*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
-    if (full && p.d_vec) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(drow + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n + j < p.N) drow[j] = o[j];
-    }
-  } else if (p.d_type == LL_OUT_BF16) {
-    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
-    if (full && p.d_vec) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        uint4 u;
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(o[j + 0], o[j + 1]);
-        __nv_bfloat162 h1 = __floats2bfloat162_rn(o[j + 2], o[j + 3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(o[j + 4], o[j + 5]);
-        __nv_bfloat162 h3 = __floats2bfloat162_rn(o[j + 6], o[j + 7]);
-        u.x = *reinterpret_cast<uint32_t*>(&h0);
-        u.y = *reinterpret_cast<uint32_t*>(&h1);
-        u.z = *reinterpret_cast<uint32_t*>(&h2);
-        u.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(drow + j) = u;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n + j < p.N) drow[j] = __float2bfloat16_rn(o[j]);
-    }
-  } else {
-    __half* drow = static_cast<__half*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
-    if (full && p.d_vec) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        uint4 u;
-        __half2 h0 = __floats2half2_rn(o[j + 0], o[j + 1]);
-        __half2 h1 = __floats2half2_rn(o[j + 2], o[j + 3]);
-        __half2 h2 = __floats2half2_rn(o[j + 4], o[j + 5]);
-        __half2 h3 = __floats2half2_rn(o[j + 6], o[j + 7]);
-        u.x = *reinterpret_cast<uint32_t*>(&h0);
-        u.y = *reinterpret_cast<uint32_t*>(&h1);
-        u.z = *reinterpret_cast<uint32_t*>(&h2);
-        u.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(drow + j) = u;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n + j < p.N) drow[j] = __float2half_rn(o[j]);
-    }
-  }
+  __syncwarp();
 }
 
 template <class Cfg, uint32_t AB_FMT>
@@ -188,7 +219,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+  float* epi_stage = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
   // bars: full[S], empty[S], tfull[2], tempty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   uint32_t* abort_flag = tmem_slot + 1;
@@ -329,6 +361,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // ---------------------------------------------------------------- epilogue (16-bit)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    float* st = epi_stage + (warp - 2) * 32 * 32;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int mb, nb;
@@ -338,28 +371,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int m = mb * 128 + q * 32 + lane;
+      const int m_base = mb * 128 + q * 32;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
         tmem_ld_wait();
+        if (c == BN / 32 - 1) {  // the accumulator is in registers: hand TMEM back now
+          tc_fence_before();
+          mbar_arrive(tempty_bar(ab));
+        }
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        store_chunk32(p, m, nb * BN + c * 32, v);
+        epilogue_chunk<8>(p, st, m_base, nb * BN + c * 32, v, lane);
       }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(ab));
       ++acc_it;
     }
   } else {
     // ---------------------------------------------------------------- promotion + epilogue (FP8)
     constexpr int HALF = BN / 2;  // columns per thread
-    const int ew = warp - 2;
+    constexpr int CH = HALF / 32;
+    const int ew = warp - Cfg::EPI_WARP0;
     const int q = warp & 3;
     const int h = ew >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    float* st = epi_stage + ew * 32 * 32;
     uint32_t pit = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -371,16 +408,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const bool col_ok = ncol0 < p.N;
       const int nblk = ncol0 / 128;
       const float* sa_row = p.sA + static_cast<int64_t>(row_ok ? m : 0) * p.ld_sa;
-      float acc[HALF];
+      float acc[CH][32];
 #pragma unroll
-      for (int j = 0; j < HALF; ++j) acc[j] = 0.0f;
-      float sa_next = row_ok ? sa_row[0] : 0.0f;
-      float sb_next = col_ok ? p.sB[nblk] : 0.0f;
+      for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[c][j] = 0.0f;
+      float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
+      float sb_next = col_ok ? __ldg(p.sB + nblk) : 0.0f;
       for (int kb = 0; kb < KB; ++kb) {
         const float s = sa_next * sb_next;
-        if (kb + 1 < KB) {
-          sa_next = row_ok ? sa_row[kb + 1] : 0.0f;
-          sb_next = col_ok ? p.sB[static_cast<int64_t>(kb + 1) * p.ld_sb + nblk] : 0.0f;
+        if (kb + 1 < KB) {  // next block's scales travel while this block is promoted
+          sa_next = row_ok ? __ldg(sa_row + kb + 1) : 0.0f;
+          sb_next = col_ok ? __ldg(p.sB + static_cast<int64_t>(kb + 1) * p.ld_sb + nblk) : 0.0f;
         }
         const uint32_t pb = pit & 1u;
         bool w = wait_bounded(tfull_bar(pb), (pit >> 1) & 1u, wctx, kRoleEpilogue);
@@ -390,21 +429,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           break;
         }
         tc_fence_after();
+        // 16 columns per TMEM load keep 128 accumulators + staging within the
+        // register budget of a 320-thread block
 #pragma unroll
-        for (int c = 0; c < HALF / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_x32(tmem_base + lane_base + pb * BN + h * HALF + c * 32, r);
+        for (int c = 0; c < 2 * CH; ++c) {
+          uint32_t r[16];
+          tmem_ld_x16(tmem_base + lane_base + pb * BN + h * HALF + c * 16, r);
           tmem_ld_wait();
+          if (c == 2 * CH - 1) {  // partial fully read: the MMAs may reuse the buffer
+            tc_fence_before();
+            mbar_arrive(tempty_bar(pb));
+          }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), s, acc[c * 32 + j]);
+          for (int j = 0; j < 16; j += 2)
+            ffma2(acc[c >> 1][(c & 1) * 16 + j], acc[c >> 1][(c & 1) * 16 + j + 1],
+                  __uint_as_float(r[j]), __uint_as_float(r[j + 1]), s);
         }
-        tc_fence_before();
-        mbar_arrive(tempty_bar(pb));
         ++pit;
       }
       if (!ok) break;
 #pragma unroll
-      for (int c = 0; c < HALF / 32; ++c) store_chunk32(p, m, ncol0 + c * 32, acc + c * 32);
+      for (int c = 0; c < CH; ++c) epilogue_chunk<4>(p, st, mb * 128 + q * 32, ncol0 + c * 32, acc[c], lane);
     }
   }
 
@@ -479,7 +524,8 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
   p.d_type = a.d_type;
   const int dsize = a.d_type == LL_OUT_F32 ? 4 : 2;
   p.c_vec = a.C != nullptr && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * 4) % 16 == 0);
-  p.d_vec = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * dsize) % 16 == 0);
+  // vector stores: 16 bytes (FP32) or 8 bytes (BF16 / FP16) per lane, at 4-column steps
+  p.d_vec = (reinterpret_cast<uintptr_t>(a.D) % (4 * dsize) == 0) && ((a.ldd * dsize) % (4 * dsize) == 0);
   p.sA = a.scale_a;
   p.ld_sa = a.ld_sa;
   p.sB = a.scale_b;
@@ -498,7 +544,7 @@ ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
   const int tiles_m = (a.M + 127) / 128;
   auto tiles = [&](int bn) { return tiles_m * ((a.N + bn - 1) / bn); };
   if (a.in_type == LL_IN_E4M3) {
-    if (tiles(256) >= ctx.num_sms || a.N > 128) return run<TileCfg<256, true>, 0>(a, ctx);
+    if (a.N > 128) return run<TileCfg<256, true>, 0>(a, ctx);
     return run<TileCfg<128, true>, 0>(a, ctx);
   }
   const bool bf = a.in_type == LL_IN_BF16;

@@ -7,16 +7,18 @@
 // At batch 1 every weight byte is used once, so the kernel is bound by HBM bandwidth
 // and does not use tensor cores (an M = 1 tile would leave 15/16 of an MMA idle).
 //
-// Design (fast path: K % 16 == 0, ldw % 16 == 0, 16-byte aligned x and W, K <= 32768):
+// Design (fast path: K % 16 == 0, ldw % 16 == 0, 16-byte aligned x and W, 1024 <= K <= 32768):
 //   * grid = one CTA per SM; CTA b owns the contiguous rows [b*N/G, (b+1)*N/G), so the
 //     weight stream is split evenly over the SMs.
 //   * one producer thread streams the CTA's rows into a ring of 32 KB shared-memory
 //     stages with cp.async.bulk (one copy per stage when rows are contiguous), so
 //     ~190 KB per SM are in flight from the first cycle.
-//   * 8 consumer warps: warp w takes rows w, w+8, ... of a stage; each lane reads
-//     16-byte chunks (lane-strided, conflict-free), multiplies them with the matching
-//     16 bytes of x (staged once in shared memory) with four dp4a, and the warp
-//     reduces its 32 partial sums with shuffles.  Lane 0 dequantises and stores.
+//   * 8 consumer warps stage x and the CTA's w_scale values in shared memory while the
+//     first weights are in flight.  Warp w takes rows w, w+8, ... of a stage; each lane
+//     reads 16-byte chunks (lane-strided, conflict-free), multiplies them with the
+//     matching 16 bytes of x with four dp4a, and releases the stage to the producer as
+//     soon as its reads are done; then the warp reduces its 32 partial sums with
+//     shuffles and lane 0 dequantises and stores.
 // Any other shape runs a plain warp-per-row kernel with scalar loads (same results).
 #include <cuda_fp16.h>
 
@@ -28,6 +30,7 @@ namespace ll {
 constexpr int kGvWarps = 8;
 constexpr int kGvThreads = 32 * (kGvWarps + 1);
 constexpr int kGvStageBytes = 32768;
+constexpr int kGvMaxRowsPerWarp = 4;  // rows of one stage per consumer warp (K >= 1024)
 
 struct GemvParams {
   int N, K;
@@ -41,6 +44,7 @@ struct GemvParams {
   int rows_per_stage;
   int stages;
   int contiguous;  // ldw == K: a stage is one contiguous copy
+  int max_rows_per_cta;
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -66,21 +70,19 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_w8a8_bulk_kernel(const Gem
   const int S = p.stages;
   const int kpad = (p.K + 127) & ~127;
   uint8_t* xs = smem + S * kGvStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(xs + kpad);  // full[S], empty[S]
-  uint32_t* abort_flag = reinterpret_cast<uint32_t*>(bars + 2 * S);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  float* sws = reinterpret_cast<float*>(xs + kpad);  // w_scale of this CTA's rows
   const int G = gridDim.x;
   const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.N / G);
   const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.N / G);
   const int nrows = r1 - r0;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sws + ((p.max_rows_per_cta + 1) & ~1));
+  uint32_t* abort_flag = reinterpret_cast<uint32_t*>(bars + 2 * S);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int RS = p.rows_per_stage;
   const int nchunks = (nrows + RS - 1) / RS;
 
-  // stage x (K bytes) in shared memory
-  for (int i = threadIdx.x; i < p.K / 16; i += blockDim.x)
-    reinterpret_cast<int4*>(xs)[i] = __ldg(reinterpret_cast<const int4*>(p.x) + i);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(bars + s), 1);
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_w8a8_bulk_kernel(const Gem
 
   if (warp == kGvWarps) {
     // ---------------------------------------------------------------- producer
+    // starts streaming weights at once; the consumers stage x and the scales meanwhile
     if (lane == 0) {
       int issued = 0;
       for (int i = 0; i < nchunks; ++i) {
@@ -120,7 +123,13 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_w8a8_bulk_kernel(const Gem
     }
   } else {
     // ---------------------------------------------------------------- consumers
-    const float sx = *p.x_scale;
+    const int ct = threadIdx.x;  // 0 .. 32 * kGvWarps - 1
+    for (int i = ct; i < p.K / 16; i += 32 * kGvWarps)
+      reinterpret_cast<int4*>(xs)[i] = __ldg(reinterpret_cast<const int4*>(p.x) + i);
+    for (int i = ct; i < nrows; i += 32 * kGvWarps) sws[i] = __ldg(p.w_scale + r0 + i);
+    const float sx = __ldg(p.x_scale);
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * kGvWarps) : "memory");  // consumer warps only
+
     const int kc = p.K / 16;
     const int4* xv = reinterpret_cast<const int4*>(xs);
     for (int i = 0; i < nchunks; ++i) {
@@ -130,23 +139,44 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_w8a8_bulk_kernel(const Gem
       if (!ok) break;
       const int rows = min(RS, nrows - i * RS);
       const uint8_t* stage = smem + s * kGvStageBytes;
-      for (int r = warp; r < rows; r += kGvWarps) {
-        const int4* wrow = reinterpret_cast<const int4*>(stage + r * p.K);
-        int acc0 = 0, acc1 = 0;
+      // dot products of this warp's rows of the stage, then release the stage at once
+      int part[kGvMaxRowsPerWarp];
+      int nr = 0;
+#pragma unroll
+      for (int j = 0; j < kGvMaxRowsPerWarp; ++j) {
+        const int r = warp + j * kGvWarps;
+        part[j] = 0;
+        if (r < rows) {
+          const int4* wrow = reinterpret_cast<const int4*>(stage + r * p.K);
+          int acc0 = 0, acc1 = 0;
 #pragma unroll 4
-        for (int c = lane; c < kc; c += 32) {
-          const int4 w = wrow[c];
-          const int4 a = xv[c];
-          acc0 = __dp4a(w.x, a.x, acc0);
-          acc1 = __dp4a(w.y, a.y, acc1);
-          acc0 = __dp4a(w.z, a.z, acc0);
-          acc1 = __dp4a(w.w, a.w, acc1);
+          for (int c = lane; c < kc; c += 32) {
+            const int4 w = wrow[c];
+            const int4 a = xv[c];
+            acc0 = __dp4a(w.x, a.x, acc0);
+            acc1 = __dp4a(w.y, a.y, acc1);
+            acc0 = __dp4a(w.z, a.z, acc0);
+            acc1 = __dp4a(w.w, a.w, acc1);
+          }
+          part[j] = acc0 + acc1;
+          nr = j + 1;
         }
-        const int z = warp_sum(acc0 + acc1);
-        if (lane == 0) dequant_store(p, r0 + i * RS + r, z, sx);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(bars + S + s));
+#pragma unroll
+      for (int j = 0; j < kGvMaxRowsPerWarp; ++j) {
+        if (j < nr) {
+          const int z = warp_sum(part[j]);
+          const int rl = i * RS + warp + j * kGvWarps;  // row within this CTA
+          if (lane == 0) {
+            const int o = r0 + rl;
+            if (p.z_out) p.z_out[o] = z;
+            const float t = __fmul_rn(__int2float_rn(z), sx);
+            p.y[o] = __float2half_rn(__fmul_rn(t, sws[rl]));
+          }
+        }
+      }
     }
   }
 }
@@ -182,18 +212,25 @@ ll_status launch_gemv_w8a8(int N, int K, const int8_t* x, const float* x_scale, 
   const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
                        (reinterpret_cast<uintptr_t>(W) % 16 == 0) && (K % 16 == 0) &&
                        (ldw % 16 == 0);
-  if (aligned && K > 0 && K <= 32768) {
+  if (aligned && K >= 1024 && K <= 32768) {
     const int kpad = (K + 127) & ~127;
-    int stages = (220 * 1024 - kpad) / kGvStageBytes;
+    p.rows_per_stage = kGvStageBytes / K;  // <= kGvWarps * kGvMaxRowsPerWarp for K >= 1024
+    const int chunks = (N + p.rows_per_stage - 1) / p.rows_per_stage;
+    const int grid = chunks < ctx.num_sms ? chunks : ctx.num_sms;
+    p.max_rows_per_cta = (N + grid - 1) / grid;
+    const int scale_bytes = ((p.max_rows_per_cta + 1) & ~1) * 4;
+    int stages = (220 * 1024 - kpad - scale_bytes) / kGvStageBytes;
     if (stages > 6) stages = 6;
+    if (stages < 2) {
+      p.stages = 0;
+      gemv_w8a8_plain_kernel<<<(N + 7) / 8, 256, 0, ctx.stream>>>(p);
+      return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+    }
     p.stages = stages;
-    p.rows_per_stage = kGvStageBytes / K;
-    const int smem = stages * kGvStageBytes + kpad + 2 * stages * 8 + 16 + 128;
+    const int smem = stages * kGvStageBytes + kpad + scale_bytes + 2 * stages * 8 + 16 + 128;
     if (cudaFuncSetAttribute(gemv_w8a8_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return LL_ERR_CUDA;
-    int chunks = (N + p.rows_per_stage - 1) / p.rows_per_stage;
-    const int grid = chunks < ctx.num_sms ? chunks : ctx.num_sms;
     gemv_w8a8_bulk_kernel<<<grid, kGvThreads, smem, ctx.stream>>>(p);
   } else {
     p.stages = 0;

@@ -63,7 +63,7 @@ struct WaitCtx {
 // Wait until the phase with the given parity of `bar` has completed.  Gives up
 // when the CTA's abort flag is set, or after ctx.timeout_ns, in which case it
 // records the timeout (first writer wins) and raises the CTA's abort flag.
-static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
                                           uint32_t role) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -82,7 +82,7 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
 }
 
 // Same, but ignores the abort flag: used while draining copies that are in flight.
-static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > timeout_ns) return false;
@@ -185,8 +185,30 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// Each thread of the warp reads 16 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// a0 += p0 * s, a1 += p1 * s as one packed FP32x2 FMA (two independent FP32 FMAs,
+// each rounded to nearest even).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float p0, float p1, float s) {
+  uint64_t acc, pp, ss;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "f"(p0), "f"(p1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(pp), "l"(ss));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
 }
 
 // Shared-memory matrix descriptor for tcgen05.mma (the tcgen05 "matrix descriptor"):
