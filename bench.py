@@ -50,8 +50,7 @@ def gemv_bytes(N, K):
 
 KERNEL_SOURCES = {
     "gemm_tc_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/ptx.cuh"],
-    "gemv_w8a8_bulk_kernel": ["linear_layer_gb300/csrc/gemv_w8a8.cu",
-                              "linear_layer_gb300/csrc/ptx.cuh"],
+    "gemv_w8a8_kernel": ["linear_layer_gb300/csrc/gemv_w8a8.cu"],
 }
 
 
@@ -365,8 +364,8 @@ def bench_gemv(args, dev, stream, peaks, peak_src):
             "us_per_launch": round(launch_s * 1e6, 3),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
-                         "traffic": measured_traffic("w8a8_gemv_4096x11008", "gemv_w8a8_bulk_kernel"),
-                         "kernel": "gemv_w8a8_bulk_kernel", "peak_source": peak_src + " hbm_gbs",
+                         "traffic": measured_traffic("w8a8_gemv_4096x11008", "gemv_w8a8_kernel"),
+                         "kernel": "gemv_w8a8_kernel", "peak_source": peak_src + " hbm_gbs",
                          "algorithmic_bytes_per_launch": wbytes},
             "timing": "CUDA graph of %d launches over %d weight copies (%.0f MB > L2), %d replays" % (
                 per_graph, ncopies, ncopies * wbytes / 1e6, reps),

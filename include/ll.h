@@ -170,6 +170,11 @@ ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const void* A, i
  *   y       : N FP16 outputs (written)
  *   z_out   : N int32 raw dot products (written when not NULL)
  * |z| <= K * 128^2 must fit INT32, i.e. K <= 131071 (checked: LL_ERR_INVALID_ARG).
+ * Ordering: the kernel is launched with programmatic dependent launch.  x, x_scale
+ * are read and y, z_out written only after all preceding work on the stream has
+ * finished; W and w_scale may be read while the immediately preceding
+ * ll_linear_w8a8_gemv call on the same stream is still running, so they must not be
+ * that call's y / z_out (weights are never outputs of the previous layer).
  * N == 0: nothing is done.  K == 0: z = 0 and y = fp16(0 * s_x * s_W[o]).
  * Errors: LL_ERR_INVALID_ARG for negative sizes, ldw < K or NULL pointers.
  */
