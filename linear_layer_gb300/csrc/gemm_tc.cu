@@ -461,6 +461,232 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   }
 }
 
+
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// Large 16-bit problems run on CTA pairs (2-CTA clusters).  A pair owns a 256 x 256
+// output tile: each CTA loads its 128 rows of A and its half (128 columns) of B into
+// its own shared memory, the even CTA's single MMA thread issues tcgen05.mma with
+// cta_group::2 (M = 256), and each CTA's TMEM receives its own 128 rows of the
+// accumulator.  Per SM this halves the B traffic (TMA fill and shared-memory reads)
+// of the one-CTA 128 x 256 tile.
+//   full[s]   (even CTA)  count 1: the even CTA's producer arms it with both CTAs'
+//                         transaction bytes; both CTAs' TMA copies complete on it
+//                         (the odd CTA's bytes may land first: the transaction count
+//                         then runs negative until the arrival, which is allowed).
+//   empty[s]  (each CTA)  count 1: the MMA commit, multicast to both CTAs.
+//   tfull[b]  (each CTA)  count 1: the MMA commit, multicast to both CTAs.
+//   tempty[b] (even CTA)  count 8: one arrival per epilogue warp of each CTA.
+// Output tiles past the last full wave are split into two 256 x 128 halves when that
+// lets one half-wave finish the problem.
+template <int BN_>
+struct PairCfg {
+  static constexpr int BN = BN_;           // pair tile N
+  static constexpr int BK = 64;            // 16-bit K per stage (one 128-byte row)
+  static constexpr int UMMA_K = 16;
+  static constexpr int KSTEPS = BK / UMMA_K;
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BOX_N = 64;
+  static constexpr int B_BOX_BYTES = BK * 128;
+  static constexpr int B_BOXES_MAX = BN / 2 / B_BOX_N;  // per CTA
+  static constexpr int STAGE_BYTES = A_BYTES + B_BOXES_MAX * B_BOX_BYTES;
+  static constexpr int STAGES = 196608 / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int EPI_STAGE_BYTES = EPI_WARPS * 32 * 32 * 4;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 256 + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(TMEM_COLS <= 512, "TMEM budget");
+};
+
+struct PairSched {
+  int num_m2, num_n;  // pair tiles in M (256 rows) and N (BN columns)
+  int full_units;     // units that are whole tiles
+  int num_units;      // full_units + 2 * split tiles
+};
+
+template <class Cfg, uint32_t AB_FMT>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmParams p, const PairSched sc) {
+  constexpr int S = Cfg::STAGES;
+  constexpr int BN = Cfg::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* epi_stage = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  auto full_bar = [&](int s) { return smem_addr(bars + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + S + s); };
+  auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * S + b); };
+  auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * S + 2 + b); };
+  const uint32_t drain_bar = smem_addr(bars + 2 * S + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * Cfg::EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  WaitCtx wctx{p.status, p.timeout_ns, abort_flag};
+  const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;
+  // unit -> (first row of the pair tile, first column, columns)
+  auto unit = [&](int u, int& m0, int& n0, int& ncols) {
+    int t = u, half = -1;
+    if (u >= sc.full_units) {
+      t = sc.full_units + ((u - sc.full_units) >> 1);
+      half = (u - sc.full_units) & 1;
+    }
+    int mb, nb;
+    tile_coords(t, sc.num_m2, sc.num_n, p.group_m, mb, nb);
+    m0 = mb * 256;
+    n0 = nb * BN + (half > 0 ? BN / 2 : 0);
+    ncols = half < 0 ? BN : BN / 2;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer (each CTA)
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
+        int m0, n0, ncols;
+        unit(u, m0, n0, ncols);
+        const int boxes = ncols / 2 / Cfg::B_BOX_N;
+        const uint32_t bytes = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
+        for (int kb = 0; kb < KB; ++kb) {
+          const int s = it % S;
+          if (!wait_bounded(empty_bar(s), ((it / S) & 1u) ^ 1u, wctx, kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t cfull = mapa_cluster(full_bar(s), 0);
+          uint8_t* a_s = smem + s * Cfg::STAGE_BYTES;
+          uint8_t* b_s = a_s + Cfg::A_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+          tma_load_2d_pair(smem_addr(a_s), &tmA, cfull, kb * Cfg::BK, m0 + 128 * rank);
+          for (int j = 0; j < boxes; ++j)
+            tma_load_2d_pair(smem_addr(b_s + j * Cfg::B_BOX_BYTES), &tmB, cfull,
+                             n0 + rank * (ncols / 2) + j * Cfg::B_BOX_N, kb * Cfg::BK);
+          ++it;
+        }
+      }
+      if (!ok && rank == 0) {  // the even CTA's full barriers see both CTAs' copies
+        for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0u); j < it; ++j)
+          wait_drain(full_bar(j % S), (j / S) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
+        int m0, n0, ncols;
+        unit(u, m0, n0, ncols);
+        const uint32_t idesc = make_idesc(AB_FMT, ncols, 256);
+        const uint32_t ab = acc_it & 1u;
+        if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * BN;
+        for (int kb = 0; kb < KB; ++kb) {
+          const int s = it % S;
+          if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_addr(smem + s * Cfg::STAGE_BYTES);
+          const uint32_t b_base = a_base + Cfg::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc =
+                smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BOX_BYTES, 1024);
+            mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_pair_mc(empty_bar(s), 0x3);
+          ++it;
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(tfull_bar(ab), 0x3);
+        ++acc_it;
+      }
+      mma_commit_pair(drain_bar);
+      wait_drain(drain_bar, 0u, p.timeout_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (each CTA)
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    float* st = epi_stage + (warp - 2) * 32 * 32;
+    uint32_t acc_it = 0;
+    for (int u = pair; u < sc.num_units; u += num_pairs) {
+      int m0, n0, ncols;
+      unit(u, m0, n0, ncols);
+      const uint32_t ab = acc_it & 1u;
+      bool ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int m_base = m0 + 128 * rank + q * 32;
+      const int chunks = ncols / 32;
+#pragma unroll 1
+      for (int c = 0; c < chunks; ++c) {
+        uint32_t r[32];
+        tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
+        tmem_ld_wait();
+        if (c == chunks - 1) {  // accumulator in registers: release it to the MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_cluster(tempty_bar(ab), 0));
+        }
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        epilogue_chunk<8>(p, st, m_base, n0 + c * 32, v, lane);
+      }
+      ++acc_it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -497,20 +723,7 @@ static bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
   return r == CUDA_SUCCESS;
 }
 
-template <class Cfg, uint32_t AB_FMT>
-static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
-  auto kern = gemm_tc_kernel<Cfg, AB_FMT>;
-  // the attribute is per device; setting it on every call is cheap and always correct
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
-      cudaSuccess)
-    return LL_ERR_CUDA;
-  const CUtensorMapDataType dt =
-      Cfg::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-               : (AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-  CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
-  if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
-
+static GemmParams make_params(const GemmArgs& a, const LaunchCtx& ctx) {
   GemmParams p;
   p.M = a.M;
   p.N = a.N;
@@ -534,10 +747,92 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
   p.timeout_ns = ctx.timeout_ns;
   p.group_m = 8;
 
+  return p;
+}
+
+constexpr int kMaxDev = 64;
+
+template <class Cfg, uint32_t AB_FMT>
+static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
+  auto kern = gemm_tc_kernel<Cfg, AB_FMT>;
+  // the attribute is per device; setting it on every call is cheap and always correct
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+      cudaSuccess)
+    return LL_ERR_CUDA;
+  const CUtensorMapDataType dt =
+      Cfg::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+               : (AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
+  if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
+
+  GemmParams p = make_params(a, ctx);
+
   const int num_tiles = ((a.M + 127) / 128) * ((a.N + Cfg::BN - 1) / Cfg::BN);
   const int grid = num_tiles < ctx.num_sms ? num_tiles : ctx.num_sms;
   kern<<<grid, Cfg::THREADS, Cfg::SMEM, ctx.stream>>>(tmA, tmB, p);
   return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+
+template <uint32_t AB_FMT>
+static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
+  using Cfg = PairCfg<256>;
+  auto kern = gemm_tc2_kernel<Cfg, AB_FMT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+      cudaSuccess)
+    return LL_ERR_CUDA;
+  const CUtensorMapDataType dt =
+      AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, a.A, dt, 2, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
+  if (!make_map(&tmB, a.B, dt, 2, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
+  GemmParams p = make_params(a, ctx);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // co-resident CTA pairs (one CTA per SM): the persistent grid
+  static int max_pairs[kMaxDev] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDev) return LL_ERR_NO_DEVICE;
+  if (max_pairs[dev] == 0) {
+    cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = ctx.num_sms / 2;
+    }
+    max_pairs[dev] = n;
+  }
+  PairSched sc;
+  sc.num_m2 = (a.M + 255) / 256;
+  sc.num_n = (a.N + Cfg::BN - 1) / Cfg::BN;
+  const int T = sc.num_m2 * sc.num_n;
+  const int P = T < max_pairs[dev] ? T : max_pairs[dev];
+  const int waves = T / P, rem = T - waves * P;
+  if (rem > 0 && 2 * rem <= P) {  // finish with one half-wave of 256 x 128 halves
+    sc.full_units = waves * P;
+    sc.num_units = sc.full_units + 2 * rem;
+  } else {
+    sc.full_units = T;
+    sc.num_units = T;
+  }
+  cfg.gridDim = dim3(2 * P);
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p, sc) != cudaSuccess) {
+    cudaGetLastError();
+    return LL_ERR_CUDA;
+  }
+  return LL_OK;
 }
 
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
@@ -548,6 +843,9 @@ ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
     return run<TileCfg<128, true>, 0>(a, ctx);
   }
   const bool bf = a.in_type == LL_IN_BF16;
+  // large problems: CTA pairs with 256 x 256 tiles
+  if (((a.M + 255) / 256) * ((a.N + 255) / 256) >= ctx.num_sms / 4)
+    return bf ? run_pair<1>(a, ctx) : run_pair<0>(a, ctx);
   int bn = 64;
   if (tiles(256) >= ctx.num_sms)
     bn = 256;
