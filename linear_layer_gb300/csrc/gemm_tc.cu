@@ -43,6 +43,7 @@ struct GemmParams {
   int64_t ldd;
   int d_type;
   int c_vec, d_vec;  // rows of C / D may be accessed with 4-element vectors
+  int d_row16;       // rows of D start on 16-byte boundaries
   const float* sA;
   int64_t ld_sa;
   const float* sB;
@@ -464,9 +465,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
 // ------------------------------------------------------------------ CTA-pair kernel
 //
-// Large 16-bit problems run on CTA pairs (2-CTA clusters).  A pair owns a 256 x 256
-// output tile: each CTA loads its 128 rows of A and its half (128 columns) of B into
-// its own shared memory, the even CTA's single MMA thread issues tcgen05.mma with
+// Large problems run on CTA pairs (2-CTA clusters).  A pair owns a 256 x 256 output
+// tile: each CTA loads its 128 rows of A and its half (128 columns) of B into its own
+// shared memory, the even CTA's single MMA thread issues tcgen05.mma with
 // cta_group::2 (M = 256), and each CTA's TMEM receives its own 128 rows of the
 // accumulator.  Per SM this halves the B traffic (TMA fill and shared-memory reads)
 // of the one-CTA 128 x 256 tile.
@@ -476,28 +477,43 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 //                         then runs negative until the arrival, which is allowed).
 //   empty[s]  (each CTA)  count 1: the MMA commit, multicast to both CTAs.
 //   tfull[b]  (each CTA)  count 1: the MMA commit, multicast to both CTAs.
-//   tempty[b] (even CTA)  count 8: one arrival per epilogue warp of each CTA.
+//   tempty[b] (even CTA)  one arrival per epilogue warp of each CTA.
+// 16-bit inputs: the accumulator of a tile is double buffered in TMEM (2 x 256
+// columns) and 4 epilogue warps per CTA drain one while the MMAs fill the other.
 // Output tiles past the last full wave are split into two 256 x 128 halves when that
 // lets one half-wave finish the problem.
-template <int BN_>
+// FP8 inputs: each 128-K block is accumulated into one of two TMEM partial buffers;
+// a scale warp stages that block's scale_a (this CTA's 128 rows) and scale_b (the
+// tile's two 128-column blocks) into a shared-memory ring with cp.async, and 8
+// promotion warps add scale_a * scale_b * partial into FP32 registers (32 rows x 128
+// columns per warp), then store the tile straight from registers.
+template <int BN_, bool FP8_>
 struct PairCfg {
-  static constexpr int BN = BN_;           // pair tile N
-  static constexpr int BK = 64;            // 16-bit K per stage (one 128-byte row)
-  static constexpr int UMMA_K = 16;
+  static constexpr int BN = BN_;  // pair tile N
+  static constexpr bool FP8 = FP8_;
+  static constexpr int ELT = FP8 ? 1 : 2;
+  static constexpr int BK = 128 / ELT;  // K per stage (one 128-byte row)
+  static constexpr int UMMA_K = 32 / ELT;
   static constexpr int KSTEPS = BK / UMMA_K;
   static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BOX_N = 64;
+  static constexpr int B_BOX_N = 128 / ELT;
   static constexpr int B_BOX_BYTES = BK * 128;
   static constexpr int B_BOXES_MAX = BN / 2 / B_BOX_N;  // per CTA
   static constexpr int STAGE_BYTES = A_BYTES + B_BOXES_MAX * B_BOX_BYTES;
   static constexpr int STAGES = 196608 / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int EPI_WARPS = 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int EPI_STAGE_BYTES = EPI_WARPS * 32 * 32 * 4;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 256 + 1024;
+  static constexpr int EPI_WARP0 = FP8 ? 3 : 2;  // warps: producer, MMA, [scales], epilogue
+  static constexpr int EPI_WARPS = FP8 ? 8 : 4;
+  static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+  static constexpr int EPI_STAGE_BYTES = FP8 ? 0 : EPI_WARPS * 32 * 32 * 4;
+  static constexpr int SC_SLOTS = FP8 ? 8 : 0;
+  static constexpr int SC_FLOATS = 128 + 4;  // scale_a of 128 rows, scale_b of 2 blocks, pad
+  static constexpr int SC_BYTES = SC_SLOTS * SC_FLOATS * 4;
+  static constexpr int NBARS = 2 * STAGES + 5 + 2 * SC_SLOTS;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + SC_BYTES + NBARS * 8 + 16 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(TMEM_COLS <= 512, "TMEM budget");
+  static_assert(B_BOXES_MAX >= 1, "B half must cover a whole swizzle row");
 };
 
 struct PairSched {
@@ -506,19 +522,90 @@ struct PairSched {
   int num_units;      // full_units + 2 * split tiles
 };
 
+// FP8 epilogue straight from registers: lane = one row, acc = 4 x 32 consecutive
+// columns from n0.  D = alpha * acc + beta * C.
+template <int CH>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0,
+                                              const float (&acc)[CH][32]) {
+  if (m >= p.M) return;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int n = n0 + 32 * c;
+    if (n >= p.N) break;
+    const bool full = n + 32 <= p.N;
+    float o[32];
+    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
+    if (p.beta != 0.0f && full && p.c_vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 cv = *reinterpret_cast<const float4*>(crow + j);
+        o[j] = p.alpha * acc[c][j] + p.beta * cv.x;
+        o[j + 1] = p.alpha * acc[c][j + 1] + p.beta * cv.y;
+        o[j + 2] = p.alpha * acc[c][j + 2] + p.beta * cv.z;
+        o[j + 3] = p.alpha * acc[c][j + 3] + p.beta * cv.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        o[j] = p.alpha * acc[c][j];
+        if (p.beta != 0.0f && n + j < p.N) o[j] += p.beta * crow[j];
+      }
+    }
+    const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
+    if (p.d_type == LL_OUT_F32) {
+      float* dp = static_cast<float*>(p.D) + off;
+      if (full && p.d_row16) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < p.N) dp[j] = o[j];
+      }
+    } else {
+      const bool bf = p.d_type == LL_OUT_BF16;
+      uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (bf) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+          w[j] = *reinterpret_cast<uint32_t*>(&h2);
+        } else {
+          __half2 h2 = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
+          w[j] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+      }
+      if (full && p.d_row16) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<uint4*>(dp + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < p.N) dp[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+      }
+    }
+  }
+}
+
 template <class Cfg, uint32_t AB_FMT>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p, const PairSched sc) {
   constexpr int S = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
+  constexpr int J = Cfg::SC_SLOTS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* epi_stage = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
-  // bars: full[S], empty[S], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  float* scales = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES +
+                                               Cfg::SC_BYTES);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain, sc_full[J], sc_empty[J]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
   uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -531,6 +618,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * S + b); };
   auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * S + 2 + b); };
   const uint32_t drain_bar = smem_addr(bars + 2 * S + 4);
+  auto sc_full_bar = [&](int j) { return smem_addr(bars + 2 * S + 5 + j); };
+  auto sc_empty_bar = [&](int j) { return smem_addr(bars + 2 * S + 5 + J + j); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -542,6 +631,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(tempty_bar(b), 2 * Cfg::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    for (int j = 0; j < J; ++j) {
+      mbar_init(sc_full_bar(j), 32);                  // one cp.async arrival per scale lane
+      mbar_init(sc_empty_bar(j), Cfg::EPI_WARPS);     // one arrival per promotion warp
+    }
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -613,11 +706,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int m0, n0, ncols;
         unit(u, m0, n0, ncols);
         const uint32_t idesc = make_idesc(AB_FMT, ncols, 256);
-        const uint32_t ab = acc_it & 1u;
-        if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * BN;
+        uint32_t d_tmem = 0;
+        if (!Cfg::FP8) {  // one accumulator per tile
+          const uint32_t ab = acc_it & 1u;
+          if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) break;
+          tc_fence_after();
+          d_tmem = tmem_base + ab * BN;
+        }
         for (int kb = 0; kb < KB; ++kb) {
+          if (Cfg::FP8) {  // one partial buffer per 128-K block
+            const uint32_t pb = acc_it & 1u;
+            if (!wait_bounded(tempty_bar(pb), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + pb * BN;
+          }
           const int s = it % S;
           if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
             ok = false;
@@ -631,23 +736,68 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc =
                 smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BOX_BYTES, 1024);
-            mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            if (Cfg::FP8)
+              mma_f8_pair(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+            else
+              mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair_mc(empty_bar(s), 0x3);
           ++it;
+          if (Cfg::FP8) {
+            mma_commit_pair_mc(tfull_bar(acc_it & 1u), 0x3);
+            ++acc_it;
+          }
         }
         if (!ok) break;
-        mma_commit_pair_mc(tfull_bar(ab), 0x3);
-        ++acc_it;
+        if (!Cfg::FP8) {
+          mma_commit_pair_mc(tfull_bar(acc_it & 1u), 0x3);
+          ++acc_it;
+        }
       }
       mma_commit_pair(drain_bar);
       wait_drain(drain_bar, 0u, p.timeout_ns);
     }
-  } else {
+  } else if (Cfg::FP8 && warp == 2) {
+    // ---------------------------------------------------------------- scale loader (FP8)
+    const int nblk_total = (p.N + 127) / 128;
+    uint32_t seq = 0;
+    bool ok = true;
+    for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
+      int m0, n0, ncols;
+      unit(u, m0, n0, ncols);
+      const int row0 = m0 + 128 * static_cast<int>(rank) + 4 * lane;
+      const int nb0 = n0 / 128;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int j = seq % J;
+        bool w = wait_bounded(sc_empty_bar(j), ((seq / J) & 1u) ^ 1u, wctx, kRoleProducer);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        float* slot = scales + j * Cfg::SC_FLOATS;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = row0 + i;
+          const bool v = row < p.M;
+          cp_async_4(smem_addr(slot + 4 * lane + i), v ? p.sA + static_cast<int64_t>(row) * p.ld_sa + kb : p.sA,
+                     v ? 4u : 0u);
+        }
+        if (lane < 2) {
+          const int nbk = nb0 + lane;
+          const bool v = (lane * 128 < ncols) && nbk < nblk_total;
+          cp_async_4(smem_addr(slot + 128 + lane), v ? p.sB + static_cast<int64_t>(kb) * p.ld_sb + nbk : p.sB,
+                     v ? 4u : 0u);
+        }
+        cp_async_mbar_arrive_noinc(sc_full_bar(j));
+        ++seq;
+      }
+    }
+  } else if (!Cfg::FP8) {
     // ---------------------------------------------------------------- epilogue (each CTA)
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    float* st = epi_stage + (warp - 2) * 32 * 32;
+    float* st = epi_stage + (warp - Cfg::EPI_WARP0) * 32 * 32;
     uint32_t acc_it = 0;
     for (int u = pair; u < sc.num_units; u += num_pairs) {
       int m0, n0, ncols;
@@ -667,7 +817,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (c == chunks - 1) {  // accumulator in registers: release it to the MMA
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_cluster(tempty_bar(ab), 0));
+          if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
         }
         float v[32];
 #pragma unroll
@@ -675,6 +825,63 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         epilogue_chunk<8>(p, st, m_base, n0 + c * 32, v, lane);
       }
       ++acc_it;
+    }
+  } else {
+    // ---------------------------------------------------------------- promotion (FP8, each CTA)
+    constexpr int HALF = BN / 2;  // columns per promotion warp
+    constexpr int CH = HALF / 32;
+    const int ew = warp - Cfg::EPI_WARP0;
+    const int q = warp & 3;
+    const int h = ew >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t pit = 0, seq = 0;
+    bool ok = true;
+    for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
+      int m0, n0, ncols;
+      unit(u, m0, n0, ncols);
+      const int m = m0 + 128 * static_cast<int>(rank) + q * 32 + lane;
+      float acc[CH][32];
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[c][j] = 0.0f;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int j = seq % J;
+        const uint32_t pb = pit & 1u;
+        bool w = wait_bounded(sc_full_bar(j), (seq / J) & 1u, wctx, kRoleEpilogue);
+        w = w && wait_bounded(tfull_bar(pb), (pit >> 1) & 1u, wctx, kRoleEpilogue);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float* slot = scales + j * Cfg::SC_FLOATS;
+        const float s = slot[q * 32 + lane] * slot[128 + h];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sc_empty_bar(j));
+        // 16 columns per TMEM load keep 128 accumulators + staging within the
+        // register budget
+#pragma unroll
+        for (int c = 0; c < 2 * CH; ++c) {
+          uint32_t r[16];
+          tmem_ld_x16(tmem_base + lane_base + pb * BN + h * HALF + c * 16, r);
+          tmem_ld_wait();
+          if (c == 2 * CH - 1) {  // partial fully read: the MMAs may reuse the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(pb), 0));
+          }
+#pragma unroll
+          for (int jj = 0; jj < 16; jj += 2)
+            ffma2(acc[c >> 1][(c & 1) * 16 + jj], acc[c >> 1][(c & 1) * 16 + jj + 1],
+                  __uint_as_float(r[jj]), __uint_as_float(r[jj + 1]), s);
+        }
+        ++pit;
+        ++seq;
+      }
+      if (!ok) break;
+      if (h * HALF < ncols) epilogue_rows<CH>(p, m, n0 + h * HALF, acc);
     }
   }
 
@@ -739,6 +946,7 @@ static GemmParams make_params(const GemmArgs& a, const LaunchCtx& ctx) {
   p.c_vec = a.C != nullptr && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * 4) % 16 == 0);
   // vector stores: 16 bytes (FP32) or 8 bytes (BF16 / FP16) per lane, at 4-column steps
   p.d_vec = (reinterpret_cast<uintptr_t>(a.D) % (4 * dsize) == 0) && ((a.ldd * dsize) % (4 * dsize) == 0);
+  p.d_row16 = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * dsize) % 16 == 0);
   p.sA = a.scale_a;
   p.ld_sa = a.ld_sa;
   p.sB = a.scale_b;
@@ -775,18 +983,19 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
 }
 
 
-template <uint32_t AB_FMT>
+template <bool FP8, uint32_t AB_FMT>
 static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
-  using Cfg = PairCfg<256>;
+  using Cfg = PairCfg<256, FP8>;
   auto kern = gemm_tc2_kernel<Cfg, AB_FMT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
       cudaSuccess)
     return LL_ERR_CUDA;
   const CUtensorMapDataType dt =
-      AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+          : (AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, a.A, dt, 2, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
-  if (!make_map(&tmB, a.B, dt, 2, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
+  if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
+  if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
   GemmParams p = make_params(a, ctx);
 
   cudaLaunchConfig_t cfg = {};
@@ -820,7 +1029,10 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   const int T = sc.num_m2 * sc.num_n;
   const int P = T < max_pairs[dev] ? T : max_pairs[dev];
   const int waves = T / P, rem = T - waves * P;
-  if (rem > 0 && 2 * rem <= P) {  // finish with one half-wave of 256 x 128 halves
+  // 16-bit: finish with one half-wave of 256 x 128 halves when that is shorter.
+  // (FP8 halves would give each CTA 64 one-byte columns, narrower than a 128-byte
+  // swizzle row, so FP8 keeps whole tiles.)
+  if (!FP8 && rem > 0 && 2 * rem <= P) {
     sc.full_units = waves * P;
     sc.num_units = sc.full_units + 2 * rem;
   } else {
@@ -838,14 +1050,15 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
   const int tiles_m = (a.M + 127) / 128;
   auto tiles = [&](int bn) { return tiles_m * ((a.N + bn - 1) / bn); };
+  const bool pair = ((a.M + 255) / 256) * ((a.N + 255) / 256) >= ctx.num_sms / 4;
   if (a.in_type == LL_IN_E4M3) {
+    if (pair) return run_pair<true, 0>(a, ctx);
     if (a.N > 128) return run<TileCfg<256, true>, 0>(a, ctx);
     return run<TileCfg<128, true>, 0>(a, ctx);
   }
   const bool bf = a.in_type == LL_IN_BF16;
   // large problems: CTA pairs with 256 x 256 tiles
-  if (((a.M + 255) / 256) * ((a.N + 255) / 256) >= ctx.num_sms / 4)
-    return bf ? run_pair<1>(a, ctx) : run_pair<0>(a, ctx);
+  if (pair) return bf ? run_pair<false, 1>(a, ctx) : run_pair<false, 0>(a, ctx);
   int bn = 64;
   if (tiles(256) >= ctx.num_sms)
     bn = 256;

@@ -125,6 +125,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
+// Relaxed remote arrival: for hand-backs that publish no memory writes (e.g. a TMEM
+// buffer whose reads tcgen05.wait::ld has already completed).  A release arrival
+// would first wait for all of the thread's outstanding memory operations.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA / bulk copies
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -151,6 +158,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(x), "r"(y)
       : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared; src_size 0 writes zero without reading.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_size) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_size)
+               : "memory");
+}
+
+// Arrive on `bar` once every cp.async issued so far by this thread has completed; the
+// barrier's expected count must include this arrival (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // Untiled bulk copy global -> shared (addresses 16-byte aligned, size a multiple of 16).
