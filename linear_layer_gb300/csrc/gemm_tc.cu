@@ -74,7 +74,7 @@ struct TileCfg {
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int EPI_WARP0 = 2;  // first epilogue warp
   static constexpr int THREADS = 32 * EPI_WARP0 + EPI_THREADS;
-  static constexpr int EPI_STAGE_BYTES = EPI_WARPS * 32 * 32 * 4;  // one 32x32 FP32 chunk per warp
+  static constexpr int EPI_STAGE_BYTES = FP8 ? 0 : EPI_WARPS * 32 * 32 * 4;  // 32x32 FP32 per warp
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 256 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(B_BOXES >= 1 && BN % B_BOX_N == 0, "tile N must cover whole swizzle rows");
@@ -110,9 +110,11 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
 // c of row r is stored at slot c ^ (r & 7), which keeps the row-per-lane writes and
 // the segment-per-8-lanes reads free of bank conflicts.  Afterwards lane l handles
 // columns 4*(l%8) .. 4*(l%8)+3 of rows 4*i + l/8 (i = 0..7): each warp access is four
-// 128-byte row segments, for any leading dimension.  C loads are issued G rows at a
-// time before the stores of those rows (C may alias D, so a later load cannot move
-// above an earlier store).
+// 128-byte row segments (4-element vectors where the pitch allows, else scalars).  C
+// loads are issued G rows at a time before the stores of those rows (C may alias D, so
+// a later load cannot move above an earlier store).  Measured alternatives that were
+// slower: a column-per-lane pass for unaligned pitches, and prefetching the next
+// tile's C rows into L2 (it evicted operand panels).
 template <int G>  // rows handled per batch of C loads (8 or 4; smaller = fewer registers)
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, float* st, int m_base, int n0,
                                                const float (&v)[32], int lane) {
@@ -207,6 +209,74 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, float* st, i
     }
   }
   __syncwarp();
+}
+
+// FP8 epilogue straight from registers: lane = one row, acc = 4 x 32 consecutive
+// columns from n0.  D = alpha * acc + beta * C.
+template <int CH>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0,
+                                              const float (&acc)[CH][32]) {
+  if (m >= p.M) return;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int n = n0 + 32 * c;
+    if (n >= p.N) break;
+    const bool full = n + 32 <= p.N;
+    float o[32];
+    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
+    if (p.beta != 0.0f && full && p.c_vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 cv = *reinterpret_cast<const float4*>(crow + j);
+        o[j] = p.alpha * acc[c][j] + p.beta * cv.x;
+        o[j + 1] = p.alpha * acc[c][j + 1] + p.beta * cv.y;
+        o[j + 2] = p.alpha * acc[c][j + 2] + p.beta * cv.z;
+        o[j + 3] = p.alpha * acc[c][j + 3] + p.beta * cv.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        o[j] = p.alpha * acc[c][j];
+        if (p.beta != 0.0f && n + j < p.N) o[j] += p.beta * crow[j];
+      }
+    }
+    const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
+    if (p.d_type == LL_OUT_F32) {
+      float* dp = static_cast<float*>(p.D) + off;
+      if (full && p.d_row16) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < p.N) dp[j] = o[j];
+      }
+    } else {
+      const bool bf = p.d_type == LL_OUT_BF16;
+      uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (bf) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+          w[j] = *reinterpret_cast<uint32_t*>(&h2);
+        } else {
+          __half2 h2 = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
+          w[j] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+      }
+      if (full && p.d_row16) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<uint4*>(dp + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < p.N) dp[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+      }
+    }
+  }
 }
 
 template <class Cfg, uint32_t AB_FMT>
@@ -397,7 +467,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int q = warp & 3;
     const int h = ew >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    float* st = epi_stage + ew * 32 * 32;
     uint32_t pit = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -449,8 +518,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ++pit;
       }
       if (!ok) break;
-#pragma unroll
-      for (int c = 0; c < CH; ++c) epilogue_chunk<4>(p, st, mb * 128 + q * 32, ncol0 + c * 32, acc[c], lane);
+      epilogue_rows<CH>(p, m, ncol0, acc);
     }
   }
 
@@ -486,7 +554,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 // a scale warp stages that block's scale_a (this CTA's 128 rows) and scale_b (the
 // tile's two 128-column blocks) into a shared-memory ring with cp.async, and 8
 // promotion warps add scale_a * scale_b * partial into FP32 registers (32 rows x 128
-// columns per warp), then store the tile straight from registers.
+// columns per warp), then store the tile straight from registers.  The two partial
+// buffers fill TMEM, so a buffer must be read and handed back within one block's MMA
+// time (measured: 16 warps of 64 columns were slower, twice the hand-back arrivals).
 template <int BN_, bool FP8_>
 struct PairCfg {
   static constexpr int BN = BN_;  // pair tile N
@@ -521,74 +591,6 @@ struct PairSched {
   int full_units;     // units that are whole tiles
   int num_units;      // full_units + 2 * split tiles
 };
-
-// FP8 epilogue straight from registers: lane = one row, acc = 4 x 32 consecutive
-// columns from n0.  D = alpha * acc + beta * C.
-template <int CH>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0,
-                                              const float (&acc)[CH][32]) {
-  if (m >= p.M) return;
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int n = n0 + 32 * c;
-    if (n >= p.N) break;
-    const bool full = n + 32 <= p.N;
-    float o[32];
-    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
-    if (p.beta != 0.0f && full && p.c_vec) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 cv = *reinterpret_cast<const float4*>(crow + j);
-        o[j] = p.alpha * acc[c][j] + p.beta * cv.x;
-        o[j + 1] = p.alpha * acc[c][j + 1] + p.beta * cv.y;
-        o[j + 2] = p.alpha * acc[c][j + 2] + p.beta * cv.z;
-        o[j + 3] = p.alpha * acc[c][j + 3] + p.beta * cv.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        o[j] = p.alpha * acc[c][j];
-        if (p.beta != 0.0f && n + j < p.N) o[j] += p.beta * crow[j];
-      }
-    }
-    const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
-    if (p.d_type == LL_OUT_F32) {
-      float* dp = static_cast<float*>(p.D) + off;
-      if (full && p.d_row16) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n + j < p.N) dp[j] = o[j];
-      }
-    } else {
-      const bool bf = p.d_type == LL_OUT_BF16;
-      uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (bf) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-          w[j] = *reinterpret_cast<uint32_t*>(&h2);
-        } else {
-          __half2 h2 = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
-          w[j] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-      }
-      if (full && p.d_row16) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<uint4*>(dp + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n + j < p.N) dp[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
-      }
-    }
-  }
-}
 
 template <class Cfg, uint32_t AB_FMT>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
@@ -828,11 +830,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- promotion (FP8, each CTA)
-    constexpr int HALF = BN / 2;  // columns per promotion warp
+    constexpr int GROUPS = Cfg::EPI_WARPS / 4;  // warps per TMEM lane quarter
+    constexpr int HALF = BN / GROUPS;           // columns per promotion warp
     constexpr int CH = HALF / 32;
     const int ew = warp - Cfg::EPI_WARP0;
     const int q = warp & 3;
     const int h = ew >> 2;
+    const int sb_idx = (h * HALF) / 128;  // which of the tile's 128-column scale blocks
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t pit = 0, seq = 0;
     bool ok = true;
@@ -857,7 +861,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         tc_fence_after();
         const float* slot = scales + j * Cfg::SC_FLOATS;
-        const float s = slot[q * 32 + lane] * slot[128 + h];
+        const float s = slot[q * 32 + lane] * slot[128 + sb_idx];
         __syncwarp();
         if (lane == 0) mbar_arrive(sc_empty_bar(j));
         // 16 columns per TMEM load keep 128 accumulators + staging within the
