@@ -17,6 +17,10 @@ Functions and the passages they follow:
   factors per tensor, row or block; 1x128 blocks of A, 128x128 blocks of B.
 * ``gemv_w8a8`` -- "NVIDIA A100: chip to SIMT", sections 5.1-5.2: int8 x int8
   summed exactly, then y = fp16(float(z) * s_x * s_W[o]).
+* ``quantize_per_token_f16`` -- same page, 5.1: the activation is quantised per token
+  at run time (symmetric, s = amax / 127, zero point 0).
+* ``gemv_w8a8_ex`` -- same page, 5.1: optional bias in the float epilogue, or an INT8
+  requantised output for a next layer that takes INT8.
 """
 import ctypes
 import os
@@ -52,6 +56,11 @@ def lib():
                                                ctypes.c_double, vp, i64, vp, i64, vp, i64,
                                                vp, i64, ctypes.c_double, vp, i64, vp,
                                                ctypes.c_int, vp, vp]
+        L.orc_quantize_per_token_f16.restype = ctypes.c_int
+        L.orc_quantize_per_token_f16.argtypes = [ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp]
+        L.orc_gemv_w8a8_ex.restype = ctypes.c_int
+        L.orc_gemv_w8a8_ex.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_float, vp, i64, vp,
+                                       vp, ctypes.c_int, ctypes.c_float, vp, vp, vp]
         L.orc_gemv_w8a8.restype = ctypes.c_int
         L.orc_gemv_w8a8.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_float, vp, i64,
                                     vp, vp, vp]
@@ -141,6 +150,37 @@ def gemv_w8a8(N, K, x, s_x, W, ldw, s_W):
     if rc != 0:
         raise ValueError("orc_gemv_w8a8 failed with code %d" % rc)
     return z, y.view(np.float16)
+
+
+def quantize_per_token_f16(M, K, x_bits, ldx=None):
+    """(q int8 M x K, s float32 [M]) from FP16 bits x (M x ldx)."""
+    ldx = K if ldx is None else ldx
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    q = np.zeros((M, K), dtype=np.int8)
+    s = np.zeros(M, dtype=np.float32)
+    rc = lib().orc_quantize_per_token_f16(M, K, _ptr(x), ldx, _ptr(q), K, _ptr(s))
+    if rc != 0:
+        raise ValueError("orc_quantize_per_token_f16 failed with code %d" % rc)
+    return q, s
+
+
+def gemv_w8a8_ex(N, K, x, s_x, W, ldw, s_W, bias=None, out_int8=False, s_y=1.0):
+    """(z int64 [N], y) with y FP16 [N] or int8 [N] (out_int8)."""
+    x = np.ascontiguousarray(x, dtype=np.int8)
+    W = np.ascontiguousarray(W, dtype=np.int8)
+    s_W = np.ascontiguousarray(s_W, dtype=np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    z = np.zeros(N, dtype=np.int64)
+    y16 = np.zeros(N, dtype=np.uint16)
+    y8 = np.zeros(N, dtype=np.int8)
+    rc = lib().orc_gemv_w8a8_ex(N, K, _ptr(x), float(np.float32(s_x)), _ptr(W), ldw, _ptr(s_W),
+                                _ptr(b), 1 if out_int8 else 0, float(np.float32(s_y)), _ptr(z),
+                                _ptr(y16), _ptr(y8))
+    if rc == 5:
+        raise OverflowError("W8A8 dot product exceeds the INT32 range")
+    if rc != 0:
+        raise ValueError("orc_gemv_w8a8_ex failed with code %d" % rc)
+    return z, (y8 if out_int8 else y16.view(np.float16))
 
 
 def threads_used() -> int:

@@ -248,3 +248,71 @@ int orc_gemv_w8a8(int N, int K, const int8_t* x, float s_x, const int8_t* W, int
   }
   return bad ? 5 : 0;
 }
+
+/* ------------------------------------------------------------------ W8A8 neighbours */
+
+/*
+ * Symmetric per-token activation quantiser (A100 page, section 5.1: the activation is
+ * quantised at run time by the preceding operator or a separate quantisation step,
+ * per-token scale s_x, zero point 0).  Reading: for each row i of x (FP16 bits,
+ * M x K, pitch ldx)
+ *   s_x[i] = amax_k |x[i][k]| / 127            (FP32 division; 1 for an all-zero row)
+ *   q[i][k] = clamp(rint(x[i][k] / s_x[i]), -127, 127)   (FP32 division, ties to even)
+ * q is int8 M x K (pitch ldq); s is FP32 [M].
+ */
+int orc_quantize_per_token_f16(int M, int K, const uint16_t* x, int64_t ldx, int8_t* q, int64_t ldq,
+                               float* s) {
+  if (M < 0 || K < 0) return 1;
+  for (int64_t i = 0; i < M; ++i) {
+    double amax = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double v = fabs(orc_decode_f16(x[i * ldx + k]));
+      if (v > amax) amax = v;
+    }
+    const float si = (amax > 0.0) ? (float)amax / 127.0f : 1.0f;
+    s[i] = si;
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = (float)orc_decode_f16(x[i * ldx + k]);
+      float r = nearbyintf(v / si);
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+      q[i * ldq + k] = (int8_t)r;
+    }
+  }
+  return 0;
+}
+
+/*
+ * W8A8 GEMV with the epilogue variants of the A100 page, section 5.1 (an optional bias
+ * added in the floating-point epilogue after dequantisation; or requantisation to INT8
+ * for a next layer that takes INT8 instead of writing FP16):
+ *   v[o] = (float(z[o]) * s_x) * s_W[o]      (as orc_gemv_w8a8)
+ *   v[o] = v[o] + bias[o]                     (FP32 add; only when bias != NULL)
+ *   out_int8 == 0: y16[o] = fp16_rn(v[o])
+ *   out_int8 != 0: y8[o]  = clamp(rint(v[o] / s_y), -127, 127)   (FP32 division, ties to even)
+ */
+int orc_gemv_w8a8_ex(int N, int K, const int8_t* x, float s_x, const int8_t* W, int64_t ldw,
+                     const float* s_W, const float* bias, int out_int8, float s_y, int64_t* z,
+                     uint16_t* y16, int8_t* y8) {
+  if (N < 0 || K < 0) return 1;
+  int bad = 0;
+  for (int o = 0; o < N; ++o) {
+    int64_t acc = 0;
+    for (int64_t k = 0; k < K; ++k) acc += (int64_t)x[k] * (int64_t)W[(int64_t)o * ldw + k];
+    if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;
+    if (z) z[o] = acc;
+    float v = (float)(int32_t)acc;
+    v = v * s_x;
+    v = v * s_W[o];
+    if (bias) v = v + bias[o];
+    if (out_int8) {
+      float r = nearbyintf(v / s_y);
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+      if (y8) y8[o] = (int8_t)r;
+    } else if (y16) {
+      y16[o] = orc_encode_f16_rn((double)v);
+    }
+  }
+  return bad ? 5 : 0;
+}

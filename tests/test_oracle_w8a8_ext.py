@@ -1,0 +1,106 @@
+"""Pins of the W8A8 neighbours in the oracle ("NVIDIA A100: chip to SIMT", section 5.1):
+the per-token activation quantiser (symmetric, s = amax / 127, zero point 0) and the
+GEMV epilogue variants (bias in the float epilogue; INT8 requantised output).
+
+Checks: integer-valued tokens with amax 127 quantise to themselves with s = 1; sign
+symmetry; all-zero tokens; the round-trip error bound |x - q s| <= s / 2; the amax
+element maps to +-127; the numpy float32 sequence bit for bit; bias = 0 and no bias
+agree with the plain GEMV; W = 0 gives fp16(bias); INT8 requantisation against numpy
+and its clamp.
+"""
+import numpy as np
+import pytest
+
+import workloads as wl
+
+
+def _f16(vals):
+    return np.asarray(vals, dtype=np.float64).astype(np.float16)
+
+
+def test_quantize_integer_token_is_identity(orc):
+    rng = np.random.default_rng(401)
+    x = rng.integers(-127, 128, size=(3, 50)).astype(np.float64)
+    x[:, 7] = 127.0  # amax 127 in every row
+    q, s = orc.quantize_per_token_f16(3, 50, _f16(x).view(np.uint16))
+    assert np.all(s == 1.0)
+    assert np.array_equal(q.astype(np.int64), x.astype(np.int64))
+
+
+def test_quantize_symmetry_zero_rows_and_bounds(orc):
+    rng = np.random.default_rng(402)
+    x = _f16(rng.standard_normal((4, 300)) * 3.0)
+    x[2] = 0.0
+    q, s = orc.quantize_per_token_f16(4, 300, x.view(np.uint16))
+    qn, sn = orc.quantize_per_token_f16(4, 300, (-x).view(np.uint16))
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+    assert s[2] == 1.0 and np.all(q[2] == 0)
+    xf = x.astype(np.float64)
+    for i in (0, 1, 3):
+        assert np.max(np.abs(q[i])) == 127
+        assert q[i][np.argmax(np.abs(xf[i]))] == np.sign(xf[i][np.argmax(np.abs(xf[i]))]) * 127
+        assert np.all(np.abs(xf[i] - q[i] * float(s[i])) <= 0.5 * float(s[i]) * (1 + 1e-6))
+
+
+def test_quantize_matches_numpy_float32_sequence(orc):
+    rng = np.random.default_rng(403)
+    x = _f16(rng.standard_normal((5, 4096)))
+    q, s = orc.quantize_per_token_f16(5, 4096, x.view(np.uint16))
+    xf = x.astype(np.float32)
+    amax = np.max(np.abs(xf), axis=1)
+    sn = (amax / np.float32(127.0)).astype(np.float32)
+    qn = np.clip(np.rint(xf / sn[:, None]), -127, 127).astype(np.int8)
+    assert np.array_equal(s, sn)
+    assert np.array_equal(q, qn)
+
+
+def test_quantize_padded_pitch(orc):
+    x = _f16(np.random.default_rng(404).standard_normal((2, 40)))
+    xp = np.full((2, 48), 0x7C00, np.uint16)  # +inf in the padding must not be read
+    xp[:, :40] = x.view(np.uint16)
+    q1, s1 = orc.quantize_per_token_f16(2, 40, x.view(np.uint16))
+    q2, s2 = orc.quantize_per_token_f16(2, 40, xp, ldx=48)
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+
+
+def test_gemv_ex_without_variants_is_plain_gemv(orc):
+    N, K = 70, 512
+    x, sx, W, sW = wl.gemv_inputs(N, K)
+    z0, y0 = orc.gemv_w8a8(N, K, x, sx, W, K, sW)
+    z1, y1 = orc.gemv_w8a8_ex(N, K, x, sx, W, K, sW)
+    z2, y2 = orc.gemv_w8a8_ex(N, K, x, sx, W, K, sW, bias=np.zeros(N, np.float32))
+    assert np.array_equal(z0, z1) and np.array_equal(y0.view(np.uint16), y1.view(np.uint16))
+    assert np.array_equal(y0.view(np.uint16), y2.view(np.uint16))
+
+
+def test_gemv_ex_bias_only(orc):
+    N, K = 9, 64
+    bias = np.random.default_rng(405).standard_normal(N).astype(np.float32)
+    _, y = orc.gemv_w8a8_ex(N, K, np.ones(K, np.int8), 0.01, np.zeros((N, K), np.int8), K,
+                            np.full(N, 0.5, np.float32), bias=bias)
+    assert np.array_equal(y.view(np.uint16), bias.astype(np.float16).view(np.uint16))
+
+
+def test_gemv_ex_bias_and_int8_against_numpy(orc):
+    N, K = 300, 4096
+    x, sx, W, sW = wl.gemv_inputs(N, K)
+    bias = (np.random.default_rng(406).standard_normal(N) * 4).astype(np.float32)
+    zn = W.astype(np.int64) @ x.astype(np.int64)
+    v = (zn.astype(np.float32) * np.float32(sx)) * sW + bias
+    z, y16 = orc.gemv_w8a8_ex(N, K, x, sx, W, K, sW, bias=bias)
+    assert np.array_equal(z, zn)
+    assert np.array_equal(y16.view(np.uint16), v.astype(np.float16).view(np.uint16))
+    s_y = np.float32(0.05)
+    _, y8 = orc.gemv_w8a8_ex(N, K, x, sx, W, K, sW, bias=bias, out_int8=True, s_y=s_y)
+    assert np.array_equal(y8, np.clip(np.rint(v / s_y), -127, 127).astype(np.int8))
+    assert np.any(np.abs(y8) == 127)  # the clamp is exercised
+
+
+def test_gemv_ex_int8_identity_scale(orc):
+    # s_x = s_W = s_y = 1 and small z: the requantised output is z itself
+    N, K = 5, 16
+    x = np.ones(K, np.int8)
+    W = np.zeros((N, K), np.int8)
+    W[:, 0] = np.array([-3, -1, 0, 2, 7], np.int8)
+    _, y8 = orc.gemv_w8a8_ex(N, K, x, 1.0, W, K, np.ones(N, np.float32), out_int8=True, s_y=1.0)
+    assert list(y8) == [-3, -1, 0, 2, 7]
