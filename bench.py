@@ -402,6 +402,68 @@ def bench_gemv(args, dev, stream, peaks, peak_src):
             "status": ll.status_string(st)}
 
 
+def bench_gemv_fused(args, dev, stream, peaks, peak_src):
+    """FP16 activation -> fused per-token quantiser + W8A8 GEMV + bias, FP16 out."""
+    import numpy as np
+    import torch
+
+    import linear_layer_gb300 as ll
+    import workloads as wl
+    cfg = wl.WORKLOADS["w8a8_gemv_4096x11008"]
+    N, K = cfg["N"], cfg["K"]
+    _, _, W, sW = wl.gemv_inputs(N, K)
+    xh = np.random.default_rng(wl.SEED_X).standard_normal(K).astype(np.float16)
+    bias = np.random.default_rng(wl.SEED_C).standard_normal(N).astype(np.float32)
+    wbytes = N * K + 2 * K + 4 * N + 4 * N + 2 * N + K + 4  # W, x fp16, s_W, bias, y, x_q, s_x
+    ncopies = max(2, math.ceil(4 * L2_BYTES / wbytes))
+    tW0 = _up(W, dev)
+    copies = []
+    for _ in range(ncopies):
+        copies.append((torch.from_numpy(xh).to(dev), torch.empty(K, dtype=torch.int8, device=dev),
+                       torch.empty(1, device=dev), tW0.clone(), _up(sW, dev), _up(bias, dev),
+                       torch.empty(N, dtype=torch.float16, device=dev)))
+    del tW0
+
+    def call(i):
+        tx, txq, txs, tw, tsw, tb, ty = copies[i % ncopies]
+        ll.linear_f16_w8a8_gemv(N, K, tx, txq, txs, tw, K, tsw, tb, ll.GEMV_OUT_F16, None, ty,
+                                stream=stream)
+
+    for i in range(5):
+        call(i)
+    torch.cuda.synchronize(dev)
+    per_graph = ncopies * 20
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(per_graph):
+                call(i)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(3, min(20, args.steps // 10 + 3))
+
+    def replay(_):
+        with torch.cuda.stream(stream):
+            g.replay()
+
+    total_ms, _ = time_events(replay, reps, stream)
+    launch_s = total_ms / 1e3 / (reps * per_graph)
+    gbs = wbytes / launch_s / 1e9
+    peak = peaks["hbm_gbs"]
+    st, _ = ll.get_device_status(stream)
+    return {"metric": "FP16-activation W8A8 GEMV (fused per-token quantiser + bias) HBM GB/s",
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_launch": round(launch_s * 1e6, 3),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "kernel": "gemv_w8a8_kernel<true>", "peak_source": peak_src + " hbm_gbs",
+                         "algorithmic_bytes_per_launch": wbytes},
+            "timing": "CUDA graph of %d launches over %d weight copies, %d replays" % (
+                per_graph, ncopies, reps),
+            "status": ll.status_string(st)}
+
+
 def bench_fp8(args, dev, stream, peaks, peak_src):
     import torch
 
@@ -556,7 +618,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the GEMV / FP8 / ragged lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "gemv", "fp8", "ragged"], default="all",
+    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged"], default="all",
                     help="all = the contract line; otherwise time one other kernel and print its object")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -573,7 +635,8 @@ def main(argv=None):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=dev)
 
-    single = {"gemv": bench_gemv, "fp8": bench_fp8, "ragged": bench_ragged}.get(args.workload)
+    single = {"gemv": bench_gemv, "gemv_fused": bench_gemv_fused, "fp8": bench_fp8,
+              "ragged": bench_ragged}.get(args.workload)
     if single is not None:
         res = single(args, dev, stream, peaks, peak_src)
         if rank == 0:
@@ -584,6 +647,8 @@ def main(argv=None):
     extra = {}
     if not args.no_extra:
         extra["w8a8_gemv_4096x11008"] = bench_gemv(args, dev, stream, peaks, peak_src)
+        extra["f16_act_w8a8_gemv_fused_4096x11008"] = bench_gemv_fused(args, dev, stream, peaks,
+                                                                       peak_src)
         extra["e4m3_gemm_8192"] = bench_fp8(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_4093x5003x2056"] = bench_ragged(args, dev, stream, peaks, peak_src)
     barrier(dev)

@@ -182,6 +182,57 @@ ll_status ll_linear_w8a8_gemv(int N, int K, const int8_t* x, const float* x_scal
                               const int8_t* W, int64_t ldw, const float* w_scale, void* y,
                               int32_t* z_out, ll_stream_t stream);
 
+/* Output of the W8A8 GEMV variants. */
+typedef enum { LL_GEMV_OUT_F16 = 0, LL_GEMV_OUT_I8 = 1 } ll_gemv_out_type;
+
+/*
+ * W8A8 GEMV with the epilogue variants of the A100 page, section 5.1 (an optional
+ * bias is added in the floating-point epilogue after dequantisation; a next layer
+ * that takes INT8 can receive a requantised INT8 output instead of FP16):
+ *
+ *   v[o] = (float(z[o]) * x_scale) * w_scale[o]          (as ll_linear_w8a8_gemv)
+ *   v[o] = v[o] + bias[o]                                 (when bias != NULL; FP32 add)
+ *   y_type == LL_GEMV_OUT_F16: y[o] = fp16_rn(v[o])                    (y FP16 [N])
+ *   y_type == LL_GEMV_OUT_I8:  y[o] = clamp(rint(v[o] / *y_scale), -127, 127)   (y int8 [N])
+ *
+ *   bias    : N FP32 or NULL          y_scale : device pointer to one FP32 (INT8 output)
+ * Other arguments, ordering and errors as ll_linear_w8a8_gemv; LL_ERR_INVALID_ARG also
+ * for an unknown y_type or a NULL y_scale with INT8 output.
+ */
+ll_status ll_linear_w8a8_gemv_ex(int N, int K, const int8_t* x, const float* x_scale,
+                                 const int8_t* W, int64_t ldw, const float* w_scale,
+                                 const float* bias, int y_type, const float* y_scale, void* y,
+                                 int32_t* z_out, ll_stream_t stream);
+
+/*
+ * Symmetric per-token activation quantiser (A100 page, section 5.1: the activation is
+ * quantised at run time by the preceding operator or a separate quantisation step):
+ *
+ *   scale[i] = amax_k |x[i][k]| / 127        (FP32; 1 for an all-zero row)
+ *   q[i][k]  = clamp(rint(x[i][k] / scale[i]), -127, 127)   (FP32 division, ties to even)
+ *
+ *   x : M x K FP16 (ldx >= K)    q : M x K int8 (ldq >= K)    scale : M FP32
+ * M == 0: nothing.  Errors: LL_ERR_INVALID_ARG for negative sizes, ld < K, NULL pointers.
+ */
+ll_status ll_quantize_per_token_f16(int M, int K, const void* x, int64_t ldx, int8_t* q,
+                                    int64_t ldq, float* scale, ll_stream_t stream);
+
+/*
+ * The batch-1 linear layer on an FP16 activation: the per-token quantiser fused into
+ * the W8A8 GEMV (every CTA quantises x into its shared memory; the int8 activation
+ * never goes through HBM on the way to the dot products).  Results are bit-identical to
+ * ll_quantize_per_token_f16 (M = 1) followed by ll_linear_w8a8_gemv_ex.
+ *
+ *   x       : K FP16 (the activation of one token)
+ *   x_q     : K int8, written with the quantised activation (required)
+ *   x_scale : one FP32, written with its scale (required)
+ *   other arguments, ordering and errors as ll_linear_w8a8_gemv_ex.
+ */
+ll_status ll_linear_f16_w8a8_gemv(int N, int K, const void* x, int8_t* x_q, float* x_scale,
+                                  const int8_t* W, int64_t ldw, const float* w_scale,
+                                  const float* bias, int y_type, const float* y_scale, void* y,
+                                  int32_t* z_out, ll_stream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /*

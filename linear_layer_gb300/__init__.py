@@ -12,6 +12,9 @@ gemm_f16             ll_gemm_f16
 gemm_bf16            ll_gemm_bf16
 gemm_fp8_blockscaled ll_gemm_fp8_blockscaled
 linear_w8a8_gemv     ll_linear_w8a8_gemv
+linear_w8a8_gemv_ex  ll_linear_w8a8_gemv_ex
+linear_f16_w8a8_gemv ll_linear_f16_w8a8_gemv
+quantize_per_token_f16 ll_quantize_per_token_f16
 gemm_f16_noalloc     ll_gemm_f16_noalloc
 gemm_workspace_size  ll_gemm_workspace_size
 get_device_status    ll_get_device_status
@@ -27,12 +30,14 @@ LIB_PATH = os.path.join(_HERE, "lib", "liblinear_layer_gb300.so")
 LL_OK, LL_ERR_INVALID_ARG, LL_ERR_MISALIGNED, LL_ERR_UNSUPPORTED = 0, 1, 2, 3
 LL_ERR_WORKSPACE, LL_ERR_CUDA, LL_ERR_DEVICE_TIMEOUT, LL_ERR_NO_DEVICE = 4, 5, 6, 7
 IN_F16, IN_BF16, IN_E4M3 = 0, 1, 2
+GEMV_OUT_F16, GEMV_OUT_I8 = 0, 1
 OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 
 # every symbol the header declares
 EXPORTS = ["ll_gemm_workspace_size", "ll_gemm_f16", "ll_gemm_bf16", "ll_gemm_fp8_blockscaled",
            "ll_gemm_f16_noalloc",
-           "ll_linear_w8a8_gemv", "ll_get_device_status", "ll_set_wait_timeout_ns",
+           "ll_linear_w8a8_gemv", "ll_linear_w8a8_gemv_ex", "ll_linear_f16_w8a8_gemv",
+           "ll_quantize_per_token_f16", "ll_get_device_status", "ll_set_wait_timeout_ns",
            "ll_debug_timeout_probe", "ll_status_string", "ll_version"]
 
 
@@ -61,6 +66,12 @@ def _load():
                                           f32, vp, i64, vp, i64, i32, vp, ctypes.c_size_t, vp]
     L.ll_linear_w8a8_gemv.restype = i32
     L.ll_linear_w8a8_gemv.argtypes = [i32, i32, vp, vp, vp, i64, vp, vp, vp, vp]
+    L.ll_linear_w8a8_gemv_ex.restype = i32
+    L.ll_linear_w8a8_gemv_ex.argtypes = [i32, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp, vp, vp]
+    L.ll_linear_f16_w8a8_gemv.restype = i32
+    L.ll_linear_f16_w8a8_gemv.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp, vp, i32, vp, vp, vp, vp]
+    L.ll_quantize_per_token_f16.restype = i32
+    L.ll_quantize_per_token_f16.argtypes = [i32, i32, vp, i64, vp, i64, vp, vp]
     L.ll_get_device_status.restype = i32
     L.ll_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.ll_set_wait_timeout_ns.restype = i32
@@ -156,6 +167,25 @@ def gemm_fp8_blockscaled(M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb, scale_b
 def linear_w8a8_gemv(N, K, x, x_scale, W, ldw, w_scale, y, z_out=None, stream=None):
     return _check(lib.ll_linear_w8a8_gemv(N, K, _p(x), _p(x_scale), _p(W), ldw, _p(w_scale), _p(y),
                                           _p(z_out), _stream(stream)), "ll_linear_w8a8_gemv")
+
+
+def linear_w8a8_gemv_ex(N, K, x, x_scale, W, ldw, w_scale, bias, y_type, y_scale, y, z_out=None,
+                        stream=None):
+    return _check(lib.ll_linear_w8a8_gemv_ex(N, K, _p(x), _p(x_scale), _p(W), ldw, _p(w_scale),
+                                             _p(bias), y_type, _p(y_scale), _p(y), _p(z_out),
+                                             _stream(stream)), "ll_linear_w8a8_gemv_ex")
+
+
+def linear_f16_w8a8_gemv(N, K, x, x_q, x_scale, W, ldw, w_scale, bias, y_type, y_scale, y,
+                         z_out=None, stream=None):
+    return _check(lib.ll_linear_f16_w8a8_gemv(N, K, _p(x), _p(x_q), _p(x_scale), _p(W), ldw,
+                                              _p(w_scale), _p(bias), y_type, _p(y_scale), _p(y),
+                                              _p(z_out), _stream(stream)), "ll_linear_f16_w8a8_gemv")
+
+
+def quantize_per_token_f16(M, K, x, ldx, q, ldq, scale, stream=None):
+    return _check(lib.ll_quantize_per_token_f16(M, K, _p(x), ldx, _p(q), ldq, _p(scale),
+                                                _stream(stream)), "ll_quantize_per_token_f16")
 
 
 def get_device_status(stream=None):

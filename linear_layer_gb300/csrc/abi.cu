@@ -210,6 +210,52 @@ ll_status ll_linear_w8a8_gemv(int N, int K, const int8_t* x, const float* x_scal
   return ll::launch_gemv_w8a8(N, K, x, x_scale, W, ldw, w_scale, y, z_out, ctx);
 }
 
+ll_status ll_linear_w8a8_gemv_ex(int N, int K, const int8_t* x, const float* x_scale,
+                                 const int8_t* W, int64_t ldw, const float* w_scale,
+                                 const float* bias, int y_type, const float* y_scale, void* y,
+                                 int32_t* z_out, ll_stream_t stream) {
+  if (N < 0 || K < 0 || K > 131071) return LL_ERR_INVALID_ARG;
+  if (y_type != LL_GEMV_OUT_F16 && y_type != LL_GEMV_OUT_I8) return LL_ERR_INVALID_ARG;
+  if (N == 0) return LL_OK;
+  if (x_scale == nullptr || w_scale == nullptr || y == nullptr || ldw < K) return LL_ERR_INVALID_ARG;
+  if (K > 0 && (x == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
+  if (y_type == LL_GEMV_OUT_I8 && y_scale == nullptr) return LL_ERR_INVALID_ARG;
+  ll::LaunchCtx ctx;
+  ll_status st = current_ctx(stream, ctx);
+  if (st != LL_OK) return st;
+  return ll::launch_gemv_w8a8_ex(N, K, x, x_scale, nullptr, nullptr, nullptr, W, ldw, w_scale, bias,
+                                 y_type == LL_GEMV_OUT_I8, y_scale, y, z_out, ctx);
+}
+
+ll_status ll_linear_f16_w8a8_gemv(int N, int K, const void* x, int8_t* x_q, float* x_scale,
+                                  const int8_t* W, int64_t ldw, const float* w_scale,
+                                  const float* bias, int y_type, const float* y_scale, void* y,
+                                  int32_t* z_out, ll_stream_t stream) {
+  if (N < 0 || K < 0 || K > 131071) return LL_ERR_INVALID_ARG;
+  if (y_type != LL_GEMV_OUT_F16 && y_type != LL_GEMV_OUT_I8) return LL_ERR_INVALID_ARG;
+  if (N == 0) return LL_OK;
+  if (x_q == nullptr || x_scale == nullptr || w_scale == nullptr || y == nullptr || ldw < K)
+    return LL_ERR_INVALID_ARG;
+  if (K > 0 && (x == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
+  if (y_type == LL_GEMV_OUT_I8 && y_scale == nullptr) return LL_ERR_INVALID_ARG;
+  ll::LaunchCtx ctx;
+  ll_status st = current_ctx(stream, ctx);
+  if (st != LL_OK) return st;
+  return ll::launch_gemv_w8a8_ex(N, K, nullptr, nullptr, x, x_q, x_scale, W, ldw, w_scale, bias,
+                                 y_type == LL_GEMV_OUT_I8, y_scale, y, z_out, ctx);
+}
+
+ll_status ll_quantize_per_token_f16(int M, int K, const void* x, int64_t ldx, int8_t* q,
+                                    int64_t ldq, float* scale, ll_stream_t stream) {
+  if (M < 0 || K < 0 || ldx < K || ldq < K) return LL_ERR_INVALID_ARG;
+  if (M == 0) return LL_OK;
+  if (scale == nullptr || (K > 0 && (x == nullptr || q == nullptr))) return LL_ERR_INVALID_ARG;
+  ll::LaunchCtx ctx;
+  ll_status st = current_ctx(stream, ctx);
+  if (st != LL_OK) return st;
+  return ll::launch_quantize_per_token(M, K, x, ldx, q, ldq, scale, ctx);
+}
+
 ll_status ll_get_device_status(ll_stream_t stream, uint32_t* detail) {
   ll::LaunchCtx ctx;
   ll_status st = current_ctx(stream, ctx);

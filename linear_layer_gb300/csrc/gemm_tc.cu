@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const GemmParams p, const PairSched sc) {
   constexpr int S = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
-  constexpr int J = Cfg::SC_SLOTS;
+  constexpr int J = Cfg::SC_SLOTS > 0 ? Cfg::SC_SLOTS : 1;  // (FP8 scale ring; unused otherwise)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

@@ -34,12 +34,18 @@ constexpr int kGvBatch = 8;  // 16-byte chunks per lane in flight (4 KB per warp
 
 struct GemvParams {
   int N, K;
-  const int8_t* x;
-  const float* x_scale;
+  const int8_t* x;        // int8 activation (or NULL when xh is given)
+  const float* x_scale;   // its scale (device, one float)
+  const __half* xh;       // FP16 activation, quantised in the kernel (fused path)
+  int8_t* xq_out;         // fused path: where CTA 0 stores the quantised activation
+  float* xs_out;          //   and its scale (both optional)
   const int8_t* W;
   int64_t ldw;
   const float* w_scale;
-  __half* y;
+  const float* bias;      // optional, added after dequantisation
+  int out_i8;             // 0: FP16 y; 1: INT8 y requantised with *y_scale
+  const float* y_scale;
+  void* y;
   int32_t* z_out;
 };
 
@@ -49,12 +55,96 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
-__device__ __forceinline__ void dequant_store(const GemvParams& p, int o, int z, float sx) {
+// v = (float(z) * s_x) * s_W[o] (+ bias[o]); y = fp16_rn(v), or
+// y = clamp(rint(v / s_y), -127, 127) for an INT8 next layer.
+__device__ __forceinline__ void dequant_store(const GemvParams& p, int o, int z, float sx, float sw,
+                                              float sy) {
   if (p.z_out) p.z_out[o] = z;
   const float f = __int2float_rn(z);
   const float t = __fmul_rn(f, sx);
-  const float u = __fmul_rn(t, p.w_scale[o]);
-  p.y[o] = __float2half_rn(u);
+  float u = __fmul_rn(t, sw);
+  if (p.bias) u = __fadd_rn(u, p.bias[o]);
+  if (p.out_i8) {
+    const int r = __float2int_rn(__fdiv_rn(u, sy));
+    static_cast<int8_t*>(p.y)[o] = static_cast<int8_t>(max(-127, min(127, r)));
+  } else {
+    static_cast<__half*>(p.y)[o] = __float2half_rn(u);
+  }
+}
+
+// Symmetric per-token quantisation of one row of K FP16 values by the whole CTA:
+// s = amax / 127 (1 for an all-zero row), q = clamp(rint(x / s), -127, 127), each
+// step one FP32 operation rounded to nearest even.  q goes to shared memory `xq`;
+// returns s.  `red` is 32 floats of shared scratch.  When x is 16-byte aligned, K is a
+// multiple of 8 and the row fits VEC_MAX 8-element chunks per thread, each thread
+// loads its chunks once (16-byte loads) and keeps them in registers for both passes.
+template <int THREADS>
+__device__ __forceinline__ float block_amax(float amax, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < THREADS / 32 ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  return red[0];
+}
+
+__device__ __forceinline__ int8_t quant1(float v, float s) {
+  const int r = __float2int_rn(__fdiv_rn(v, s));
+  return static_cast<int8_t>(max(-127, min(127, r)));
+}
+
+template <int THREADS>
+__device__ __forceinline__ float quantize_row_to_smem(const __half* x, int K, int8_t* xq, float* red) {
+  constexpr int VEC_MAX = 4;
+  if ((reinterpret_cast<uintptr_t>(x) % 16 == 0) && (K % 8 == 0) && K <= THREADS * 8 * VEC_MAX) {
+    const int nvec = K / 8;
+    uint4 v[VEC_MAX];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VEC_MAX; ++j) {
+      const int c = threadIdx.x + j * THREADS;
+      v[j] = c < nvec ? reinterpret_cast<const uint4*>(x)[c] : make_uint4(0, 0, 0, 0);
+      const __half2* h = reinterpret_cast<const __half2*>(&v[j]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h[e]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+    const float a = block_amax<THREADS>(amax, red);
+    const float s = a > 0.0f ? __fdiv_rn(a, 127.0f) : 1.0f;
+#pragma unroll
+    for (int j = 0; j < VEC_MAX; ++j) {
+      const int c = threadIdx.x + j * THREADS;
+      if (c < nvec) {
+        const __half2* h = reinterpret_cast<const __half2*>(&v[j]);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h[e]);
+          const uint32_t pair = static_cast<uint8_t>(quant1(f.x, s)) | (static_cast<uint32_t>(static_cast<uint8_t>(quant1(f.y, s))) << 8);
+          if (e < 2)
+            lo |= pair << (16 * e);
+          else
+            hi |= pair << (16 * (e - 2));
+        }
+        reinterpret_cast<uint2*>(xq)[c] = make_uint2(lo, hi);
+      }
+    }
+    return s;
+  }
+  float amax = 0.0f;
+  for (int k = threadIdx.x; k < K; k += THREADS) amax = fmaxf(amax, fabsf(__half2float(x[k])));
+  const float a = block_amax<THREADS>(amax, red);
+  const float s = a > 0.0f ? __fdiv_rn(a, 127.0f) : 1.0f;
+  for (int k = threadIdx.x; k < K; k += THREADS) xq[k] = quant1(__half2float(x[k]), s);
+  return s;
 }
 
 __device__ __forceinline__ int4 ld_stream(const int4* p) {
@@ -75,8 +165,10 @@ __device__ __forceinline__ void load_batch(int4 (&w)[kGvBatch], const int4* row,
   }
 }
 
+template <bool XF16>
 __global__ void __launch_bounds__(kGvThreads, kGvCtasPerSm) gemv_w8a8_kernel(const GemvParams p) {
   extern __shared__ int4 xs[];  // x, K bytes
+  __shared__ float red[32];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int G = gridDim.x * (kGvThreads / 32);
@@ -86,9 +178,21 @@ __global__ void __launch_bounds__(kGvThreads, kGvCtasPerSm) gemv_w8a8_kernel(con
   if (r < p.N) load_batch(w, reinterpret_cast<const int4*>(p.W + static_cast<int64_t>(r) * p.ldw), 0, nch, lane);
 
   asm volatile("griddepcontrol.wait;" ::: "memory");  // x / outputs: after preceding work
-  for (int i = threadIdx.x; i < nch; i += kGvThreads) xs[i] = reinterpret_cast<const int4*>(p.x)[i];
-  __syncthreads();
-  const float sx = *p.x_scale;
+  float sx;
+  if (XF16) {  // fused upstream quantiser: every CTA quantises x into its shared memory
+    sx = quantize_row_to_smem<kGvThreads>(p.xh, p.K, reinterpret_cast<int8_t*>(xs), red);
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      if (p.xq_out)
+        for (int i = threadIdx.x; i < nch; i += kGvThreads) reinterpret_cast<int4*>(p.xq_out)[i] = xs[i];
+      if (p.xs_out && threadIdx.x == 0) *p.xs_out = sx;
+    }
+  } else {
+    for (int i = threadIdx.x; i < nch; i += kGvThreads) xs[i] = reinterpret_cast<const int4*>(p.x)[i];
+    __syncthreads();
+    sx = *p.x_scale;
+  }
+  const float sy = p.out_i8 ? *p.y_scale : 1.0f;
 
   while (r < p.N) {
     const int4* row = reinterpret_cast<const int4*>(p.W + static_cast<int64_t>(r) * p.ldw);
@@ -113,7 +217,7 @@ __global__ void __launch_bounds__(kGvThreads, kGvCtasPerSm) gemv_w8a8_kernel(con
     if (rn < p.N)  // next row in flight while this one is reduced and stored
       load_batch(w, reinterpret_cast<const int4*>(p.W + static_cast<int64_t>(rn) * p.ldw), 0, nch, lane);
     const int z = warp_sum(acc0 + acc1);
-    if (lane == 0) dequant_store(p, r, z, sx);
+    if (lane == 0) dequant_store(p, r, z, sx, p.w_scale[r], sy);
     r = rn;
   }
 }
@@ -127,30 +231,37 @@ __global__ void __launch_bounds__(256) gemv_w8a8_plain_kernel(const GemvParams p
   int acc = 0;
   for (int k = lane; k < p.K; k += 32) acc += static_cast<int>(p.x[k]) * static_cast<int>(wrow[k]);
   const int z = warp_sum(acc);
-  if (lane == 0) dequant_store(p, o, z, *p.x_scale);
+  if (lane == 0) dequant_store(p, o, z, *p.x_scale, p.w_scale[o], p.out_i8 ? *p.y_scale : 1.0f);
 }
 
-ll_status launch_gemv_w8a8(int N, int K, const int8_t* x, const float* x_scale, const int8_t* W,
-                           int64_t ldw, const float* w_scale, void* y, int32_t* z_out,
-                           const LaunchCtx& ctx) {
-  GemvParams p;
-  p.N = N;
-  p.K = K;
-  p.x = x;
-  p.x_scale = x_scale;
-  p.W = W;
-  p.ldw = ldw;
-  p.w_scale = w_scale;
-  p.y = static_cast<__half*>(y);
-  p.z_out = z_out;
-  const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
-                       (reinterpret_cast<uintptr_t>(W) % 16 == 0) && (K % 16 == 0) &&
-                       (ldw % 16 == 0);
+// Per-token quantiser, one CTA per row (x FP16 M x ldx -> q int8 M x ldq, s FP32 [M]).
+__global__ void __launch_bounds__(256) quantize_per_token_kernel(int M, int K, const __half* x,
+                                                                 int64_t ldx, int8_t* q, int64_t ldq,
+                                                                 float* scale) {
+  extern __shared__ int8_t qrow[];
+  __shared__ float red[32];
+  for (int i = blockIdx.x; i < M; i += gridDim.x) {
+    const float s = quantize_row_to_smem<256>(x + static_cast<int64_t>(i) * ldx, K, qrow, red);
+    __syncthreads();
+    for (int k = threadIdx.x; k < K; k += 256) q[static_cast<int64_t>(i) * ldq + k] = qrow[k];
+    if (threadIdx.x == 0) scale[i] = s;
+    __syncthreads();
+  }
+}
+
+static ll_status launch_gemv(const GemvParams& p0, const LaunchCtx& ctx) {
+  GemvParams p = p0;
+  const int N = p.N, K = p.K;
+  const bool xh = p.xh != nullptr;
+  const bool x_aligned = xh ? (reinterpret_cast<uintptr_t>(p.xh) % 16 == 0)
+                            : (reinterpret_cast<uintptr_t>(p.x) % 16 == 0);
+  const bool aligned = x_aligned && (reinterpret_cast<uintptr_t>(p.W) % 16 == 0) && (K % 16 == 0) &&
+                       (p.ldw % 16 == 0) && (!p.xq_out || reinterpret_cast<uintptr_t>(p.xq_out) % 16 == 0);
   if (aligned && K > 0) {
-    const int smem = K;  // x staged in shared memory (K is a multiple of 16)
+    const int smem = K;  // x staged (as int8) in shared memory (K is a multiple of 16)
+    auto kern = xh ? gemv_w8a8_kernel<true> : gemv_w8a8_kernel<false>;
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(gemv_w8a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return LL_ERR_CUDA;
     int grid = kGvCtasPerSm * ctx.num_sms;
     const int need = (N + kGvThreads / 32 - 1) / (kGvThreads / 32);  // one warp per row at most
@@ -165,13 +276,74 @@ ll_status launch_gemv_w8a8(int N, int K, const int8_t* x, const float* x_scale, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemv_w8a8_kernel, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
       cudaGetLastError();
       return LL_ERR_CUDA;
     }
     return LL_OK;
   }
+  if (xh) {  // unaligned fused request: quantise into the caller's outputs, then the plain GEMV
+    quantize_per_token_kernel<<<1, 256, K > 0 ? K : 1, ctx.stream>>>(1, K, p.xh, K, p.xq_out, K, p.xs_out);
+    if (cudaGetLastError() != cudaSuccess) return LL_ERR_CUDA;
+    p.x = p.xq_out;
+    p.x_scale = p.xs_out;
+    p.xh = nullptr;
+  }
   gemv_w8a8_plain_kernel<<<(N + 7) / 8, 256, 0, ctx.stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+static GemvParams gemv_params(int N, int K, const int8_t* x, const float* x_scale, const int8_t* W,
+                              int64_t ldw, const float* w_scale, void* y, int32_t* z_out) {
+  GemvParams p;
+  p.N = N;
+  p.K = K;
+  p.x = x;
+  p.x_scale = x_scale;
+  p.xh = nullptr;
+  p.xq_out = nullptr;
+  p.xs_out = nullptr;
+  p.W = W;
+  p.ldw = ldw;
+  p.w_scale = w_scale;
+  p.bias = nullptr;
+  p.out_i8 = 0;
+  p.y_scale = nullptr;
+  p.y = y;
+  p.z_out = z_out;
+  return p;
+}
+
+ll_status launch_gemv_w8a8(int N, int K, const int8_t* x, const float* x_scale, const int8_t* W,
+                           int64_t ldw, const float* w_scale, void* y, int32_t* z_out,
+                           const LaunchCtx& ctx) {
+  return launch_gemv(gemv_params(N, K, x, x_scale, W, ldw, w_scale, y, z_out), ctx);
+}
+
+ll_status launch_gemv_w8a8_ex(int N, int K, const int8_t* x, const float* x_scale, const void* xh,
+                              int8_t* xq_out, float* xs_out, const int8_t* W, int64_t ldw,
+                              const float* w_scale, const float* bias, int out_i8,
+                              const float* y_scale, void* y, int32_t* z_out, const LaunchCtx& ctx) {
+  GemvParams p = gemv_params(N, K, x, x_scale, W, ldw, w_scale, y, z_out);
+  p.xh = static_cast<const __half*>(xh);
+  p.xq_out = xq_out;
+  p.xs_out = xs_out;
+  p.bias = bias;
+  p.out_i8 = out_i8;
+  p.y_scale = y_scale;
+  return launch_gemv(p, ctx);
+}
+
+ll_status launch_quantize_per_token(int M, int K, const void* x, int64_t ldx, int8_t* q, int64_t ldq,
+                                    float* scale, const LaunchCtx& ctx) {
+  const int smem = K > 0 ? K : 1;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(quantize_per_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return LL_ERR_CUDA;
+  int grid = M < 8 * ctx.num_sms ? M : 8 * ctx.num_sms;
+  quantize_per_token_kernel<<<grid, 256, smem, ctx.stream>>>(M, K, static_cast<const __half*>(x), ldx, q,
+                                                             ldq, scale);
   return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 

@@ -56,4 +56,16 @@ ll_status launch_gemv_w8a8(int N, int K, const int8_t* x, const float* x_scale, 
                            int64_t ldw, const float* w_scale, void* y, int32_t* z_out,
                            const LaunchCtx& ctx);
 
+// W8A8 GEMV with epilogue variants and the optional fused FP16-activation quantiser
+// (xh != NULL: x and x_scale are ignored; xq_out / xs_out receive the quantised
+// activation and its scale when not NULL, and are required when xh is unaligned).
+ll_status launch_gemv_w8a8_ex(int N, int K, const int8_t* x, const float* x_scale, const void* xh,
+                              int8_t* xq_out, float* xs_out, const int8_t* W, int64_t ldw,
+                              const float* w_scale, const float* bias, int out_i8,
+                              const float* y_scale, void* y, int32_t* z_out, const LaunchCtx& ctx);
+
+// Per-token activation quantiser (gemv_w8a8.cu).
+ll_status launch_quantize_per_token(int M, int K, const void* x, int64_t ldx, int8_t* q, int64_t ldq,
+                                    float* scale, const LaunchCtx& ctx);
+
 }  // namespace ll
