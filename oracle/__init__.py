@@ -15,6 +15,8 @@ Functions and the passages they follow:
   low-precision inputs and a wide accumulator; here alpha*A*B + beta*C in double.
 * ``gemm_fp8_blockscaled`` -- same chapter, "精度" section: FP8 needs scaling
   factors per tensor, row or block; 1x128 blocks of A, 128x128 blocks of B.
+* ``decode_e5m2`` / ``gemm_f8_blockscaled_mixed`` -- "Tensor Core" chapter, table
+  "精度": FP8 E5M2 1/5/2 (wider range, used for gradients) beside E4M3.
 * ``gemv_w8a8`` -- "NVIDIA A100: chip to SIMT", sections 5.1-5.2: int8 x int8
   summed exactly, then y = fp16(float(z) * s_x * s_W[o]).
 * ``quantize_per_token_f16`` -- same page, 5.1: the activation is quantised per token
@@ -43,6 +45,8 @@ def lib():
         L.orc_decode_bf16.argtypes = [ctypes.c_uint16]
         L.orc_decode_e4m3.restype = ctypes.c_double
         L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
+        L.orc_decode_e5m2.restype = ctypes.c_double
+        L.orc_decode_e5m2.argtypes = [ctypes.c_uint8]
         L.orc_encode_f16_rn.restype = ctypes.c_uint16
         L.orc_encode_f16_rn.argtypes = [ctypes.c_double]
         vp = ctypes.c_void_p
@@ -56,6 +60,9 @@ def lib():
                                                ctypes.c_double, vp, i64, vp, i64, vp, i64,
                                                vp, i64, ctypes.c_double, vp, i64, vp,
                                                ctypes.c_int, vp, vp]
+        L.orc_gemm_f8_blockscaled_mixed.restype = ctypes.c_int
+        L.orc_gemm_f8_blockscaled_mixed.argtypes = [ctypes.c_int, ctypes.c_int] + \
+            L.orc_gemm_fp8_blockscaled.argtypes
         L.orc_quantize_per_token_f16.restype = ctypes.c_int
         L.orc_quantize_per_token_f16.argtypes = [ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp]
         L.orc_gemv_w8a8_ex.restype = ctypes.c_int
@@ -85,6 +92,10 @@ def decode_bf16(bits: int) -> float:
 
 def decode_e4m3(bits: int) -> float:
     return lib().orc_decode_e4m3(int(bits) & 0xFF)
+
+
+def decode_e5m2(bits: int) -> float:
+    return lib().orc_decode_e5m2(int(bits) & 0xFF)
 
 
 def encode_f16_rn(v: float) -> int:
@@ -133,6 +144,29 @@ def gemm_fp8_blockscaled(M, N, K, alpha, A, lda, sA, ld_sa, B, ldb, sB, ld_sb, b
                                         ldc, _ptr(rows), len(rows), _ptr(D), _ptr(S))
     if rc != 0:
         raise ValueError("orc_gemm_fp8_blockscaled failed with code %d" % rc)
+    return D, S
+
+
+F8 = {"e4m3": 0, "e5m2": 1}
+
+
+def gemm_f8_blockscaled_mixed(a_fmt, b_fmt, M, N, K, alpha, A, lda, sA, ld_sa, B, ldb, sB, ld_sb,
+                              beta=0.0, C=None, ldc=0, rows=None, want_absab=True):
+    """Block-scaled 8-bit GEMM with per-operand formats ("e4m3" / "e5m2")."""
+    rows = _rows(M, rows)
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    sA = np.ascontiguousarray(sA, dtype=np.float32)
+    sB = np.ascontiguousarray(sB, dtype=np.float32)
+    C = None if C is None else np.ascontiguousarray(C, dtype=np.float32)
+    D = np.zeros((len(rows), N), dtype=np.float64)
+    S = np.zeros((len(rows), N), dtype=np.float64) if want_absab else None
+    rc = lib().orc_gemm_f8_blockscaled_mixed(F8[a_fmt], F8[b_fmt], M, N, K, float(alpha), _ptr(A),
+                                             lda, _ptr(sA), ld_sa, _ptr(B), ldb, _ptr(sB), ld_sb,
+                                             float(beta), _ptr(C), ldc, _ptr(rows), len(rows),
+                                             _ptr(D), _ptr(S))
+    if rc != 0:
+        raise ValueError("orc_gemm_f8_blockscaled_mixed failed with code %d" % rc)
     return D, S
 
 

@@ -83,6 +83,23 @@ double orc_decode_e4m3(uint8_t b) {
   return sign ? -v : v;
 }
 
+/* FP8 E5M2: sign 1, exponent 5 (bias 15), mantissa 2, with infinities and NaNs as in
+ * IEEE binary formats (exponent 31: mantissa 0 = inf, else NaN); largest finite 57344. */
+double orc_decode_e5m2(uint8_t b) {
+  int sign = (b >> 7) & 1;
+  int e = (b >> 2) & 0x1F;
+  int m = b & 0x3;
+  double v;
+  if (e == 31) {
+    v = (m == 0) ? INFINITY : NAN;
+  } else if (e == 0) {
+    v = ldexp((double)m, -16); /* m * 2^(1-15-2) */
+  } else {
+    v = ldexp((double)(4 + m), e - 17); /* (1 + m/4) * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
 /* Round a double to the nearest binary16 (ties to even) and return its bits.
  * Written from the binary16 definition: quantum 2^-24 below 2^-14, otherwise
  * 2^(e-10) for |v| in [2^e, 2^(e+1)); magnitudes that round past 65504 become inf. */
@@ -170,11 +187,32 @@ int orc_gemm(int kind, int M, int N, int K, double alpha, const void* A, int64_t
  * sB is ceil(K/128) x ceil(N/128) (ld_sb), one scale per 128 x 128 block of B.
  * absab[i][j] = sum_k |dec8(A[i][k]) sA[i][k/128]| * |dec8(B[k][j]) sB[k/128][j/128]|.
  */
+static double decode_f8(int fmt, uint8_t b) {
+  return fmt == 1 ? orc_decode_e5m2(b) : orc_decode_e4m3(b);
+}
+
+/* As orc_gemm_fp8_blockscaled, with each operand's 8-bit format chosen separately
+ * (fmt 0 = E4M3, 1 = E5M2). */
+int orc_gemm_f8_blockscaled_mixed(int a_fmt, int b_fmt, int M, int N, int K, double alpha,
+                                  const uint8_t* A, int64_t lda, const float* sA, int64_t ld_sa,
+                                  const uint8_t* B, int64_t ldb, const float* sB, int64_t ld_sb,
+                                  double beta, const float* C, int64_t ldc, const int32_t* rows,
+                                  int nrows, double* D_ref, double* absab);
+
 int orc_gemm_fp8_blockscaled(int M, int N, int K, double alpha, const uint8_t* A, int64_t lda,
                              const float* sA, int64_t ld_sa, const uint8_t* B, int64_t ldb,
                              const float* sB, int64_t ld_sb, double beta, const float* C,
                              int64_t ldc, const int32_t* rows, int nrows, double* D_ref,
                              double* absab) {
+  return orc_gemm_f8_blockscaled_mixed(0, 0, M, N, K, alpha, A, lda, sA, ld_sa, B, ldb, sB, ld_sb,
+                                       beta, C, ldc, rows, nrows, D_ref, absab);
+}
+
+int orc_gemm_f8_blockscaled_mixed(int a_fmt, int b_fmt, int M, int N, int K, double alpha,
+                                  const uint8_t* A, int64_t lda, const float* sA, int64_t ld_sa,
+                                  const uint8_t* B, int64_t ldb, const float* sB, int64_t ld_sb,
+                                  double beta, const float* C, int64_t ldc, const int32_t* rows,
+                                  int nrows, double* D_ref, double* absab) {
   if (M < 0 || N < 0 || K < 0 || nrows < 0) return 1;
   for (int r = 0; r < nrows; ++r)
     if (rows[r] < 0 || rows[r] >= M) return 2;
@@ -183,7 +221,7 @@ int orc_gemm_fp8_blockscaled(int M, int N, int K, double alpha, const uint8_t* A
   double* Bd = (double*)malloc(sizeof(double) * ((size_t)K * (size_t)N + 1));
   if (!Bd) return 4;
   for (int64_t k = 0; k < K; ++k)
-    for (int64_t j = 0; j < N; ++j) Bd[k * N + j] = orc_decode_e4m3(B[k * ldb + j]);
+    for (int64_t j = 0; j < N; ++j) Bd[k * N + j] = decode_f8(b_fmt, B[k * ldb + j]);
 
 #pragma omp parallel for schedule(dynamic, 1)
   for (int r = 0; r < nrows; ++r) {
@@ -196,7 +234,7 @@ int orc_gemm_fp8_blockscaled(int M, int N, int K, double alpha, const uint8_t* A
       for (int64_t j = 0; j < N; ++j) part[j] = 0.0;
       const double sa = (double)sA[i * ld_sa + kb];
       for (int64_t k = kb * 128; k < k_end; ++k) {
-        const double a = orc_decode_e4m3(A[i * lda + k]);
+        const double a = decode_f8(a_fmt, A[i * lda + k]);
         const double* brow = Bd + k * N;
         for (int64_t j = 0; j < N; ++j) {
           part[j] += a * brow[j];

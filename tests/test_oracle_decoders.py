@@ -85,3 +85,16 @@ def test_f16_encoder_vs_numpy(orc):
         want = vals.astype(np.float16).view(np.uint16)
     for v, w in zip(vals, want):
         assert orc.encode_f16_rn(float(v)) == int(w), float(v)
+
+
+def test_e5m2_exhaustive(orc):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e5m2)
+    lib_vals = codes.to(torch.float64).numpy()
+    for code in range(256):
+        assert _same(orc.decode_e5m2(code), float(lib_vals[code])), hex(code)
+
+
+@pytest.mark.parametrize("code,value", [(0x7B, 57344.0), (0x01, 2.0 ** -16), (0x04, 2.0 ** -14),
+                                        (0x3C, 1.0), (0x7C, math.inf), (0xFC, -math.inf)])
+def test_e5m2_spot(orc, code, value):
+    assert orc.decode_e5m2(code) == value

@@ -192,3 +192,33 @@ def test_generated_gemv_workload_fits_int32(orc):
     z, y = orc.gemv_w8a8(256, 4096, x, sx, W, 4096, sW)
     assert np.all(np.abs(z) <= 4096 * 127 * 127)
     assert np.all(np.isfinite(y.astype(np.float32)))
+
+
+def _f8(bits, fmt):
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(bits)).view(dt).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+def test_f8_mixed_formats_vs_numpy(orc, a_fmt, b_fmt):
+    M, N, K = 9, 260, 300
+    A, sA = wl.e4m3_blockquant_rowblocks(M, K, 241, fmt=a_fmt)
+    B, sB = wl.e4m3_blockquant(K, N, 242, 128, 128, fmt=b_fmt)
+    KB, NB = sA.shape[1], sB.shape[1]
+    D, S = orc.gemm_f8_blockscaled_mixed(a_fmt, b_fmt, M, N, K, 1.0, A.ravel(), K, sA.ravel(), KB,
+                                         B.ravel(), N, sB.ravel(), NB)
+    SA, SB = _expand(sA, sB, M, N, K)
+    Ad = _f8(A, a_fmt) * SA
+    Bd = _f8(B, b_fmt) * SB
+    assert np.all(np.abs(D - Ad @ Bd) <= 1e-12 * (np.abs(Ad) @ np.abs(Bd)) + 1e-300)
+
+
+def test_f8_mixed_e4m3_pair_equals_fp8_entry(orc):
+    M, N, K = 5, 130, 200
+    A, sA, B, sB = _fp8_case(M, N, K, 251)
+    KB, NB = sA.shape[1], sB.shape[1]
+    D1, _ = orc.gemm_fp8_blockscaled(M, N, K, 1.0, A.ravel(), K, sA.ravel(), KB, B.ravel(), N,
+                                     sB.ravel(), NB)
+    D2, _ = orc.gemm_f8_blockscaled_mixed("e4m3", "e4m3", M, N, K, 1.0, A.ravel(), K, sA.ravel(), KB,
+                                          B.ravel(), N, sB.ravel(), NB)
+    assert np.array_equal(D1, D2)

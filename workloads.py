@@ -18,7 +18,8 @@ Distributions (the workload shapes of the pages' linear layer):
 * FP8 E4M3 operands: N(0, 1) in float32, one FP32 scale per block
   s = amax(|block|) / 448 (s = 1 for an all-zero block), code = e4m3(x / s) rounded
   to nearest even; blocks are 1 x 128 for A and 128 x 128 for B.  Turning the FP32
-  values into E4M3 bytes uses torch's float8_e4m3fn conversion.
+  values into E4M3 bytes uses torch's float8_e4m3fn conversion.  E5M2 operands the
+  same with amax / 57344 and torch's float8_e5m2.
 
 Leading dimensions larger than the row width leave padding columns; they are
 filled with a NaN code so that a kernel which reads padding poisons its result.
@@ -91,14 +92,22 @@ def scales_uniform(n, seed, lo=0.001, hi=0.02):
     return np.random.default_rng(seed).uniform(lo, hi, size=n).astype(np.float32)
 
 
-def _to_e4m3_bits(v32):
+F8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+
+
+def _to_f8_bits(v32, fmt="e4m3"):
     import torch
-    t = torch.from_numpy(np.ascontiguousarray(v32)).to(torch.float8_e4m3fn)
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    t = torch.from_numpy(np.ascontiguousarray(v32)).to(dt)
     return t.view(torch.uint8).numpy()
 
 
-def e4m3_blockquant(rows, cols, seed, block_rows, block_cols, ld=None):
-    """Quantise N(0, 1) float32 draws to E4M3 per block of block_rows x block_cols.
+def _to_e4m3_bits(v32):
+    return _to_f8_bits(v32, "e4m3")
+
+
+def e4m3_blockquant(rows, cols, seed, block_rows, block_cols, ld=None, fmt="e4m3"):
+    """Quantise N(0, 1) float32 draws to E4M3 (or E5M2) per block of block_rows x block_cols.
 
     Returns (codes uint8 rows x ld, scales float32 ceil(rows/br) x ceil(cols/bc)).
     """
@@ -114,14 +123,14 @@ def e4m3_blockquant(rows, cols, seed, block_rows, block_cols, ld=None):
         for bj in range(nbc):
             c0, c1 = bj * block_cols, min(cols, (bj + 1) * block_cols)
             amax = np.float32(np.max(np.abs(blk[:, c0:c1]))) if (r1 > r0 and c1 > c0) else 0
-            s = np.float32(amax) / np.float32(448.0) if amax > 0 else np.float32(1.0)
+            s = np.float32(amax) / np.float32(F8_MAX[fmt]) if amax > 0 else np.float32(1.0)
             scales[bi, bj] = s
             q[r0:r1, c0:c1] = blk[:, c0:c1] / s
-    codes = _to_e4m3_bits(q)
+    codes = _to_f8_bits(q, fmt)
     return _pad(codes, ld, NAN_BITS["e4m3"], np.uint8), scales
 
 
-def e4m3_blockquant_rowblocks(rows, cols, seed, ld=None):
+def e4m3_blockquant_rowblocks(rows, cols, seed, ld=None, fmt="e4m3"):
     """A operand: 1 x 128 blocks (one scale per row and 128-wide K block)."""
     ld = cols if ld is None else ld
     v = np.random.default_rng(seed).standard_normal(size=(rows, cols), dtype=np.float32)
@@ -130,9 +139,9 @@ def e4m3_blockquant_rowblocks(rows, cols, seed, ld=None):
     vp = np.pad(v, ((0, 0), (0, pad))) if pad else v
     blocks = vp.reshape(rows, nbc, 128)
     amax = np.max(np.abs(blocks), axis=2).astype(np.float32)
-    scales = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    scales = np.where(amax > 0, amax / np.float32(F8_MAX[fmt]), np.float32(1.0)).astype(np.float32)
     q = (blocks / scales[:, :, None]).reshape(rows, nbc * 128)[:, :cols]
-    codes = _to_e4m3_bits(q.astype(np.float32))
+    codes = _to_f8_bits(q.astype(np.float32), fmt)
     return _pad(codes, ld, NAN_BITS["e4m3"], np.uint8), scales
 
 
