@@ -48,7 +48,7 @@ typedef enum {
 } ll_status;
 
 /* Element type of the A and B operands. */
-typedef enum { LL_IN_F16 = 0, LL_IN_BF16 = 1, LL_IN_E4M3 = 2 } ll_in_type;
+typedef enum { LL_IN_F16 = 0, LL_IN_BF16 = 1, LL_IN_E4M3 = 2, LL_IN_E5M2 = 3 } ll_in_type;
 
 /* Element type of the output D. */
 typedef enum { LL_OUT_F32 = 0, LL_OUT_BF16 = 1, LL_OUT_F16 = 2 } ll_out_type;
@@ -149,6 +149,24 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
 ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const void* A, int64_t lda,
                               const void* B, int64_t ldb, float beta, const float* C,
                               int64_t ldc, void* D, int64_t ldd, int d_type, ll_stream_t stream);
+
+/*
+ * ll_gemm_fp8_blockscaled with each operand's 8-bit format chosen separately:
+ * a_type, b_type in { LL_IN_E4M3, LL_IN_E5M2 }.
+ *
+ * Defined by: "Tensor Core" chapter, table "精度：FP16、BF16、TF32、FP8": FP8 E5M2
+ * (1/5/2, wider range, used for gradients) beside E4M3 (1/4/3).  E5M2 follows the IEEE
+ * conventions (bias 15, infinities and NaNs at exponent 31, largest finite 57344).
+ * Scales, layouts, tails and errors as ll_gemm_fp8_blockscaled; LL_ERR_INVALID_ARG for
+ * any other a_type / b_type.
+ */
+ll_status ll_gemm_f8_blockscaled_mixed(int a_type, int b_type, int M, int N, int K, float alpha,
+                                       const uint8_t* A, int64_t lda, const float* scale_a,
+                                       int64_t ld_sa, const uint8_t* B, int64_t ldb,
+                                       const float* scale_b, int64_t ld_sb, float beta,
+                                       const float* C, int64_t ldc, void* D, int64_t ldd,
+                                       int d_type, void* workspace, size_t ws_bytes,
+                                       ll_stream_t stream);
 
 /* ------------------------------------------------------------------ W8A8 GEMV */
 

@@ -11,6 +11,7 @@ Python name          C entry point
 gemm_f16             ll_gemm_f16
 gemm_bf16            ll_gemm_bf16
 gemm_fp8_blockscaled ll_gemm_fp8_blockscaled
+gemm_f8_blockscaled_mixed ll_gemm_f8_blockscaled_mixed
 linear_w8a8_gemv     ll_linear_w8a8_gemv
 linear_w8a8_gemv_ex  ll_linear_w8a8_gemv_ex
 linear_f16_w8a8_gemv ll_linear_f16_w8a8_gemv
@@ -29,13 +30,13 @@ LIB_PATH = os.path.join(_HERE, "lib", "liblinear_layer_gb300.so")
 
 LL_OK, LL_ERR_INVALID_ARG, LL_ERR_MISALIGNED, LL_ERR_UNSUPPORTED = 0, 1, 2, 3
 LL_ERR_WORKSPACE, LL_ERR_CUDA, LL_ERR_DEVICE_TIMEOUT, LL_ERR_NO_DEVICE = 4, 5, 6, 7
-IN_F16, IN_BF16, IN_E4M3 = 0, 1, 2
+IN_F16, IN_BF16, IN_E4M3, IN_E5M2 = 0, 1, 2, 3
 GEMV_OUT_F16, GEMV_OUT_I8 = 0, 1
 OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 
 # every symbol the header declares
 EXPORTS = ["ll_gemm_workspace_size", "ll_gemm_f16", "ll_gemm_bf16", "ll_gemm_fp8_blockscaled",
-           "ll_gemm_f16_noalloc",
+           "ll_gemm_f16_noalloc", "ll_gemm_f8_blockscaled_mixed",
            "ll_linear_w8a8_gemv", "ll_linear_w8a8_gemv_ex", "ll_linear_f16_w8a8_gemv",
            "ll_quantize_per_token_f16", "ll_get_device_status", "ll_set_wait_timeout_ns",
            "ll_debug_timeout_probe", "ll_status_string", "ll_version"]
@@ -64,6 +65,8 @@ def _load():
     L.ll_gemm_fp8_blockscaled.restype = i32
     L.ll_gemm_fp8_blockscaled.argtypes = [i32, i32, i32, f32, vp, i64, vp, i64, vp, i64, vp, i64,
                                           f32, vp, i64, vp, i64, i32, vp, ctypes.c_size_t, vp]
+    L.ll_gemm_f8_blockscaled_mixed.restype = i32
+    L.ll_gemm_f8_blockscaled_mixed.argtypes = [i32, i32] + L.ll_gemm_fp8_blockscaled.argtypes
     L.ll_linear_w8a8_gemv.restype = i32
     L.ll_linear_w8a8_gemv.argtypes = [i32, i32, vp, vp, vp, i64, vp, vp, vp, vp]
     L.ll_linear_w8a8_gemv_ex.restype = i32
@@ -162,6 +165,17 @@ def gemm_fp8_blockscaled(M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb, scale_b
                                               ldb, _p(scale_b), ld_sb, beta, _p(C), ldc, _p(D), ldd,
                                               d_type, w, wb, _stream(stream)),
                   "ll_gemm_fp8_blockscaled")
+
+
+def gemm_f8_blockscaled_mixed(a_type, b_type, M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb,
+                              scale_b, ld_sb, beta, C, ldc, D, ldd, d_type, workspace=None,
+                              stream=None):
+    w, wb = _ws(workspace)
+    return _check(lib.ll_gemm_f8_blockscaled_mixed(a_type, b_type, M, N, K, alpha, _p(A), lda,
+                                                   _p(scale_a), ld_sa, _p(B), ldb, _p(scale_b),
+                                                   ld_sb, beta, _p(C), ldc, _p(D), ldd, d_type, w,
+                                                   wb, _stream(stream)),
+                  "ll_gemm_f8_blockscaled_mixed")
 
 
 def linear_w8a8_gemv(N, K, x, x_scale, W, ldw, w_scale, y, z_out=None, stream=None):

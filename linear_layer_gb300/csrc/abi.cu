@@ -59,7 +59,7 @@ ll_status current_ctx(ll_stream_t stream, ll::LaunchCtx& ctx) {
   return LL_OK;
 }
 
-int in_esize(int in_type) { return in_type == LL_IN_E4M3 ? 1 : 2; }
+int in_esize(int in_type) { return (in_type == LL_IN_E4M3 || in_type == LL_IN_E5M2) ? 1 : 2; }
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
@@ -85,7 +85,7 @@ ll_status gemm_common(ll::GemmArgs a, void* workspace, size_t ws_bytes, ll_strea
     return LL_ERR_INVALID_ARG;
   if (a.K > 0) {
     if (a.A == nullptr || a.B == nullptr || a.lda < a.K || a.ldb < a.N) return LL_ERR_INVALID_ARG;
-    if (a.in_type == LL_IN_E4M3) {
+    if (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) {
       const int64_t kb = (a.K + 127) / 128, nb = (a.N + 127) / 128;
       if (a.scale_a == nullptr || a.scale_b == nullptr || a.ld_sa < kb || a.ld_sb < nb)
         return LL_ERR_INVALID_ARG;
@@ -146,6 +146,7 @@ static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, co
                                int64_t ldc, void* D, int64_t ldd, int d_type) {
   ll::GemmArgs a;
   a.in_type = in_type;
+  a.b_type = in_type;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -190,6 +191,24 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
                                   void* workspace, size_t ws_bytes, ll_stream_t stream) {
   ll::GemmArgs a = dense_args(LL_IN_E4M3, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd,
                               d_type);
+  a.scale_a = scale_a;
+  a.ld_sa = ld_sa;
+  a.scale_b = scale_b;
+  a.ld_sb = ld_sb;
+  return gemm_common(a, workspace, ws_bytes, stream);
+}
+
+ll_status ll_gemm_f8_blockscaled_mixed(int a_type, int b_type, int M, int N, int K, float alpha,
+                                       const uint8_t* A, int64_t lda, const float* scale_a,
+                                       int64_t ld_sa, const uint8_t* B, int64_t ldb,
+                                       const float* scale_b, int64_t ld_sb, float beta,
+                                       const float* C, int64_t ldc, void* D, int64_t ldd,
+                                       int d_type, void* workspace, size_t ws_bytes,
+                                       ll_stream_t stream) {
+  auto f8 = [](int t) { return t == LL_IN_E4M3 || t == LL_IN_E5M2; };
+  if (!f8(a_type) || !f8(b_type)) return LL_ERR_INVALID_ARG;
+  ll::GemmArgs a = dense_args(a_type, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type);
+  a.b_type = b_type;
   a.scale_a = scale_a;
   a.ld_sa = ld_sa;
   a.scale_b = scale_b;

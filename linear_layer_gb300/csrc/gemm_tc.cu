@@ -84,11 +84,15 @@ struct TileCfg {
   static_assert(STAGES >= 2, "need at least two stages");
 };
 
+// Operand formats of an MMA, packed as a | (b << 3): kind::f16 0 = FP16, 1 = BF16;
+// kind::f8f6f4 0 = E4M3, 1 = E5M2.
+__host__ __device__ constexpr uint32_t fmt_pair(uint32_t a, uint32_t b) { return a | (b << 3); }
+
 // tcgen05 instruction descriptor (kind::f16 / kind::f8f6f4): D = F32 (bits 4-5 = 1),
 // A/B format (bits 7-9 / 10-12), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
 // N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_fmt, int n, int m) {
-  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | (1u << 16) |
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t fmts, int n, int m) {
+  return (1u << 4) | ((fmts & 7u) << 7) | (((fmts >> 3) & 7u) << 10) | (1u << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
@@ -973,7 +977,7 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
     return LL_ERR_CUDA;
   const CUtensorMapDataType dt =
       Cfg::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-               : (AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+               : ((AB_FMT & 7u) == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   CUtensorMap tmA, tmB;
   if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
   if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
@@ -996,7 +1000,7 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
     return LL_ERR_CUDA;
   const CUtensorMapDataType dt =
       FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-          : (AB_FMT == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+          : ((AB_FMT & 7u) == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   CUtensorMap tmA, tmB;
   if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
   if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
@@ -1051,26 +1055,36 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   return LL_OK;
 }
 
+template <uint32_t F>
+static ll_status run_fp8(const GemmArgs& a, const LaunchCtx& ctx, bool pair) {
+  if (pair) return run_pair<true, F>(a, ctx);
+  if (a.N > 128) return run<TileCfg<256, true>, F>(a, ctx);
+  return run<TileCfg<128, true>, F>(a, ctx);
+}
+
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
   const int tiles_m = (a.M + 127) / 128;
   auto tiles = [&](int bn) { return tiles_m * ((a.N + bn - 1) / bn); };
   const bool pair = ((a.M + 255) / 256) * ((a.N + 255) / 256) >= ctx.num_sms / 4;
-  if (a.in_type == LL_IN_E4M3) {
-    if (pair) return run_pair<true, 0>(a, ctx);
-    if (a.N > 128) return run<TileCfg<256, true>, 0>(a, ctx);
-    return run<TileCfg<128, true>, 0>(a, ctx);
+  if (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) {
+    const bool a5 = a.in_type == LL_IN_E5M2, b5 = a.b_type == LL_IN_E5M2;
+    if (!a5 && !b5) return run_fp8<fmt_pair(0, 0)>(a, ctx, pair);
+    if (a5 && b5) return run_fp8<fmt_pair(1, 1)>(a, ctx, pair);
+    if (!a5) return run_fp8<fmt_pair(0, 1)>(a, ctx, pair);
+    return run_fp8<fmt_pair(1, 0)>(a, ctx, pair);
   }
+  constexpr uint32_t F16 = fmt_pair(0, 0), BF16 = fmt_pair(1, 1);
   const bool bf = a.in_type == LL_IN_BF16;
   // large problems: CTA pairs with 256 x 256 tiles
-  if (pair) return bf ? run_pair<false, 1>(a, ctx) : run_pair<false, 0>(a, ctx);
+  if (pair) return bf ? run_pair<false, BF16>(a, ctx) : run_pair<false, F16>(a, ctx);
   int bn = 64;
   if (tiles(256) >= ctx.num_sms)
     bn = 256;
   else if (tiles(128) >= ctx.num_sms)
     bn = 128;
-  if (bn == 256) return bf ? run<TileCfg<256, false>, 1>(a, ctx) : run<TileCfg<256, false>, 0>(a, ctx);
-  if (bn == 128) return bf ? run<TileCfg<128, false>, 1>(a, ctx) : run<TileCfg<128, false>, 0>(a, ctx);
-  return bf ? run<TileCfg<64, false>, 1>(a, ctx) : run<TileCfg<64, false>, 0>(a, ctx);
+  if (bn == 256) return bf ? run<TileCfg<256, false>, BF16>(a, ctx) : run<TileCfg<256, false>, F16>(a, ctx);
+  if (bn == 128) return bf ? run<TileCfg<128, false>, BF16>(a, ctx) : run<TileCfg<128, false>, F16>(a, ctx);
+  return bf ? run<TileCfg<64, false>, BF16>(a, ctx) : run<TileCfg<64, false>, F16>(a, ctx);
 }
 
 }  // namespace ll

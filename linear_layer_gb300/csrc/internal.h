@@ -16,7 +16,8 @@ struct LaunchCtx {
 };
 
 struct GemmArgs {
-  int in_type;  // ll_in_type
+  int in_type;  // ll_in_type (of A; and of B unless b_type says otherwise)
+  int b_type;   // ll_in_type of B (8-bit inputs may mix E4M3 and E5M2)
   int M, N, K;
   float alpha, beta;
   const void* A;

@@ -75,6 +75,7 @@ extern "C" ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const
 
   ll::GemmArgs a;
   a.in_type = LL_IN_F16;
+  a.b_type = LL_IN_F16;
   a.M = M;
   a.N = N;
   a.K = K;

@@ -118,3 +118,37 @@ def test_gemv_rejects_overflowing_k():
     with pytest.raises(ll.LLError) as e:
         ll.linear_w8a8_gemv(1, 131072, t, f, t, 131072, f, f, None)
     assert e.value.status == ll.LL_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+@pytest.mark.parametrize("M,N,K", [(200, 300, 389), (2048, 2048, 512)])
+def test_f8_mixed_formats(orc, a_fmt, b_fmt, M, N, K):
+    import linear_layer_gb300 as ll
+    code = {"e4m3": ll.IN_E4M3, "e5m2": ll.IN_E5M2}
+    A, sA = wl.e4m3_blockquant_rowblocks(M, K, 61, fmt=a_fmt)
+    B, sB = wl.e4m3_blockquant(K, N, 62, 128, 128, fmt=b_fmt)
+    C = wl.f32_normal(M, N, 63)
+    KB, NB = sA.shape[1], sB.shape[1]
+    tD = out_tensor(M, N, "f32")
+    need = ll.gemm_workspace_size(M, N, K, K, N, ll.IN_E4M3)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+    ll.gemm_f8_blockscaled_mixed(code[a_fmt], code[b_fmt], M, N, K, 0.5, up(A), K, up(sA), KB, up(B),
+                                 N, up(sB), NB, 1.5, up(C), N, tD, N, ll.OUT_F32, workspace=ws)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, word
+    rows = np.arange(M) if M <= 300 else np.array([0, 1, 127, 128, 255, 256, 1000, M - 1])
+    ref, absab = orc.gemm_f8_blockscaled_mixed(a_fmt, b_fmt, M, N, K, 0.5, A.ravel(), K, sA.ravel(),
+                                               KB, B.ravel(), N, sB.ravel(), NB, 1.5, C.ravel(), N,
+                                               rows=rows)
+    check_close(tD.cpu().numpy()[rows], ref, absab, K, "f32", "e4m3",
+                what="%s x %s %dx%dx%d" % (a_fmt, b_fmt, M, N, K))
+
+
+def test_f8_mixed_rejects_16bit_types():
+    import linear_layer_gb300 as ll
+    t = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    f = torch.zeros(64, dtype=torch.float32, device="cuda")
+    with pytest.raises(ll.LLError) as e:
+        ll.gemm_f8_blockscaled_mixed(ll.IN_F16, ll.IN_E4M3, 4, 4, 4, 1.0, t, 4, f, 1, t, 4, f, 1, 0.0,
+                                     None, 4, f, 4, ll.OUT_F32)
+    assert e.value.status == ll.LL_ERR_INVALID_ARG
