@@ -66,6 +66,8 @@ def lib():
         L.orc_quantize_per_token_f16.restype = ctypes.c_int
         L.orc_quantize_per_token_f16.argtypes = [ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp]
         L.orc_gemv_w8a8_ex.restype = ctypes.c_int
+        L.orc_linear_w8a8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, i64, vp, vp, i64,
+                                      vp, vp, ctypes.c_int, ctypes.c_float, vp, vp, vp, i64]
         L.orc_gemv_w8a8_ex.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_float, vp, i64, vp,
                                        vp, ctypes.c_int, ctypes.c_float, vp, vp, vp]
         L.orc_gemv_w8a8.restype = ctypes.c_int
@@ -214,6 +216,27 @@ def gemv_w8a8_ex(N, K, x, s_x, W, ldw, s_W, bias=None, out_int8=False, s_y=1.0):
         raise OverflowError("W8A8 dot product exceeds the INT32 range")
     if rc != 0:
         raise ValueError("orc_gemv_w8a8_ex failed with code %d" % rc)
+    return z, (y8 if out_int8 else y16.view(np.float16))
+
+
+def linear_w8a8(M, N, K, X, ldx, s_x, W, ldw, s_W, bias=None, out_int8=False, s_y=1.0):
+    """Batch of M tokens: (z int64 [M, N], Y [M, N]) with Y FP16 or int8 (out_int8);
+    X is M x ldx int8, s_x [M] per-token scales."""
+    X = np.ascontiguousarray(X, dtype=np.int8)
+    W = np.ascontiguousarray(W, dtype=np.int8)
+    s_x = np.ascontiguousarray(s_x, dtype=np.float32)
+    s_W = np.ascontiguousarray(s_W, dtype=np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    z = np.zeros((M, N), dtype=np.int64)
+    y16 = np.zeros((M, N), dtype=np.uint16)
+    y8 = np.zeros((M, N), dtype=np.int8)
+    rc = lib().orc_linear_w8a8(M, N, K, _ptr(X), ldx, _ptr(s_x), _ptr(W), ldw, _ptr(s_W), _ptr(b),
+                               1 if out_int8 else 0, float(np.float32(s_y)), _ptr(z), _ptr(y16),
+                               _ptr(y8), N)
+    if rc == 5:
+        raise OverflowError("W8A8 dot product exceeds the INT32 range")
+    if rc != 0:
+        raise ValueError("orc_linear_w8a8 failed with code %d" % rc)
     return z, (y8 if out_int8 else y16.view(np.float16))
 
 

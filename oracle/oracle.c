@@ -354,3 +354,29 @@ int orc_gemv_w8a8_ex(int N, int K, const int8_t* x, float s_x, const int8_t* W, 
   }
   return bad ? 5 : 0;
 }
+
+/* ------------------------------------------------------------------ W8A8, several tokens */
+
+/*
+ * The W8A8 linear layer for a batch of M tokens ("NVIDIA A100: chip to SIMT", section
+ * 5.1: the activation scale is per token, the weight scale per output channel).  Each
+ * token m is its own symmetric W8A8 product with its own s_x[m]:
+ *   z[m][o] = sum_k X[m][k] * W[o][k]                 (int64; INT32 range checked)
+ *   v       = (float(z[m][o]) * s_x[m]) * s_W[o]  (+ bias[o])
+ *   Y[m][o] = fp16_rn(v), or clamp(rint(v / s_y), -127, 127) with out_int8
+ * X is M x ldx, Y is M x ldy (2-byte or 1-byte elements), z is M x N.
+ */
+int orc_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, const float* s_x,
+                    const int8_t* W, int64_t ldw, const float* s_W, const float* bias, int out_int8,
+                    float s_y, int64_t* z, uint16_t* y16, int8_t* y8, int64_t ldy) {
+  if (M < 0 || N < 0 || K < 0) return 1;
+  int bad = 0;
+  for (int m = 0; m < M; ++m) {
+    const int rc = orc_gemv_w8a8_ex(N, K, X + (int64_t)m * ldx, s_x[m], W, ldw, s_W, bias, out_int8,
+                                    s_y, z ? z + (int64_t)m * N : NULL,
+                                    y16 ? y16 + (int64_t)m * ldy : NULL, y8 ? y8 + (int64_t)m * ldy : NULL);
+    if (rc == 5) bad = 1;
+    else if (rc != 0) return rc;
+  }
+  return bad ? 5 : 0;
+}

@@ -104,3 +104,43 @@ def test_gemv_ex_int8_identity_scale(orc):
     W[:, 0] = np.array([-3, -1, 0, 2, 7], np.int8)
     _, y8 = orc.gemv_w8a8_ex(N, K, x, 1.0, W, K, np.ones(N, np.float32), out_int8=True, s_y=1.0)
     assert list(y8) == [-3, -1, 0, 2, 7]
+
+
+# ------------------------------------------------------- several tokens (per-token s_x)
+
+
+def test_batch_against_numpy(orc):
+    # z = X W^T exactly; y in the FP32 order of section 5.2 with each token's own s_x
+    M, N, K = 6, 130, 1000
+    X, s_x, W, s_W = wl.batch_w8a8_inputs(M, N, K, ldx=1008, ldw=1008)
+    bias = (np.random.default_rng(407).standard_normal(N) * 2).astype(np.float32)
+    z, y = orc.linear_w8a8(M, N, K, X, 1008, s_x, W, 1008, s_W, bias=bias)
+    zn = X[:, :K].astype(np.int64) @ W[:, :K].astype(np.int64).T
+    assert np.array_equal(z, zn)
+    v = (zn.astype(np.float32) * s_x[:, None]) * s_W[None, :] + bias[None, :]
+    assert np.array_equal(y.view(np.uint16), v.astype(np.float16).view(np.uint16))
+
+
+def test_batch_token_scale_is_per_row(orc):
+    # a distinct power-of-two s_x per token scales only that token's row, exactly; a
+    # transposed (per-channel) use of s_x would fail this
+    M, N, K = 4, 9, 64
+    X = np.ones((M, K), np.int8)
+    W = np.zeros((N, K), np.int8)
+    W[:, 0] = np.arange(1, N + 1)
+    s_x = np.array([1.0, 2.0, 0.5, 4.0], np.float32)
+    _, y = orc.linear_w8a8(M, N, K, X, K, s_x, W, K, np.ones(N, np.float32))
+    for m in range(M):
+        assert np.array_equal(y[m].astype(np.float64), s_x[m] * np.arange(1, N + 1))
+
+
+def test_batch_int8_output_and_single_token_reduction(orc):
+    M, N, K = 3, 200, 4096
+    X, s_x, W, s_W = wl.batch_w8a8_inputs(M, N, K)
+    z8, y8 = orc.linear_w8a8(M, N, K, X, K, s_x, W, K, s_W, out_int8=True, s_y=0.05)
+    v = (z8.astype(np.float32) * s_x[:, None]) * s_W[None, :]
+    assert np.array_equal(y8, np.clip(np.rint(v / np.float32(0.05)), -127, 127).astype(np.int8))
+    # token 0 of the batch is the batch-1 workload: the same z as the GEMV oracle
+    x0, sx0, _, _ = wl.gemv_inputs(N, K)
+    z1, _ = orc.gemv_w8a8(N, K, x0, sx0, W, K, s_W)
+    assert np.array_equal(z8[0], z1)

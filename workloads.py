@@ -161,6 +161,21 @@ def fp8_inputs(M, N, K, beta=0.0, lda=None, ldb=None, ldc=None):
     return A, sA, B, sB, C
 
 
+def batch_w8a8_inputs(M, N, K, ldx=None, ldw=None):
+    """A batch of M int8 tokens for the W8A8 layer: (X int8 [M x ldx], s_x float32 [M],
+    W int8 [N x ldw], s_W float32 [N]); token 0 and the weights are those of
+    gemv_inputs, so the batch-1 case is the same layer."""
+    ldx = K if ldx is None else ldx
+    x0, _, W, s_W = gemv_inputs(N, K, ldw)
+    X = np.full((M, ldx), 77, dtype=np.int8)  # padding a kernel must not read
+    if M > 0:
+        X[0, :K] = x0
+        if M > 1:
+            X[1:, :K] = int8_uniform((M - 1, K), SEED_X + 100)
+    s_x = scales_uniform(M, SEED_SX)
+    return X, s_x, W, s_W
+
+
 def gemv_inputs(N, K, ldw=None):
     """(x int8 [K], s_x float32 scalar, W int8 [N x ldw], s_W float32 [N])."""
     ldw = K if ldw is None else ldw
