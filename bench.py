@@ -464,6 +464,69 @@ def bench_gemv_fused(args, dev, stream, peaks, peak_src):
             "status": ll.status_string(st)}
 
 
+def bench_w8a8_tokens(args, dev, stream, peaks, peak_src):
+    """The W8A8 layer (N = 11008, K = 4096) for a few tokens: dp4a up to 16 tokens, the
+    exact FP16 tensor-core path in passes of up to 32 above that."""
+    import torch
+
+    import linear_layer_gb300 as ll
+    import workloads as wl
+    cfg = wl.WORKLOADS["w8a8_gemv_4096x11008"]
+    N, K = cfg["N"], cfg["K"]
+    out = {"metric": "W8A8 linear layer, several tokens: weight GB/s and int8 TOPS",
+           "unit": "GB/s", "per_tokens": {}}
+    _, _, W, sW = wl.batch_w8a8_inputs(1, N, K)
+    ncopies = max(2, math.ceil(4 * L2_BYTES / (N * K)))
+    tW0 = _up(W, dev)
+    tWs = [tW0.clone() for _ in range(ncopies)]
+    del tW0
+    tsW = _up(sW, dev)
+    for M in (2, 4, 8, 16, 24, 32):
+        X, sx, _, _ = wl.batch_w8a8_inputs(M, N, K)
+        tX, tsx = _up(X, dev), _up(sx, dev)
+        tY = torch.empty((M, N), dtype=torch.float16, device=dev)
+
+        def call(i):
+            ll.linear_w8a8(M, N, K, tX, K, tsx, tWs[i % ncopies], K, tsW, None, ll.GEMV_OUT_F16, None,
+                           tY, N, stream=stream)
+
+        for i in range(5):
+            call(i)
+        torch.cuda.synchronize(dev)
+        per_graph = ncopies * 20
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for i in range(per_graph):
+                    call(i)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize(dev)
+        reps = max(3, min(20, args.steps // 10 + 3))
+
+        def replay(_):
+            with torch.cuda.stream(stream):
+                g.replay()
+
+        total_ms, _ = time_events(replay, reps, stream)
+        launch_s = total_ms / 1e3 / (reps * per_graph)
+        abytes = N * K + M * K + 4 * M + 4 * N + 2 * M * N
+        out["per_tokens"][str(M)] = {
+            "us_per_layer": round(launch_s * 1e6, 3),
+            "GBs": round(abytes / launch_s / 1e9, 1),
+            "frac_of_hbm": round(abytes / launch_s / 1e9 / peaks["hbm_gbs"], 4),
+            "int8_TOPS": round(2.0 * M * N * K / launch_s / 1e12, 2),
+            "path": "dp4a" if M <= 16 else "tensor cores (exact FP16 path)"}
+        del g
+    st, _ = ll.get_device_status(stream)
+    out["value"] = out["per_tokens"]["2"]["GBs"]
+    out["timing"] = "per token count: CUDA graph of %d launches over %d weight copies (%.0f MB > L2)" % (
+        ncopies * 20, ncopies, ncopies * N * K / 1e6)
+    out["status"] = ll.status_string(st)
+    return out
+
+
 def bench_fp8(args, dev, stream, peaks, peak_src):
     import torch
 
@@ -618,7 +681,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the GEMV / FP8 / ragged lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged"], default="all",
+    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged", "tokens"],
+                    default="all",
                     help="all = the contract line; otherwise time one other kernel and print its object")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -636,7 +700,7 @@ def main(argv=None):
     stream = torch.cuda.Stream(device=dev)
 
     single = {"gemv": bench_gemv, "gemv_fused": bench_gemv_fused, "fp8": bench_fp8,
-              "ragged": bench_ragged}.get(args.workload)
+              "ragged": bench_ragged, "tokens": bench_w8a8_tokens}.get(args.workload)
     if single is not None:
         res = single(args, dev, stream, peaks, peak_src)
         if rank == 0:
@@ -649,6 +713,7 @@ def main(argv=None):
         extra["w8a8_gemv_4096x11008"] = bench_gemv(args, dev, stream, peaks, peak_src)
         extra["f16_act_w8a8_gemv_fused_4096x11008"] = bench_gemv_fused(args, dev, stream, peaks,
                                                                        peak_src)
+        extra["w8a8_linear_tokens_4096x11008"] = bench_w8a8_tokens(args, dev, stream, peaks, peak_src)
         extra["e4m3_gemm_8192"] = bench_fp8(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_4093x5003x2056"] = bench_ragged(args, dev, stream, peaks, peak_src)
     barrier(dev)

@@ -223,6 +223,35 @@ ll_status ll_linear_w8a8_gemv_ex(int N, int K, const int8_t* x, const float* x_s
                                  int32_t* z_out, ll_stream_t stream);
 
 /*
+ * W8A8 linear layer for a batch of M tokens (A100 page, section 5.1: the activation
+ * scale is per token, the weight scale per output channel, zero point 0; section 5.2:
+ * the dequantisation order).  Token m is the batch-1 layer with its own scale:
+ *
+ *   z[m][o] = sum_k X[m][k] * W[o][k]                           (exact INT32)
+ *   v       = (float(z[m][o]) * x_scale[m]) * w_scale[o]  (+ bias[o])
+ *   Y[m][o] = fp16_rn(v)  or  clamp(rint(v / *y_scale), -127, 127)   (as y_type)
+ *
+ *   X       : M x K int8 row-major, row pitch ldx >= K bytes (one token per row)
+ *   x_scale : M FP32 (device)          W, ldw, w_scale, bias, y_type, y_scale: as
+ *   Y       : M x N, pitch ldy >= N      ll_linear_w8a8_gemv_ex
+ *             elements (FP16 or int8)
+ *   z_out   : M x N INT32 with pitch ldz >= N, or NULL
+ * Every weight byte is read from memory once per group of up to 16 tokens: larger M
+ * runs as consecutive groups.  M == 1 is exactly ll_linear_w8a8_gemv_ex.  Results are
+ * bit-identical to M calls of ll_linear_w8a8_gemv_ex, one per token.
+ * Ordering: programmatic dependent launch as ll_linear_w8a8_gemv (W and w_scale may be
+ * read before the preceding kernel of the stream has finished; X, the scales and the
+ * outputs only after).
+ * M == 0 or N == 0: nothing.  Errors: LL_ERR_INVALID_ARG for negative sizes,
+ * K > 131071, ldx < K, ldw < K, ldy < N, ldz < N with z_out, NULL pointers, an unknown
+ * y_type or a NULL y_scale with INT8 output.
+ */
+ll_status ll_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, const float* x_scale,
+                         const int8_t* W, int64_t ldw, const float* w_scale, const float* bias,
+                         int y_type, const float* y_scale, void* Y, int64_t ldy, int32_t* z_out,
+                         int64_t ldz, ll_stream_t stream);
+
+/*
  * Symmetric per-token activation quantiser (A100 page, section 5.1: the activation is
  * quantised at run time by the preceding operator or a separate quantisation step):
  *

@@ -264,6 +264,25 @@ ll_status ll_linear_f16_w8a8_gemv(int N, int K, const void* x, int8_t* x_q, floa
                                  y_type == LL_GEMV_OUT_I8, y_scale, y, z_out, ctx);
 }
 
+ll_status ll_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, const float* x_scale,
+                         const int8_t* W, int64_t ldw, const float* w_scale, const float* bias,
+                         int y_type, const float* y_scale, void* Y, int64_t ldy, int32_t* z_out,
+                         int64_t ldz, ll_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || K > 131071) return LL_ERR_INVALID_ARG;
+  if (y_type != LL_GEMV_OUT_F16 && y_type != LL_GEMV_OUT_I8) return LL_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return LL_OK;
+  if (x_scale == nullptr || w_scale == nullptr || Y == nullptr || ldy < N || ldw < K || ldx < K)
+    return LL_ERR_INVALID_ARG;
+  if (K > 0 && (X == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
+  if (z_out != nullptr && ldz < N) return LL_ERR_INVALID_ARG;
+  if (y_type == LL_GEMV_OUT_I8 && y_scale == nullptr) return LL_ERR_INVALID_ARG;
+  ll::LaunchCtx ctx;
+  ll_status st = current_ctx(stream, ctx);
+  if (st != LL_OK) return st;
+  return ll::launch_linear_w8a8(M, N, K, X, ldx, x_scale, W, ldw, w_scale, bias, y_type == LL_GEMV_OUT_I8,
+                                y_scale, Y, ldy, z_out, ldz, ctx);
+}
+
 ll_status ll_quantize_per_token_f16(int M, int K, const void* x, int64_t ldx, int8_t* q,
                                     int64_t ldq, float* scale, ll_stream_t stream) {
   if (M < 0 || K < 0 || ldx < K || ldq < K) return LL_ERR_INVALID_ARG;

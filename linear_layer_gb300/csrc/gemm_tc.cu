@@ -924,8 +924,8 @@ static EncodeTiledFn encode_fn() {
 }
 
 // 2-D row-major matrix rows x cols (pitch in elements) with a box of box_cols x box_rows.
-static bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
-                     int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows) {
+bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
+                        int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -979,8 +979,8 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
       Cfg::FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                : ((AB_FMT & 7u) == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
-  if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
+  if (!make_tensor_map_2d(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
+  if (!make_tensor_map_2d(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
 
   GemmParams p = make_params(a, ctx);
 
@@ -1002,8 +1002,8 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
       FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
           : ((AB_FMT & 7u) == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
-  if (!make_map(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
+  if (!make_tensor_map_2d(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
+  if (!make_tensor_map_2d(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
   GemmParams p = make_params(a, ctx);
 
   cudaLaunchConfig_t cfg = {};

@@ -147,14 +147,6 @@ __device__ __forceinline__ float quantize_row_to_smem(const __half* x, int K, in
   return s;
 }
 
-__device__ __forceinline__ int4 ld_stream(const int4* p) {
-  int4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Request chunks base + lane + 32 j (j < kGvBatch) of row `row`; chunks past the row are zero.
 __device__ __forceinline__ void load_batch(int4 (&w)[kGvBatch], const int4* row, int base,
                                            int nch, int lane) {

@@ -1,5 +1,6 @@
 // Host-side interfaces shared between the C ABI (abi.cu) and the kernel files.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,6 +50,11 @@ ll_status launch_scale_c(const GemmArgs& a, const LaunchCtx& ctx);
 ll_status launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int rows,
                         int cols, int esize, const LaunchCtx& ctx);
 
+// Tensor map of a row-major rows x cols matrix (pitch in elements), tiles of box_cols x
+// box_rows, 128-byte swizzle, zero fill out of bounds (gemm_tc.cu).
+bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
+                        int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows);
+
 // Bounded-wait probe (aux.cu).
 ll_status launch_timeout_probe(const LaunchCtx& ctx);
 
@@ -64,6 +70,20 @@ ll_status launch_gemv_w8a8_ex(int N, int K, const int8_t* x, const float* x_scal
                               int8_t* xq_out, float* xs_out, const int8_t* W, int64_t ldw,
                               const float* w_scale, const float* bias, int out_i8,
                               const float* y_scale, void* y, int32_t* z_out, const LaunchCtx& ctx);
+
+// W8A8 linear layer for M tokens (w8a8_batch.cu): X M x ldx int8, x_scale [M], Y M x ldy
+// (FP16, or INT8 with out_i8), Z M x ldz int32 or NULL.
+ll_status launch_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, const float* x_scale,
+                             const int8_t* W, int64_t ldw, const float* w_scale, const float* bias,
+                             int out_i8, const float* y_scale, void* Y, int64_t ldy, int32_t* Z,
+                             int64_t ldz, const LaunchCtx& ctx);
+
+// The same for 1..64 tokens on the tensor cores (w8a8_tc.cu): K % 16 == 0, ldx and ldw
+// multiples of 16, 16-byte aligned X and W.
+ll_status launch_w8a8_tc(int M, int N, int K, const int8_t* X, int64_t ldx, const float* x_scale,
+                         const int8_t* W, int64_t ldw, const float* w_scale, const float* bias, int out_i8,
+                         const float* y_scale, void* Y, int64_t ldy, int32_t* Z, int64_t ldz,
+                         const LaunchCtx& ctx);
 
 // Per-token activation quantiser (gemv_w8a8.cu).
 ll_status launch_quantize_per_token(int M, int K, const void* x, int64_t ldx, int8_t* q, int64_t ldq,
