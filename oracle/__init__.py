@@ -66,6 +66,8 @@ def lib():
         L.orc_quantize_per_token_f16.restype = ctypes.c_int
         L.orc_quantize_per_token_f16.argtypes = [ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp]
         L.orc_gemv_w8a8_ex.restype = ctypes.c_int
+        L.orc_linear_w8a16.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp, vp,
+                                       vp, vp]
         L.orc_linear_w8a8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, i64, vp, vp, i64,
                                       vp, vp, ctypes.c_int, ctypes.c_float, vp, vp, vp, i64]
         L.orc_gemv_w8a8_ex.argtypes = [ctypes.c_int, ctypes.c_int, vp, ctypes.c_float, vp, i64, vp,
@@ -238,6 +240,21 @@ def linear_w8a8(M, N, K, X, ldx, s_x, W, ldw, s_W, bias=None, out_int8=False, s_
     if rc != 0:
         raise ValueError("orc_linear_w8a8 failed with code %d" % rc)
     return z, (y8 if out_int8 else y16.view(np.float16))
+
+
+def linear_w8a16(M, N, K, X_bits, ldx, W, ldw, s_W, bias=None):
+    """Weight-only layer: (y float64 [M, N], absab [M, N]); X_bits are BF16 codes
+    (uint16, M x ldx), W int8 N x ldw, s_W float32 [N]."""
+    X = np.ascontiguousarray(X_bits, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.int8)
+    s_W = np.ascontiguousarray(s_W, dtype=np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    y = np.zeros((M, N), dtype=np.float64)
+    ab = np.zeros((M, N), dtype=np.float64)
+    rc = lib().orc_linear_w8a16(M, N, K, _ptr(X), ldx, _ptr(W), ldw, _ptr(s_W), _ptr(b), _ptr(y), _ptr(ab))
+    if rc != 0:
+        raise ValueError("orc_linear_w8a16 failed with code %d" % rc)
+    return y, ab
 
 
 def threads_used() -> int:

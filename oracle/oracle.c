@@ -380,3 +380,34 @@ int orc_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, const flo
   }
   return bad ? 5 : 0;
 }
+
+/* ------------------------------------------------------------------ weight-only INT8 */
+
+/*
+ * Weight-only linear layer (the Tensor Core chapter's mixed-precision GEMM with the
+ * weights kept in INT8 and a per-output-channel scale, as in the A100 page section
+ * 5.1's s_W[o]; the activation stays BF16):
+ *   y[m][o] = s_W[o] * sum_k dec_bf16(X[m][k]) * W[o][k]  (+ bias[o])
+ * in double; y is M x N (pitch N).  absab[m][o] = |s_W[o]| * sum_k |x| |W| bounds the
+ * rounding of any FP32 evaluation.
+ */
+int orc_linear_w8a16(int M, int N, int K, const uint16_t* X, int64_t ldx, const int8_t* W, int64_t ldw,
+                     const float* s_W, const float* bias, double* y, double* absab) {
+  if (M < 0 || N < 0 || K < 0) return 1;
+  for (int m = 0; m < M; ++m) {
+    for (int o = 0; o < N; ++o) {
+      double acc = 0.0, aab = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double xv = orc_decode_bf16(X[(int64_t)m * ldx + k]);
+        const double wv = (double)W[(int64_t)o * ldw + k];
+        acc += xv * wv;
+        aab += fabs(xv * wv);
+      }
+      double v = (double)s_W[o] * acc;
+      if (bias) v += (double)bias[o];
+      y[(int64_t)m * N + o] = v;
+      if (absab) absab[(int64_t)m * N + o] = fabs((double)s_W[o]) * aab;
+    }
+  }
+  return 0;
+}

@@ -144,3 +144,41 @@ def test_batch_int8_output_and_single_token_reduction(orc):
     x0, sx0, _, _ = wl.gemv_inputs(N, K)
     z1, _ = orc.gemv_w8a8(N, K, x0, sx0, W, K, s_W)
     assert np.array_equal(z8[0], z1)
+
+
+# ------------------------------------------------- weight-only INT8 (BF16 activation)
+
+
+def _bf16(v):
+    import torch
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_w8a16_against_numpy(orc):
+    M, N, K = 3, 70, 500
+    X, W, s_W = wl.w8a16_inputs(M, N, K, ldx=512, ldw=512)
+    bias = (np.random.default_rng(408).standard_normal(N) * 3).astype(np.float32)
+    y, ab = orc.linear_w8a16(M, N, K, X, 512, W, 512, s_W, bias=bias)
+    import torch
+    xd = torch.from_numpy(X[:, :K].view(np.int16)).view(torch.bfloat16).double().numpy()
+    ref = (xd @ W[:, :K].astype(np.float64).T) * s_W.astype(np.float64)[None, :] + bias[None, :]
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-12)
+    assert np.allclose(ab, np.abs(xd) @ np.abs(W[:, :K].astype(np.float64)).T * s_W[None, :])
+
+
+def test_w8a16_exact_small_integers(orc):
+    # integer activations, power-of-two scales: the result is exact and hand-checkable
+    X = _bf16([[1, 2, -3, 4], [0, 0, 0, 5]])
+    W = np.array([[1, 1, 1, 1], [2, -1, 0, 3]], np.int8)
+    s_W = np.array([0.5, 4.0], np.float32)
+    y, _ = orc.linear_w8a16(2, 2, 4, X, 4, W, 4, s_W)
+    assert y.tolist() == [[0.5 * 4, 4.0 * (2 - 2 + 0 + 12)], [0.5 * 5, 4.0 * 15]]
+
+
+def test_w8a16_scale_is_per_output_channel(orc):
+    # a transposed (per-token) use of s_W would fail
+    X = _bf16(np.ones((3, 8)))
+    W = np.ones((5, 8), np.int8)
+    s_W = np.array([1, 2, 4, 8, 16], np.float32)
+    y, _ = orc.linear_w8a16(3, 5, 8, X, 8, W, 8, s_W, bias=np.full(5, 0.25, np.float32))
+    assert np.array_equal(y, np.tile(8.0 * s_W + 0.25, (3, 1)))

@@ -176,6 +176,14 @@ def batch_w8a8_inputs(M, N, K, ldx=None, ldw=None):
     return X, s_x, W, s_W
 
 
+def w8a16_inputs(M, N, K, ldx=None, ldw=None):
+    """Weight-only layer inputs: (X BF16 codes uint16 [M x ldx], W int8 [N x ldw],
+    s_W float32 [N]); X ~ N(0,1) rounded to BF16, W and s_W as gemv_inputs."""
+    _, _, W, s_W = gemv_inputs(N, K, ldw)
+    X = bf16_normal(M, K, SEED_X + 200, ldx)  # NaN codes in the padding
+    return X, W, s_W
+
+
 def gemv_inputs(N, K, ldw=None):
     """(x int8 [K], s_x float32 scalar, W int8 [N x ldw], s_W float32 [N])."""
     ldw = K if ldw is None else ldw
