@@ -273,7 +273,7 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
     peak = peaks[peak_key]
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": measured_traffic(HEADLINE, "gemm_tc2_kernel"),
-                "kernel": "gemm_tc2_kernel<PairCfg<256,false>,1> (CTA pairs)",
+                "kernel": "gemm_tc2_kernel<PairCfg<256,false>,9> (CTA pairs, BF16 x BF16)",
                 "peak_source": "%s %s" % (peak_src, peak_key),
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": set_bytes}
@@ -527,6 +527,62 @@ def bench_w8a8_tokens(args, dev, stream, peaks, peak_src):
     return out
 
 
+def bench_w8a16(args, dev, stream, peaks, peak_src):
+    """Weight-only INT8 layer with BF16 activations (N = 11008, K = 4096), 1..4 tokens."""
+    import torch
+
+    import linear_layer_gb300 as ll
+    import workloads as wl
+    cfg = wl.WORKLOADS["w8a8_gemv_4096x11008"]
+    N, K = cfg["N"], cfg["K"]
+    out = {"metric": "weight-only INT8 x BF16 linear layer: weight GB/s", "unit": "GB/s", "per_tokens": {}}
+    _, W, sW = wl.w8a16_inputs(1, N, K)
+    ncopies = max(2, math.ceil(4 * L2_BYTES / (N * K)))
+    tW0 = _up(W, dev)
+    tWs = [tW0.clone() for _ in range(ncopies)]
+    del tW0
+    tsW = _up(sW, dev)
+    for M in (1, 2, 4):
+        X, _, _ = wl.w8a16_inputs(M, N, K)
+        tX = _up(X, dev)
+        tY = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def call(i):
+            ll.linear_w8a16(M, N, K, tX, K, tWs[i % ncopies], K, tsW, None, ll.OUT_BF16, tY, N, stream=stream)
+
+        for i in range(5):
+            call(i)
+        torch.cuda.synchronize(dev)
+        per_graph = ncopies * 20
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for i in range(per_graph):
+                    call(i)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize(dev)
+        reps = max(3, min(20, args.steps // 10 + 3))
+
+        def replay(_):
+            with torch.cuda.stream(stream):
+                g.replay()
+
+        total_ms, _ = time_events(replay, reps, stream)
+        launch_s = total_ms / 1e3 / (reps * per_graph)
+        abytes = N * K + 2 * M * K + 4 * N + 2 * M * N
+        out["per_tokens"][str(M)] = {"us_per_layer": round(launch_s * 1e6, 3),
+                                     "GBs": round(abytes / launch_s / 1e9, 1),
+                                     "frac_of_hbm": round(abytes / launch_s / 1e9 / peaks["hbm_gbs"], 4)}
+        del g
+    st, _ = ll.get_device_status(stream)
+    out["value"] = out["per_tokens"]["1"]["GBs"]
+    out["timing"] = "per token count: CUDA graph of %d launches over %d weight copies" % (ncopies * 20, ncopies)
+    out["status"] = ll.status_string(st)
+    return out
+
+
 def bench_fp8(args, dev, stream, peaks, peak_src):
     import torch
 
@@ -681,7 +737,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the GEMV / FP8 / ragged lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged", "tokens"],
+    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged", "tokens", "w8a16"],
                     default="all",
                     help="all = the contract line; otherwise time one other kernel and print its object")
     args = ap.parse_args(argv)
@@ -700,7 +756,7 @@ def main(argv=None):
     stream = torch.cuda.Stream(device=dev)
 
     single = {"gemv": bench_gemv, "gemv_fused": bench_gemv_fused, "fp8": bench_fp8,
-              "ragged": bench_ragged, "tokens": bench_w8a8_tokens}.get(args.workload)
+              "ragged": bench_ragged, "tokens": bench_w8a8_tokens, "w8a16": bench_w8a16}.get(args.workload)
     if single is not None:
         res = single(args, dev, stream, peaks, peak_src)
         if rank == 0:
@@ -714,6 +770,7 @@ def main(argv=None):
         extra["f16_act_w8a8_gemv_fused_4096x11008"] = bench_gemv_fused(args, dev, stream, peaks,
                                                                        peak_src)
         extra["w8a8_linear_tokens_4096x11008"] = bench_w8a8_tokens(args, dev, stream, peaks, peak_src)
+        extra["w8a16_linear_tokens_4096x11008"] = bench_w8a16(args, dev, stream, peaks, peak_src)
         extra["e4m3_gemm_8192"] = bench_fp8(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_4093x5003x2056"] = bench_ragged(args, dev, stream, peaks, peak_src)
     barrier(dev)

@@ -252,6 +252,30 @@ ll_status ll_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, cons
                          int64_t ldz, ll_stream_t stream);
 
 /*
+ * Weight-only INT8 linear layer with BF16 activations (the Tensor Core chapter's mixed
+ * precision: low-precision storage, FP32 accumulation; weights stored as INT8 with the
+ * per-output-channel scale s_W[o] of the A100 page, section 5.1; activations not
+ * quantised):
+ *
+ *   y[m][o] = cast_out( w_scale[o] * sum_k X[m][k] * W[o][k]  (+ bias[o]) )
+ *
+ *   X       : M x K BF16 row-major, pitch ldx >= K elements (one token per row)
+ *   W       : N x K int8, pitch ldw >= K bytes (qweight[N][K], output-channel-major)
+ *   w_scale : N FP32                 bias : N FP32 or NULL
+ *   Y       : M x N, pitch ldy >= N elements, of type y_type (ll_out_type: F32, BF16, F16;
+ *             rounded to nearest even)
+ * The dot product is accumulated in FP32 (any order; results are deterministic run to
+ * run); the scale multiplies the sum, then the bias is added, in FP32.  Designed for
+ * decode-sized M (up to 4 tokens per weight pass; larger M runs as several passes).
+ * Ordering: programmatic dependent launch as ll_linear_w8a8_gemv.
+ * M == 0 or N == 0: nothing.  Errors: LL_ERR_INVALID_ARG for negative sizes, ldx < K,
+ * ldw < K, ldy < N, NULL pointers or an unknown y_type.
+ */
+ll_status ll_linear_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
+                          const float* w_scale, const float* bias, int y_type, void* Y, int64_t ldy,
+                          ll_stream_t stream);
+
+/*
  * Symmetric per-token activation quantiser (A100 page, section 5.1: the activation is
  * quantised at run time by the preceding operator or a separate quantisation step):
  *

@@ -15,6 +15,7 @@ gemm_f8_blockscaled_mixed ll_gemm_f8_blockscaled_mixed
 linear_w8a8_gemv     ll_linear_w8a8_gemv
 linear_w8a8_gemv_ex  ll_linear_w8a8_gemv_ex
 linear_w8a8          ll_linear_w8a8
+linear_w8a16         ll_linear_w8a16
 linear_f16_w8a8_gemv ll_linear_f16_w8a8_gemv
 quantize_per_token_f16 ll_quantize_per_token_f16
 gemm_f16_noalloc     ll_gemm_f16_noalloc
@@ -39,7 +40,7 @@ OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 EXPORTS = ["ll_gemm_workspace_size", "ll_gemm_f16", "ll_gemm_bf16", "ll_gemm_fp8_blockscaled",
            "ll_gemm_f16_noalloc", "ll_gemm_f8_blockscaled_mixed",
            "ll_linear_w8a8_gemv", "ll_linear_w8a8_gemv_ex", "ll_linear_f16_w8a8_gemv",
-           "ll_linear_w8a8",
+           "ll_linear_w8a8", "ll_linear_w8a16",
            "ll_quantize_per_token_f16", "ll_get_device_status", "ll_set_wait_timeout_ns",
            "ll_debug_timeout_probe", "ll_status_string", "ll_version"]
 
@@ -76,6 +77,8 @@ def _load():
     L.ll_linear_w8a8.restype = i32
     L.ll_linear_w8a8.argtypes = [i32, i32, i32, vp, i64, vp, vp, i64, vp, vp, i32, vp, vp, i64, vp,
                                  i64, vp]
+    L.ll_linear_w8a16.restype = i32
+    L.ll_linear_w8a16.argtypes = [i32, i32, i32, vp, i64, vp, i64, vp, vp, i32, vp, i64, vp]
     L.ll_linear_f16_w8a8_gemv.restype = i32
     L.ll_linear_f16_w8a8_gemv.argtypes = [i32, i32, vp, vp, vp, vp, i64, vp, vp, i32, vp, vp, vp, vp]
     L.ll_quantize_per_token_f16.restype = i32
@@ -200,6 +203,11 @@ def linear_w8a8(M, N, K, X, ldx, x_scale, W, ldw, w_scale, bias, y_type, y_scale
     return _check(lib.ll_linear_w8a8(M, N, K, _p(X), ldx, _p(x_scale), _p(W), ldw, _p(w_scale),
                                      _p(bias), y_type, _p(y_scale), _p(Y), ldy, _p(z_out), ldz,
                                      _stream(stream)), "ll_linear_w8a8")
+
+
+def linear_w8a16(M, N, K, X, ldx, W, ldw, w_scale, bias, y_type, Y, ldy, stream=None):
+    return _check(lib.ll_linear_w8a16(M, N, K, _p(X), ldx, _p(W), ldw, _p(w_scale), _p(bias), y_type,
+                                      _p(Y), ldy, _stream(stream)), "ll_linear_w8a16")
 
 
 def linear_f16_w8a8_gemv(N, K, x, x_q, x_scale, W, ldw, w_scale, bias, y_type, y_scale, y,

@@ -283,6 +283,20 @@ ll_status ll_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, cons
                                 y_scale, Y, ldy, z_out, ldz, ctx);
 }
 
+ll_status ll_linear_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
+                          const float* w_scale, const float* bias, int y_type, void* Y, int64_t ldy,
+                          ll_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return LL_ERR_INVALID_ARG;
+  if (y_type != LL_OUT_F32 && y_type != LL_OUT_BF16 && y_type != LL_OUT_F16) return LL_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return LL_OK;
+  if (w_scale == nullptr || Y == nullptr || ldy < N || ldw < K || ldx < K) return LL_ERR_INVALID_ARG;
+  if (K > 0 && (X == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
+  ll::LaunchCtx ctx;
+  ll_status st = current_ctx(stream, ctx);
+  if (st != LL_OK) return st;
+  return ll::launch_linear_w8a16(M, N, K, X, ldx, W, ldw, w_scale, bias, y_type, Y, ldy, ctx);
+}
+
 ll_status ll_quantize_per_token_f16(int M, int K, const void* x, int64_t ldx, int8_t* q,
                                     int64_t ldq, float* scale, ll_stream_t stream) {
   if (M < 0 || K < 0 || ldx < K || ldq < K) return LL_ERR_INVALID_ARG;

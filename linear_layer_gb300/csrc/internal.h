@@ -85,6 +85,12 @@ ll_status launch_w8a8_tc(int M, int N, int K, const int8_t* X, int64_t ldx, cons
                          const float* y_scale, void* Y, int64_t ldy, int32_t* Z, int64_t ldz,
                          const LaunchCtx& ctx);
 
+// Weight-only INT8 layer with BF16 activations (w8a16.cu): X M x ldx BF16, W N x ldw
+// int8, w_scale [N], bias [N] or NULL, Y M x ldy of ll_out_type y_type.
+ll_status launch_linear_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
+                              const float* w_scale, const float* bias, int y_type, void* Y, int64_t ldy,
+                              const LaunchCtx& ctx);
+
 // Per-token activation quantiser (gemv_w8a8.cu).
 ll_status launch_quantize_per_token(int M, int K, const void* x, int64_t ldx, int8_t* q, int64_t ldq,
                                     float* scale, const LaunchCtx& ctx);
