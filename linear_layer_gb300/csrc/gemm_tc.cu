@@ -302,6 +302,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + S + s); };
   auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * S + b); };
@@ -335,6 +336,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   const int num_n = (p.N + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;
+
+  // programmatic dependent launch (as in the pair kernel): L2 prefetch of the first
+  // ring of operand tiles, then the wait for the previous kernel of the stream
+  if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < num_tiles) {
+    int mb, nb;
+    tile_coords(blockIdx.x, num_m, num_n, p.group_m, mb, nb);
+    const int pre = KB < S ? KB : S;
+    for (int kb = 0; kb < pre; ++kb) {
+      tma_prefetch_l2(&tmA, kb * Cfg::BK, mb * 128);
+      for (int j = 0; j < Cfg::B_BOXES; ++j) tma_prefetch_l2(&tmB, nb * BN + j * Cfg::B_BOX_N, kb * Cfg::BK);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -616,6 +630,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
@@ -668,6 +683,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     n0 = nb * BN + (half > 0 ? BN / 2 : 0);
     ncols = half < 0 ? BN : BN / 2;
   };
+
+  // Programmatic dependent launch: everything above overlaps the previous kernel of
+  // the stream; the producer also pulls its first ring of operand tiles into L2 (L2 is
+  // coherent, so a prefetch may run ahead of the previous kernel's writes).  Operand
+  // copies into shared memory, scale and C reads and D writes come after the wait.
+  if (warp == 0 && lane == 0 && pair < sc.num_units) {
+    int m0, n0, ncols;
+    unit(pair, m0, n0, ncols);
+    const int boxes = ncols / 2 / Cfg::B_BOX_N;
+    const int pre = KB < S ? KB : S;
+    for (int kb = 0; kb < pre; ++kb) {
+      tma_prefetch_l2(&tmA, kb * Cfg::BK, m0 + 128 * static_cast<int>(rank));
+      for (int j = 0; j < boxes; ++j)
+        tma_prefetch_l2(&tmB, n0 + static_cast<int>(rank) * (ncols / 2) + j * Cfg::B_BOX_N, kb * Cfg::BK);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (each CTA)
@@ -986,8 +1018,21 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
 
   const int num_tiles = ((a.M + 127) / 128) * ((a.N + Cfg::BN - 1) / Cfg::BN);
   const int grid = num_tiles < ctx.num_sms ? num_tiles : ctx.num_sms;
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM, ctx.stream>>>(tmA, tmB, p);
-  return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) {
+    cudaGetLastError();
+    return LL_ERR_CUDA;
+  }
+  return LL_OK;
 }
 
 
@@ -1010,13 +1055,15 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   cfg.blockDim = dim3(Cfg::THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = ctx.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // co-resident CTA pairs (one CTA per SM): the persistent grid
   static int max_pairs[kMaxDev] = {};
   int dev = 0;
