@@ -803,7 +803,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
       int m0, n0, ncols;
       unit(u, m0, n0, ncols);
-      const int row0 = m0 + 128 * static_cast<int>(rank) + 4 * lane;
+      // lane l copies rows l, l + 32, l + 64, l + 96: each cp.async of the warp writes 32
+      // consecutive words (no bank conflicts)
+      const int row0 = m0 + 128 * static_cast<int>(rank) + lane;
       const int nb0 = n0 / 128;
       for (int kb = 0; kb < KB; ++kb) {
         const int j = seq % J;
@@ -816,9 +818,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         float* slot = scales + j * Cfg::SC_FLOATS;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int row = row0 + i;
+          const int row = row0 + 32 * i;
           const bool v = row < p.M;
-          cp_async_4(smem_addr(slot + 4 * lane + i), v ? p.sA + static_cast<int64_t>(row) * p.ld_sa + kb : p.sA,
+          cp_async_4(smem_addr(slot + lane + 32 * i), v ? p.sA + static_cast<int64_t>(row) * p.ld_sa + kb : p.sA,
                      v ? 4u : 0u);
         }
         if (lane < 2) {
