@@ -1,0 +1,93 @@
+"""Randomised GPU parity sweep of the GEMM entry points against the CPU oracle (seeded,
+so every run checks the same cases): FP16 / BF16 / FP8 E4M3 and E5M2 operands, random
+sizes from a few rows to several CTA-pair tiles, padded and TMA-illegal pitches,
+alpha / beta, every output type, the allocation-free entry.  Rows are sampled (first
+and last rows of tiles, the M tail and random rows); the tolerance bar is the one of
+the other GEMM tests."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import check_close, out_code, out_tensor, up
+
+pytestmark = pytest.mark.gpu
+
+OUTS = ["f32", "bf16", "f16"]
+
+
+def _case(seed):
+    rng = np.random.default_rng(9000 + seed)
+    big = rng.random() < 0.3  # some cases large enough for the CTA-pair kernel
+    M = int(rng.integers(300, 1500) if big else rng.integers(1, 400))
+    N = int(rng.integers(300, 1500) if big else rng.integers(1, 400))
+    K = int(rng.integers(1, 1200))
+    pad_a = int(rng.choice([0, 0, 8, 16, 3]))
+    pad_b = int(rng.choice([0, 0, 8, 32, 5]))
+    alpha = float(rng.choice([1.0, 0.5, -2.0]))
+    beta = float(rng.choice([0.0, 0.0, 1.0, -0.75]))
+    out = OUTS[int(rng.integers(0, 3))]
+    return rng, M, N, K, pad_a, pad_b, alpha, beta, out
+
+
+def _rows(rng, M):
+    r = {0, M - 1, min(M - 1, 127), min(M - 1, 128), min(M - 1, 255), min(M - 1, 256)}
+    r |= set(int(x) for x in rng.integers(0, M, 6))
+    return np.array(sorted(r))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_16bit(orc, seed):
+    import linear_layer_gb300 as ll
+    rng, M, N, K, pad_a, pad_b, alpha, beta, out = _case(seed)
+    kind = "f16" if seed % 2 == 0 else "bf16"
+    lda, ldb = K + pad_a, N + pad_b
+    A = wl.operand(kind, M, K, 100 + seed, ld=lda)
+    B = wl.operand(kind, K, N, 200 + seed, ld=ldb)
+    C = wl.f32_normal(M, N, 300 + seed) if beta != 0.0 else None
+    tD = out_tensor(M, N, out)
+    in_type = ll.IN_F16 if kind == "f16" else ll.IN_BF16
+    noalloc = kind == "f16" and seed % 4 == 0
+    if noalloc:
+        ll.gemm_f16_noalloc(M, N, K, alpha, up(A), lda, up(B), ldb, beta, up(C), N, tD, N, out_code(out))
+    else:
+        need = ll.gemm_workspace_size(M, N, K, lda, ldb, in_type)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+        fn = ll.gemm_f16 if kind == "f16" else ll.gemm_bf16
+        fn(M, N, K, alpha, up(A), lda, up(B), ldb, beta, up(C), N, tD, N, out_code(out), workspace=ws)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, word
+    rows = _rows(rng, M)
+    ref, absab = orc.gemm(kind, M, N, K, alpha, A.ravel(), lda, B.ravel(), ldb, beta,
+                          None if C is None else C.ravel(), N, rows=rows)
+    check_close(tD.float().cpu().numpy().astype(np.float64)[rows], ref, absab, K, out, kind,
+                what="seed %d %s %dx%dx%d lda %d ldb %d a %g b %g %s%s" % (
+                    seed, kind, M, N, K, lda, ldb, alpha, beta, out, " noalloc" if noalloc else ""))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_fp8(orc, seed):
+    import linear_layer_gb300 as ll
+    rng, M, N, K, pad_a, pad_b, alpha, beta, out = _case(100 + seed)
+    a_fmt = ["e4m3", "e5m2"][seed % 2]
+    b_fmt = ["e4m3", "e5m2"][(seed // 2) % 2]
+    lda, ldb = K + pad_a, N + pad_b
+    A, sA = wl.e4m3_blockquant_rowblocks(M, K, 400 + seed, ld=lda, fmt=a_fmt)
+    B, sB = wl.e4m3_blockquant(K, N, 500 + seed, 128, 128, ld=ldb, fmt=b_fmt)
+    C = wl.f32_normal(M, N, 600 + seed) if beta != 0.0 else None
+    KB, NB = sA.shape[1], sB.shape[1]
+    tD = out_tensor(M, N, out)
+    need = ll.gemm_workspace_size(M, N, K, lda, ldb, ll.IN_E4M3)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+    code = {"e4m3": ll.IN_E4M3, "e5m2": ll.IN_E5M2}
+    ll.gemm_f8_blockscaled_mixed(code[a_fmt], code[b_fmt], M, N, K, alpha, up(A), lda, up(sA), KB, up(B), ldb,
+                                 up(sB), NB, beta, up(C), N, tD, N, out_code(out), workspace=ws)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, word
+    rows = _rows(rng, M)
+    ref, absab = orc.gemm_f8_blockscaled_mixed(a_fmt, b_fmt, M, N, K, alpha, A.ravel(), lda, sA.ravel(), KB,
+                                               B.ravel(), ldb, sB.ravel(), NB, beta,
+                                               None if C is None else C.ravel(), N, rows=rows)
+    check_close(tD.float().cpu().numpy().astype(np.float64)[rows], ref, absab, K, out, "e4m3",
+                what="seed %d %s x %s %dx%dx%d lda %d ldb %d a %g b %g %s" % (
+                    seed, a_fmt, b_fmt, M, N, K, lda, ldb, alpha, beta, out))
