@@ -251,6 +251,71 @@ __global__ void __launch_bounds__(kWoThreads, CTAS) w8a16_kernel(const WoParams 
   }
 }
 
+// One token, K a multiple of 4096 (exact rows, as the W8A8 GEMV's exact path): warp g of
+// the grid owns rows g, g + G, ...; each lane streams 8 16-byte pieces of a row per batch
+// (4 KB per warp in flight, the next row's first batch requested before the reduction),
+// with the activation staged once per CTA in shared memory.  Measured 4491 vs 3798 GB/s
+// on the 11008 x 4096 layer against the general walk.
+__global__ void __launch_bounds__(256, 3) w8a16_row_kernel(const WoParams p) {
+  extern __shared__ int4 smem[];  // the token's K activations, BF16
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int G = gridDim.x * 8;
+  const int nb = p.K >> 12;  // 4096-element batches per row
+  int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  int4 w[8];
+  auto ld_batch = [&](int rr, int b) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      w[j] = rr < p.N ? ld_stream(reinterpret_cast<const int4*>(p.W + static_cast<int64_t>(rr) * p.ldw) + b * 256 + lane + 32 * j)
+                      : make_int4(0, 0, 0, 0);
+  };
+  ld_batch(r, 0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = threadIdx.x; i < (p.K >> 3); i += 256) smem[i] = reinterpret_cast<const int4*>(p.X)[i];
+  __syncthreads();
+  while (r < p.N) {
+    uint64_t acc2 = 0ull;
+    for (int b = 0;;) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = b * 256 + lane + 32 * j;  // 16-byte weight piece: K 16 c .. 16 c + 15
+        const int4 lo = smem[2 * c], hi = smem[2 * c + 1];
+        const uint32_t xr[8] = {static_cast<uint32_t>(lo.x), static_cast<uint32_t>(lo.y), static_cast<uint32_t>(lo.z),
+                                static_cast<uint32_t>(lo.w), static_cast<uint32_t>(hi.x), static_cast<uint32_t>(hi.y),
+                                static_cast<uint32_t>(hi.z), static_cast<uint32_t>(hi.w)};
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const uint32_t wd = e4 == 0 ? w[j].x : e4 == 1 ? w[j].y : e4 == 2 ? w[j].z : w[j].w;
+          const uint32_t q = wd ^ 0x80808080u;
+          fma_f32x2(acc2, bf16x2_to_f32x2(xr[2 * e4]), bytes_to_f32x2(q, 0));
+          fma_f32x2(acc2, bf16x2_to_f32x2(xr[2 * e4 + 1]), bytes_to_f32x2(q, 2));
+        }
+      }
+      if (++b == nb) break;
+      ld_batch(r, b);
+    }
+    const int rn = r + G;
+    ld_batch(rn, 0);  // next row in flight while this one is reduced and stored
+    uint32_t lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(acc2));
+    float v = __fadd_rn(__uint_as_float(lo), __uint_as_float(hi));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) {
+      v = __fmul_rn(v, p.w_scale[r]);
+      if (p.bias) v = __fadd_rn(v, p.bias[r]);
+      if (p.y_type == LL_OUT_F32)
+        static_cast<float*>(p.Y)[r] = v;
+      else if (p.y_type == LL_OUT_BF16)
+        static_cast<__nv_bfloat16*>(p.Y)[r] = __float2bfloat16_rn(v);
+      else
+        static_cast<__half*>(p.Y)[r] = __float2half_rn(v);
+    }
+    r = rn;
+  }
+}
+
 // Any shape or alignment: one warp per (token, output row), scalar loads.
 __global__ void __launch_bounds__(256) w8a16_plain_kernel(const WoParams p) {
   const int lane = threadIdx.x & 31;
@@ -358,6 +423,33 @@ ll_status launch_linear_w8a16(int M, int N, int K, const void* X, int64_t ldx, c
     p.M = MT;
     p.X = static_cast<const __nv_bfloat16*>(X) + static_cast<int64_t>(m0) * ldx;
     p.Y = static_cast<char*>(Y) + static_cast<int64_t>(m0) * ldy * ysize;
+    if (MT == 1 && K % 4096 == 0) {  // one token, exact rows
+      const int smem = K * 2;
+      if (smem > 48 * 1024 &&
+          cudaFuncSetAttribute(w8a16_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return LL_ERR_CUDA;
+      }
+      int grid = 3 * ctx.num_sms;
+      const int need = (N + 7) / 8;
+      if (need < grid) grid = need;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid);
+      cfg.blockDim = dim3(256);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = ctx.stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, w8a16_row_kernel, p) != cudaSuccess) {
+        cudaGetLastError();
+        return LL_ERR_CUDA;
+      }
+      m0 += 1;
+      continue;
+    }
     ll_status st;
     switch (MT) {
       // launch shapes (rows per group, pieces per step, steps in flight, CTAs per SM)
