@@ -566,6 +566,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 //   tempty[b] (even CTA)  one arrival per epilogue warp of each CTA.
 // 16-bit inputs: the accumulator of a tile is double buffered in TMEM (2 x 256
 // columns) and 4 epilogue warps per CTA drain one while the MMAs fill the other.
+// When the rows of C and D start on 16-byte boundaries each lane stores its own row
+// straight from registers (128-byte C reads, 64-byte BF16 writes per lane and chunk),
+// skipping the shared-memory transpose, whose traffic competed with the operand ring
+// (measured +3.5 % on 4096^3).  Other pitches keep the transpose, which turns them
+// into coalesced row segments (per-lane rows would be 4-byte scalar accesses).
 // Output tiles past the last full wave are split into two 256 x 128 halves when that
 // lets one half-wave finish the problem.
 // FP8 inputs: each 128-K block is accumulated into one of two TMEM partial buffers;
@@ -593,7 +598,7 @@ struct PairCfg {
   static constexpr int EPI_WARP0 = FP8 ? 3 : 2;  // warps: producer, MMA, [scales], epilogue
   static constexpr int EPI_WARPS = FP8 ? 8 : 4;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
-  static constexpr int EPI_STAGE_BYTES = FP8 ? 0 : EPI_WARPS * 32 * 32 * 4;
+  static constexpr int EPI_STAGE_BYTES = FP8 ? 0 : EPI_WARPS * 32 * 32 * 4;  // unaligned-pitch epilogue
   static constexpr int SC_SLOTS = FP8 ? 8 : 0;
   static constexpr int SC_FLOATS = 128 + 4;  // scale_a of 128 rows, scale_b of 2 blocks, pad
   static constexpr int SC_BYTES = SC_SLOTS * SC_FLOATS * 4;
@@ -838,6 +843,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     float* st = epi_stage + (warp - Cfg::EPI_WARP0) * 32 * 32;
+    // rows of C and D on 16-byte boundaries: each lane stores its own row; otherwise
+    // chunks are transposed through shared memory into coalesced row segments
+    const bool by_rows = p.d_row16 && (p.beta == 0.0f || p.c_vec);
     uint32_t acc_it = 0;
     for (int u = pair; u < sc.num_units; u += num_pairs) {
       int m0, n0, ncols;
@@ -859,10 +867,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
         }
-        float v[32];
+        float v[1][32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        epilogue_chunk<8>(p, st, m_base, n0 + c * 32, v, lane);
+        for (int j = 0; j < 32; ++j) v[0][j] = __uint_as_float(r[j]);
+        if (by_rows)
+          epilogue_rows<1>(p, m_base + lane, n0 + c * 32, v);
+        else
+          epilogue_chunk<8>(p, st, m_base, n0 + c * 32, v[0], lane);
       }
       ++acc_it;
     }
