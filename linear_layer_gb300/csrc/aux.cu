@@ -11,26 +11,57 @@
 
 namespace ll {
 
-// Each thread writes one 16-byte vector of a destination row (the destination pitch is a
-// multiple of 16 bytes); columns past `cols` are the pad and are written as zero.
-template <class T>
-__global__ void repack_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst,
-                              int64_t ld_dst, int rows, int cols) {
-  constexpr int V = 16 / sizeof(T);
-  const int64_t vec_per_row = ld_dst / V;
+// Each thread writes one 16-byte vector of a destination row (the destination pitch is
+// a multiple of 16 bytes); bytes past the source row's `row_bytes` are the pad and are
+// written as zero.  The source row may start at any element boundary: the thread reads
+// the two aligned 16-byte words that cover its 16 source bytes and funnel-shifts them
+// into place, so every global access is a full 16-byte vector.  A word is read only if
+// it holds at least one byte of the row, and an aligned 16-byte word never crosses a
+// page, so no read leaves the source allocation's pages.  The kernel lets the
+// programmatically launched GEMM behind it start its prologue at once; the GEMM's
+// dependency wait still covers every write made here.
+__global__ void repack_kernel(const uint8_t* __restrict__ src, int64_t ld_src, uint8_t* __restrict__ dst,
+                              int64_t ld_dst, int rows, int64_t row_bytes) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t vec_per_row = ld_dst / 16;
   const int64_t total = static_cast<int64_t>(rows) * vec_per_row;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / vec_per_row;
-    const int64_t c0 = (i - r * vec_per_row) * V;
-    const T* s = src + r * ld_src + c0;
-    union {
-      T e[V];
-      uint4 u;
-    } buf;
+    const int64_t b0 = (i - r * vec_per_row) * 16;  // first byte of this vector in the row
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (b0 < row_bytes) {
+      const uintptr_t sa = reinterpret_cast<uintptr_t>(src + r * ld_src + b0);
+      const uintptr_t row_end = reinterpret_cast<uintptr_t>(src + r * ld_src + row_bytes);
+      const uint32_t off = static_cast<uint32_t>(sa & 15u);
+      const uint4* base = reinterpret_cast<const uint4*>(sa - off);
+      const uint4 lo = __ldg(base);
+      const uint4 hi = (sa - off + 16 < row_end) ? __ldg(base + 1) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      // t[k] = w[off / 4 + k] through two fixed-index selections
+      const uint32_t ws = off >> 2, bs = (off & 3u) * 8u;
+      uint32_t s1[7], t[5];
 #pragma unroll
-    for (int v = 0; v < V; ++v) buf.e[v] = (c0 + v < cols) ? s[v] : T(0);
-    *reinterpret_cast<uint4*>(dst + r * ld_dst + c0) = buf.u;
+      for (int k = 0; k < 7; ++k) s1[k] = (ws & 1u) ? w[k + 1] : w[k];
+#pragma unroll
+      for (int k = 0; k < 5; ++k) t[k] = (ws & 2u) ? s1[k + 2] : s1[k];
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(t[k], t[k + 1], bs);
+      const int64_t valid = row_bytes - b0;  // >= 1
+      if (valid < 16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int64_t keep = valid - 4 * k;  // bytes of word k inside the row
+          if (keep <= 0)
+            o[k] = 0u;
+          else if (keep < 4)
+            o[k] &= (1u << (8 * keep)) - 1u;
+        }
+      }
+      out = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    *reinterpret_cast<uint4*>(dst + r * ld_dst + b0) = out;
   }
 }
 
@@ -40,13 +71,10 @@ ll_status launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_d
   const int threads = 256;
   const int64_t vecs = static_cast<int64_t>(rows) * (ld_dst * esize / 16);
   int64_t blocks = (vecs + threads - 1) / threads;
-  if (blocks > 16 * ctx.num_sms) blocks = 16 * ctx.num_sms;
-  if (esize == 2)
-    repack_kernel<uint16_t><<<static_cast<int>(blocks), threads, 0, ctx.stream>>>(
-        static_cast<const uint16_t*>(src), ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
-  else
-    repack_kernel<uint8_t><<<static_cast<int>(blocks), threads, 0, ctx.stream>>>(
-        static_cast<const uint8_t*>(src), ld_src, static_cast<uint8_t*>(dst), ld_dst, rows, cols);
+  if (blocks > 8 * ctx.num_sms) blocks = 8 * ctx.num_sms;
+  repack_kernel<<<static_cast<int>(blocks), threads, 0, ctx.stream>>>(
+      static_cast<const uint8_t*>(src), ld_src * esize, static_cast<uint8_t*>(dst), ld_dst * esize, rows,
+      static_cast<int64_t>(cols) * esize);
   return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 

@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -44,6 +45,7 @@ struct GemmParams {
   int d_type;
   int c_vec, d_vec;  // rows of C / D may be accessed with 4-element vectors
   int d_row16;       // rows of D start on 16-byte boundaries
+  int epi_tma;       // CTA-pair 16-bit epilogue through TMA (C and D rows 16-byte aligned)
   const float* sA;
   int64_t ld_sa;
   const float* sB;
@@ -107,22 +109,164 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int gro
   nb = r / gsz;
 }
 
-// Epilogue of one 32 x 32 chunk owned by a warp: rows m_base .. m_base + 31 (lane t holds
-// row m_base + t in v[0..31]), columns n0 .. n0 + 31:
+// Epilogue.  A chunk is 32 rows of a tile (lane t of the warp holds row m + t of the
+// accumulator) by 32 columns n .. n + 31:
 //   D[m][n] = alpha * acc[m][n] + beta * C[m][n]   (C not read when beta == 0)
-// The chunk is transposed through the warp's 32 x 32 FP32 staging buffer; float4 slot
-// c of row r is stored at slot c ^ (r & 7), which keeps the row-per-lane writes and
-// the segment-per-8-lanes reads free of bank conflicts.  Afterwards lane l handles
-// columns 4*(l%8) .. 4*(l%8)+3 of rows 4*i + l/8 (i = 0..7): each warp access is four
-// 128-byte row segments (4-element vectors where the pitch allows, else scalars).  C
-// loads are issued G rows at a time before the stores of those rows (C may alias D, so
-// a later load cannot move above an earlier store).  Measured alternatives that were
-// slower: a column-per-lane pass for unaligned pitches, and prefetching the next
-// tile's C rows into L2 (it evicted operand panels).
-template <int G>  // rows handled per batch of C loads (8 or 4; smaller = fewer registers)
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, float* st, int m_base, int n0,
-                                               const float (&v)[32], int lane) {
-  static_assert(8 % G == 0, "G must divide 8");
+// evaluated as fma(beta, C, alpha * acc) in FP32 and rounded once to the output type,
+// identically in both layouts below, so the two agree bit for bit.  Each chunk is split
+// into a C load into registers and a store, so that a caller can load the next chunk's
+// C while it stores this one.  C may alias D only as the same matrix (same base and
+// pitch): a thread then reads every element before it writes it, and loads of a later
+// chunk never touch elements stored earlier.
+//
+// Row layout (rows of C and D on 16-byte boundaries): each lane reads and writes its
+// own row segment straight from registers.
+__device__ __forceinline__ void load_c_row(const GemmParams& p, int m, int n, float (&cv)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) cv[j] = 0.0f;
+  if (p.beta == 0.0f || m >= p.M || n >= p.N) return;
+  const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
+  if (n + 32 <= p.N && p.c_vec) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(crow + j);
+      cv[j] = t.x;
+      cv[j + 1] = t.y;
+      cv[j + 2] = t.z;
+      cv[j + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < p.N) cv[j] = crow[j];
+  }
+}
+
+__device__ __forceinline__ void store_row(const GemmParams& p, int m, int n, const float (&acc)[32],
+                                          const float (&cv)[32]) {
+  if (m >= p.M || n >= p.N) return;
+  const bool full = n + 32 <= p.N;
+  float o[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    o[j] = p.alpha * acc[j];
+    if (p.beta != 0.0f) o[j] = fmaf(p.beta, cv[j], o[j]);
+  }
+  const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
+  if (p.d_type == LL_OUT_F32) {
+    float* dp = static_cast<float*>(p.D) + off;
+    if (full && p.d_row16) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < p.N) dp[j] = o[j];
+    }
+  } else {
+    const bool bf = p.d_type == LL_OUT_BF16;
+    uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (bf) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+        w[j] = *reinterpret_cast<uint32_t*>(&h2);
+      } else {
+        __half2 h2 = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
+        w[j] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+    }
+    if (full && p.d_row16) {
+#pragma unroll
+      for (int j = 0; j < 16; j += 4)
+        *reinterpret_cast<uint4*>(dp + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < p.N) dp[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+    }
+  }
+}
+
+// Up to CH consecutive chunks of one row (lane = row m), read straight from the FP32
+// accumulator registers (the FP8 promotion epilogue, which holds CH = 4 chunks): C is
+// consumed four columns at a time as it arrives, which keeps register pressure down.
+template <int CH>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0,
+                                              float (&acc)[CH][32]) {
+  if (m >= p.M) return;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int n = n0 + 32 * c;
+    if (n >= p.N) break;
+    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc[c][j] *= p.alpha;
+    if (p.beta != 0.0f) {
+      if (n + 32 <= p.N && p.c_vec) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 cv = *reinterpret_cast<const float4*>(crow + j);
+          acc[c][j] = fmaf(p.beta, cv.x, acc[c][j]);
+          acc[c][j + 1] = fmaf(p.beta, cv.y, acc[c][j + 1]);
+          acc[c][j + 2] = fmaf(p.beta, cv.z, acc[c][j + 2]);
+          acc[c][j + 3] = fmaf(p.beta, cv.w, acc[c][j + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < p.N) acc[c][j] = fmaf(p.beta, crow[j], acc[c][j]);
+      }
+    }
+    const float zero[32] = {};
+    // alpha and beta are applied: store_row with alpha = 1, beta = 0 only casts
+    GemmParams q = p;
+    q.alpha = 1.0f;
+    q.beta = 0.0f;
+    store_row(q, m, n, acc[c], zero);
+  }
+}
+
+// Transposed layout (any pitch): the chunk goes through the warp's 32 x 32 FP32
+// staging buffer; float4 slot c of row r is stored at slot c ^ (r & 7), which keeps
+// the row-per-lane writes and the segment-per-8-lanes reads free of bank conflicts.
+// Lane l then handles columns 4*(l%8) .. 4*(l%8)+3 of rows 4*g + l/8 (g = 0..7): each
+// warp access is four 128-byte row segments (4-element vectors where the pitch allows,
+// else scalars).  In this layout cv[4*g + i] is column 4*(l%8) + i of row 4*g + l/8.
+// Measured alternatives that were slower: a column-per-lane pass for unaligned
+// pitches, and prefetching the next tile's C rows into L2 (it evicted operand panels).
+__device__ __forceinline__ void load_c_chunk(const GemmParams& p, int m_base, int n0, int lane,
+                                             float (&cv)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) cv[j] = 0.0f;
+  const int n = n0 + 4 * (lane & 7);
+  const int ncols = min(4, p.N - n);  // valid columns of this lane (<= 0: none)
+  if (p.beta == 0.0f || ncols <= 0) return;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int m = m_base + 4 * g + (lane >> 3);
+    if (m < p.M) {
+      const float* cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
+      if (ncols == 4 && p.c_vec) {
+        const float4 t = *reinterpret_cast<const float4*>(cp);
+        cv[4 * g] = t.x;
+        cv[4 * g + 1] = t.y;
+        cv[4 * g + 2] = t.z;
+        cv[4 * g + 3] = t.w;
+      } else {
+        cv[4 * g] = cp[0];
+        if (ncols > 1) cv[4 * g + 1] = cp[1];
+        if (ncols > 2) cv[4 * g + 2] = cp[2];
+        if (ncols > 3) cv[4 * g + 3] = cp[3];
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_chunk(const GemmParams& p, float* st, int m_base, int n0,
+                                            const float (&v)[32], const float (&cv)[32], int lane) {
   float4* st4 = reinterpret_cast<float4*>(st);
 #pragma unroll
   for (int c = 0; c < 8; ++c)
@@ -130,157 +274,53 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, float* st, i
   __syncwarp();
   const int c4 = lane & 7;
   const int n = n0 + 4 * c4;
-  const int ncols = min(4, p.N - n);  // valid columns of this lane (<= 0: none)
+  const int ncols = min(4, p.N - n);
   const bool full_cols = ncols == 4;
 #pragma unroll
-  for (int g = 0; g < 8; g += G) {
-    float4 cv[G];
+  for (int g = 0; g < 8; ++g) {
+    const int r = 4 * g + (lane >> 3);
+    const int m = m_base + r;
+    if (m >= p.M || ncols <= 0) continue;
+    const float4 a = st4[r * 8 + (c4 ^ (r & 7))];
+    float o[4] = {p.alpha * a.x, p.alpha * a.y, p.alpha * a.z, p.alpha * a.w};
     if (p.beta != 0.0f) {
 #pragma unroll
-      for (int i = 0; i < G; ++i) {
-        const int m = m_base + 4 * (g + i) + (lane >> 3);
-        cv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (m < p.M && ncols > 0) {
-          const float* cp = p.C + static_cast<int64_t>(m) * p.ldc + n;
-          if (full_cols && p.c_vec) {
-            cv[i] = *reinterpret_cast<const float4*>(cp);
-          } else {
-            cv[i].x = cp[0];
-            if (ncols > 1) cv[i].y = cp[1];
-            if (ncols > 2) cv[i].z = cp[2];
-            if (ncols > 3) cv[i].w = cp[3];
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < G; ++i) {
-      const int r = 4 * (g + i) + (lane >> 3);
-      const int m = m_base + r;
-      if (m >= p.M || ncols <= 0) continue;
-      const float4 a = st4[r * 8 + (c4 ^ (r & 7))];
-      float4 o;
-      o.x = p.alpha * a.x;
-      o.y = p.alpha * a.y;
-      o.z = p.alpha * a.z;
-      o.w = p.alpha * a.w;
-      if (p.beta != 0.0f) {
-        o.x += p.beta * cv[i].x;
-        o.y += p.beta * cv[i].y;
-        o.z += p.beta * cv[i].z;
-        o.w += p.beta * cv[i].w;
-      }
-      const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
-      if (p.d_type == LL_OUT_F32) {
-        float* dp = static_cast<float*>(p.D) + off;
-        if (full_cols && p.d_vec) {
-          *reinterpret_cast<float4*>(dp) = o;
-        } else {
-          dp[0] = o.x;
-          if (ncols > 1) dp[1] = o.y;
-          if (ncols > 2) dp[2] = o.z;
-          if (ncols > 3) dp[3] = o.w;
-        }
-      } else if (p.d_type == LL_OUT_BF16) {
-        __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(p.D) + off;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
-        if (full_cols && p.d_vec) {
-          uint2 u;
-          u.x = *reinterpret_cast<uint32_t*>(&lo);
-          u.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(dp) = u;
-        } else {
-          dp[0] = lo.x;
-          if (ncols > 1) dp[1] = lo.y;
-          if (ncols > 2) dp[2] = hi.x;
-          if (ncols > 3) dp[3] = hi.y;
-        }
-      } else {
-        __half* dp = static_cast<__half*>(p.D) + off;
-        __half2 lo = __floats2half2_rn(o.x, o.y), hi = __floats2half2_rn(o.z, o.w);
-        if (full_cols && p.d_vec) {
-          uint2 u;
-          u.x = *reinterpret_cast<uint32_t*>(&lo);
-          u.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(dp) = u;
-        } else {
-          dp[0] = lo.x;
-          if (ncols > 1) dp[1] = lo.y;
-          if (ncols > 2) dp[2] = hi.x;
-          if (ncols > 3) dp[3] = hi.y;
-        }
-      }
-    }
-  }
-  __syncwarp();
-}
-
-// FP8 epilogue straight from registers: lane = one row, acc = 4 x 32 consecutive
-// columns from n0.  D = alpha * acc + beta * C.
-template <int CH>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0,
-                                              const float (&acc)[CH][32]) {
-  if (m >= p.M) return;
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int n = n0 + 32 * c;
-    if (n >= p.N) break;
-    const bool full = n + 32 <= p.N;
-    float o[32];
-    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
-    if (p.beta != 0.0f && full && p.c_vec) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 cv = *reinterpret_cast<const float4*>(crow + j);
-        o[j] = p.alpha * acc[c][j] + p.beta * cv.x;
-        o[j + 1] = p.alpha * acc[c][j + 1] + p.beta * cv.y;
-        o[j + 2] = p.alpha * acc[c][j + 2] + p.beta * cv.z;
-        o[j + 3] = p.alpha * acc[c][j + 3] + p.beta * cv.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        o[j] = p.alpha * acc[c][j];
-        if (p.beta != 0.0f && n + j < p.N) o[j] += p.beta * crow[j];
-      }
+      for (int i = 0; i < 4; ++i) o[i] = fmaf(p.beta, cv[4 * g + i], o[i]);
     }
     const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
     if (p.d_type == LL_OUT_F32) {
       float* dp = static_cast<float*>(p.D) + off;
-      if (full && p.d_row16) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      if (full_cols && p.d_vec) {
+        *reinterpret_cast<float4*>(dp) = make_float4(o[0], o[1], o[2], o[3]);
       } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n + j < p.N) dp[j] = o[j];
+        dp[0] = o[0];
+        if (ncols > 1) dp[1] = o[1];
+        if (ncols > 2) dp[2] = o[2];
+        if (ncols > 3) dp[3] = o[3];
       }
     } else {
-      const bool bf = p.d_type == LL_OUT_BF16;
-      uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
-      uint32_t w[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (bf) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-          w[j] = *reinterpret_cast<uint32_t*>(&h2);
-        } else {
-          __half2 h2 = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
-          w[j] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-      }
-      if (full && p.d_row16) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-          *reinterpret_cast<uint4*>(dp + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+      uint32_t lo, hi;
+      if (p.d_type == LL_OUT_BF16) {
+        __nv_bfloat162 l2 = __floats2bfloat162_rn(o[0], o[1]), h2 = __floats2bfloat162_rn(o[2], o[3]);
+        lo = *reinterpret_cast<uint32_t*>(&l2);
+        hi = *reinterpret_cast<uint32_t*>(&h2);
       } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n + j < p.N) dp[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+        __half2 l2 = __floats2half2_rn(o[0], o[1]), h2 = __floats2half2_rn(o[2], o[3]);
+        lo = *reinterpret_cast<uint32_t*>(&l2);
+        hi = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
+      if (full_cols && p.d_vec) {
+        *reinterpret_cast<uint2*>(dp) = make_uint2(lo, hi);
+      } else {
+        dp[0] = static_cast<uint16_t>(lo);
+        if (ncols > 1) dp[1] = static_cast<uint16_t>(lo >> 16);
+        if (ncols > 2) dp[2] = static_cast<uint16_t>(hi);
+        if (ncols > 3) dp[3] = static_cast<uint16_t>(hi >> 16);
       }
     }
   }
+  __syncwarp();
 }
 
 template <class Cfg, uint32_t AB_FMT>
@@ -473,7 +513,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        epilogue_chunk<8>(p, st, m_base, nb * BN + c * 32, v, lane);
+        float cv[32];
+        load_c_chunk(p, m_base, nb * BN + c * 32, lane, cv);
+        store_chunk(p, st, m_base, nb * BN + c * 32, v, cv, lane);
       }
       ++acc_it;
     }
@@ -593,16 +635,21 @@ struct PairCfg {
   static constexpr int B_BOX_BYTES = BK * 128;
   static constexpr int B_BOXES_MAX = BN / 2 / B_BOX_N;  // per CTA
   static constexpr int STAGE_BYTES = A_BYTES + B_BOXES_MAX * B_BOX_BYTES;
-  static constexpr int STAGES = 196608 / STAGE_BYTES;
+  // 16-bit: 5 operand stages leave room for the epilogue's C / D buffers
+  static constexpr int STAGES = FP8 ? 196608 / STAGE_BYTES : 163840 / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int EPI_WARP0 = FP8 ? 3 : 2;  // warps: producer, MMA, [scales], epilogue
   static constexpr int EPI_WARPS = FP8 ? 8 : 4;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
-  static constexpr int EPI_STAGE_BYTES = FP8 ? 0 : EPI_WARPS * 32 * 32 * 4;  // unaligned-pitch epilogue
+  // 16-bit epilogue: EPI_BUFS buffers of one 32 x 32 FP32 chunk per warp (the TMA path
+  // cycles through them; the transposing path uses the first as its staging buffer)
+  static constexpr int EPI_BUFS = FP8 ? 0 : 4;
+  static constexpr int EPI_BUF_BYTES = 32 * 32 * 4;
+  static constexpr int EPI_STAGE_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
   static constexpr int SC_SLOTS = FP8 ? 8 : 0;
   static constexpr int SC_FLOATS = 128 + 4;  // scale_a of 128 rows, scale_b of 2 blocks, pad
   static constexpr int SC_BYTES = SC_SLOTS * SC_FLOATS * 4;
-  static constexpr int NBARS = 2 * STAGES + 5 + 2 * SC_SLOTS;
+  static constexpr int NBARS = 2 * STAGES + 5 + 2 * SC_SLOTS + EPI_WARPS * EPI_BUFS;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + SC_BYTES + NBARS * 8 + 16 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(TMEM_COLS <= 512, "TMEM budget");
@@ -618,6 +665,7 @@ struct PairSched {
 template <class Cfg, uint32_t AB_FMT>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                     const GemmParams p, const PairSched sc) {
   constexpr int S = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
@@ -629,7 +677,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   float* scales = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES +
                                                Cfg::SC_BYTES);
-  // bars: full[S], empty[S], tfull[2], tempty[2], drain, sc_full[J], sc_empty[J]
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain, sc_full[J], sc_empty[J],
+  //       cfull[EPI_WARPS][EPI_BUFS] (16-bit TMA epilogue: C chunk landed in a buffer)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
   uint32_t* abort_flag = tmem_slot + 1;
 
@@ -646,6 +695,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   const uint32_t drain_bar = smem_addr(bars + 2 * S + 4);
   auto sc_full_bar = [&](int j) { return smem_addr(bars + 2 * S + 5 + j); };
   auto sc_empty_bar = [&](int j) { return smem_addr(bars + 2 * S + 5 + J + j); };
+  auto cfull_bar = [&](int w, int b) {
+    return smem_addr(bars + 2 * S + 5 + 2 * Cfg::SC_SLOTS + w * Cfg::EPI_BUFS + b);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -657,10 +709,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(tempty_bar(b), 2 * Cfg::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
-    for (int j = 0; j < J; ++j) {
+    for (int j = 0; j < Cfg::SC_SLOTS; ++j) {
       mbar_init(sc_full_bar(j), 32);                  // one cp.async arrival per scale lane
       mbar_init(sc_empty_bar(j), Cfg::EPI_WARPS);     // one arrival per promotion warp
     }
+    for (int w = 0; w < Cfg::EPI_WARPS; ++w)
+      for (int b = 0; b < Cfg::EPI_BUFS; ++b) mbar_init(cfull_bar(w, b), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -841,41 +895,224 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   } else if (!Cfg::FP8) {
     // ---------------------------------------------------------------- epilogue (each CTA)
     const int q = warp & 3;
+    const int ew = warp - Cfg::EPI_WARP0;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    float* st = epi_stage + (warp - Cfg::EPI_WARP0) * 32 * 32;
-    // rows of C and D on 16-byte boundaries: each lane stores its own row; otherwise
-    // chunks are transposed through shared memory into coalesced row segments
-    const bool by_rows = p.d_row16 && (p.beta == 0.0f || p.c_vec);
-    uint32_t acc_it = 0;
-    for (int u = pair; u < sc.num_units; u += num_pairs) {
-      int m0, n0, ncols;
-      unit(u, m0, n0, ncols);
-      const uint32_t ab = acc_it & 1u;
-      bool ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const int m_base = m0 + 128 * rank + q * 32;
-      const int chunks = ncols / 32;
-#pragma unroll 1
-      for (int c = 0; c < chunks; ++c) {
-        uint32_t r[32];
-        tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
-        tmem_ld_wait();
-        if (c == chunks - 1) {  // accumulator in registers: release it to the MMA
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
+    uint8_t* ebuf = reinterpret_cast<uint8_t*>(epi_stage) + ew * Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES;
+    const int row_off = 128 * static_cast<int>(rank) + q * 32;  // this warp's rows in a pair tile
+    if (p.epi_tma) {
+      // C and D rows on 16-byte boundaries: chunks of C arrive by TMA into this warp's
+      // ring of EPI_BUFS buffers, PF chunks ahead of the one being stored (the first ones
+      // before the accumulator is ready); each lane combines its accumulator row with
+      // its C row in place, and one TMA store per chunk writes D.  Buffer b of chunk g
+      // (b = g % EPI_BUFS) is refilled only after the store of chunk g - EPI_BUFS has
+      // read it.  Chunks wholly outside the matrix are neither loaded nor stored; the
+      // chunk that crosses column N is stored by the lanes themselves (a TMA store
+      // writes whole 16-byte units and would reach into the columns past N).
+      constexpr int R = Cfg::EPI_BUFS > 2 ? Cfg::EPI_BUFS : 3;  // (FP8 instances never get here)
+      constexpr int PF = R - 2;  // C loads in flight ahead; the latest store may still read
+      const bool use_c = p.beta != 0.0f;
+      const bool out32 = p.d_type == LL_OUT_F32;
+      const bool bf = p.d_type == LL_OUT_BF16;
+      // prefetch cursor: the chunk whose C load is issued next
+      int pu = pair, pc = 0, pchunks = 0, pm = 0, pn = 0;
+      auto cursor_unit = [&](int u) {
+        pu = u;
+        pc = 0;
+        if (u < sc.num_units) {
+          int m0, n0, ncols;
+          unit(u, m0, n0, ncols);
+          pm = m0 + row_off;
+          pn = n0;
+          pchunks = ncols / 32;
         }
-        float v[1][32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[0][j] = __uint_as_float(r[j]);
-        if (by_rows)
-          epilogue_rows<1>(p, m_base + lane, n0 + c * 32, v);
-        else
-          epilogue_chunk<8>(p, st, m_base, n0 + c * 32, v[0], lane);
+      };
+      uint32_t issued = 0;  // C loads issued by this warp
+      auto issue_c = [&]() {  // lane 0; call with the ring slot free
+        if (pu >= sc.num_units) return;
+        const int b = static_cast<int>(issued % R);
+        const int n = pn + 32 * pc;
+        if (n < p.N && pm < p.M) {
+          mbar_arrive_expect_tx(cfull_bar(ew, b), Cfg::EPI_BUF_BYTES);
+          tma_load_2d(smem_addr(ebuf + b * Cfg::EPI_BUF_BYTES), &tmC, cfull_bar(ew, b), n, pm);
+        } else {
+          mbar_arrive(cfull_bar(ew, b));
+        }
+        ++issued;
+        if (++pc == pchunks) cursor_unit(pu + num_pairs);
+      };
+      if (use_c) {
+        cursor_unit(pair);
+        if (lane == 0) {
+          tma_prefetch_desc(&tmC);
+          for (int i = 0; i < PF; ++i) issue_c();
+        }
       }
-      ++acc_it;
+      if (lane == 0) tma_prefetch_desc(&tmD);
+      uint32_t acc_it = 0, g = 0;
+      bool ok = true;
+      for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
+        int m0, n0, ncols;
+        unit(u, m0, n0, ncols);
+        const uint32_t ab = acc_it & 1u;
+        ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int m_w = m0 + row_off;
+        const int chunks = ncols / 32;
+#pragma unroll 1
+        for (int c = 0; c < chunks; ++c, ++g) {
+          const int b = static_cast<int>(g % R);
+          const uint32_t bsm = smem_addr(ebuf + b * Cfg::EPI_BUF_BYTES);
+          if (lane == 0) {
+            if (use_c) {
+              bulk_wait_read<1>();  // the slot of chunk g + PF: its store (chunk g + PF - R) has read it
+              if (static_cast<int>(issued - g) < PF + 1) issue_c();
+            } else {
+              bulk_wait_read<R - 1>();  // slot b: the store of chunk g - R has read it
+            }
+          }
+          __syncwarp();
+          uint32_t r[32];
+          tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
+          tmem_ld_wait();
+          if (c == chunks - 1) {  // accumulator in registers: release it to the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
+          }
+          float o[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = p.alpha * __uint_as_float(r[j]);
+          const float4* row = reinterpret_cast<const float4*>(ebuf + b * Cfg::EPI_BUF_BYTES + lane * 128);
+          if (use_c) {
+            bool w = wait_bounded(cfull_bar(ew, b), (g / R) & 1u, wctx, kRoleEpilogue);
+            w = __all_sync(0xffffffffu, w);
+            if (!w) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // 128-byte swizzle: 16-byte slot j of row l at j ^ (l & 7)
+              const float4 cv = row[j ^ (lane & 7)];
+              o[4 * j] = fmaf(p.beta, cv.x, o[4 * j]);
+              o[4 * j + 1] = fmaf(p.beta, cv.y, o[4 * j + 1]);
+              o[4 * j + 2] = fmaf(p.beta, cv.z, o[4 * j + 2]);
+              o[4 * j + 3] = fmaf(p.beta, cv.w, o[4 * j + 3]);
+            }
+            __syncwarp();  // every C row read before a 16-bit D row overwrites it
+          }
+          const int n = n0 + 32 * c;
+          if (n + 32 <= p.N) {  // whole chunk: through shared memory and one TMA store
+            if (out32) {
+              float4* drow = reinterpret_cast<float4*>(ebuf + b * Cfg::EPI_BUF_BYTES + lane * 128);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                drow[j ^ (lane & 7)] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            } else {
+              // 64-byte rows, 64-byte swizzle: 16-byte slot j of row l at j ^ ((l >> 1) & 3)
+              uint4* drow = reinterpret_cast<uint4*>(ebuf + b * Cfg::EPI_BUF_BYTES + lane * 64);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float lo = o[8 * j + 2 * i], hi = o[8 * j + 2 * i + 1];
+                  if (bf) {
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+                    w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+                  } else {
+                    __half2 h2 = __floats2half2_rn(lo, hi);
+                    w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+                  }
+                }
+                drow[j ^ ((lane >> 1) & 3)] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && m_w < p.M) tma_store_2d(&tmD, bsm, n, m_w);
+          } else if (n < p.N && m_w + lane < p.M) {
+            // the chunk that crosses column N: a TMA store may write whole 16-byte units
+            // past N, so each lane stores its row's valid columns itself
+            const int64_t off = static_cast<int64_t>(m_w + lane) * p.ldd + n;
+            if (out32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (n + j < p.N) static_cast<float*>(p.D)[off + j] = o[j];
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (n + j < p.N)
+                  reinterpret_cast<uint16_t*>(p.D)[off + j] =
+                      bf ? __bfloat16_as_ushort(__float2bfloat16_rn(o[j])) : __half_as_ushort(__float2half_rn(o[j]));
+            }
+          }
+          if (lane == 0) bulk_commit_group();  // one group per chunk (empty without a store)
+        }
+        ++acc_it;
+      }
+      if (lane == 0) {
+        if (!ok) {  // C loads still in flight land before the CTA may exit
+          for (uint32_t j = g; j < issued; ++j)
+            wait_drain(cfull_bar(ew, static_cast<int>(j % R)), (j / R) & 1u, p.timeout_ns);
+        }
+        bulk_wait_all();
+      }
+      __syncwarp();
+    } else {
+      // unaligned rows of C or D: each chunk is transposed through shared memory into
+      // coalesced row segments.  C is loaded into registers one chunk ahead: chunk c + 1
+      // while chunk c is stored, and the first chunk of a unit before its accumulator is
+      // ready.  Units have 8 or 4 chunks, so chunks go in (even, odd) pairs.
+      float* st = reinterpret_cast<float*>(ebuf);
+      float c_even[32], c_odd[32];
+      uint32_t acc_it = 0;
+      if (pair < sc.num_units) {
+        int m0, n0, ncols;
+        unit(pair, m0, n0, ncols);
+        load_c_chunk(p, m0 + row_off, n0, lane, c_even);
+      }
+      for (int u = pair; u < sc.num_units; u += num_pairs) {
+        int m0, n0, ncols;
+        unit(u, m0, n0, ncols);
+        const uint32_t ab = acc_it & 1u;
+        bool ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int m_base = m0 + row_off;
+        const int chunks = ncols / 32;
+#pragma unroll 1
+        for (int c = 0; c < chunks; c += 2) {
+          uint32_t r[32];
+          float v[32];
+          load_c_chunk(p, m_base, n0 + (c + 1) * 32, lane, c_odd);
+          tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          store_chunk(p, st, m_base, n0 + c * 32, v, c_even, lane);
+          if (c + 2 < chunks) {
+            load_c_chunk(p, m_base, n0 + (c + 2) * 32, lane, c_even);
+          } else if (u + num_pairs < sc.num_units) {  // the next unit's first chunk
+            int m1, n1, nc1;
+            unit(u + num_pairs, m1, n1, nc1);
+            load_c_chunk(p, m1 + row_off, n1, lane, c_even);
+          }
+          tmem_ld_x32(tmem_base + lane_base + ab * BN + (c + 1) * 32, r);
+          tmem_ld_wait();
+          if (c + 2 == chunks) {  // accumulator in registers: release it to the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          store_chunk(p, st, m_base, n0 + (c + 1) * 32, v, c_odd, lane);
+        }
+        ++acc_it;
+      }
     }
   } else {
     // ---------------------------------------------------------------- promotion (FP8, each CTA)
@@ -970,7 +1207,8 @@ static EncodeTiledFn encode_fn() {
 
 // 2-D row-major matrix rows x cols (pitch in elements) with a box of box_cols x box_rows.
 bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
-                        int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows) {
+                        int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows,
+                        CUtensorMapSwizzle swizzle) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -978,8 +1216,7 @@ bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType 
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -1000,6 +1237,7 @@ static GemmParams make_params(const GemmArgs& a, const LaunchCtx& ctx) {
   // vector stores: 16 bytes (FP32) or 8 bytes (BF16 / FP16) per lane, at 4-column steps
   p.d_vec = (reinterpret_cast<uintptr_t>(a.D) % (4 * dsize) == 0) && ((a.ldd * dsize) % (4 * dsize) == 0);
   p.d_row16 = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * dsize) % 16 == 0);
+  p.epi_tma = 0;
   p.sA = a.scale_a;
   p.ld_sa = a.ld_sa;
   p.sB = a.scale_b;
@@ -1059,10 +1297,25 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   const CUtensorMapDataType dt =
       FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
           : ((AB_FMT & 7u) == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC, tmD;
   if (!make_tensor_map_2d(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
   if (!make_tensor_map_2d(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
   GemmParams p = make_params(a, ctx);
+  // 16-bit epilogue through TMA when the rows of D (and of C, if read) start on
+  // 16-byte boundaries: 32 x 32 boxes, 128-byte rows (FP32) or 64-byte rows (16-bit)
+  memset(&tmC, 0, sizeof(tmC));
+  memset(&tmD, 0, sizeof(tmD));
+  p.epi_tma = !FP8 && p.d_row16 && (a.beta == 0.0f || p.c_vec);
+  if (p.epi_tma) {
+    const bool o32 = a.d_type == LL_OUT_F32;
+    if (!make_tensor_map_2d(&tmD, a.D, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                            o32 ? 4 : 2, a.M, a.N, a.ldd, 32, 32,
+                            o32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      return LL_ERR_CUDA;
+    if (a.beta != 0.0f &&
+        !make_tensor_map_2d(&tmC, a.C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.M, a.N, a.ldc, 32, 32))
+      return LL_ERR_CUDA;
+  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(Cfg::THREADS);
@@ -1108,7 +1361,7 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
     sc.num_units = T;
   }
   cfg.gridDim = dim3(2 * P);
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p, sc) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p, sc) != cudaSuccess) {
     cudaGetLastError();
     return LL_ERR_CUDA;
   }

@@ -51,9 +51,10 @@ ll_status launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_d
                         int cols, int esize, const LaunchCtx& ctx);
 
 // Tensor map of a row-major rows x cols matrix (pitch in elements), tiles of box_cols x
-// box_rows, 128-byte swizzle, zero fill out of bounds (gemm_tc.cu).
+// box_rows, 128-byte swizzle unless given, zero fill out of bounds (gemm_tc.cu).
 bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
-                        int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows);
+                        int64_t rows, int64_t cols, int64_t pitch, int box_cols, int box_rows,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // Bounded-wait probe (aux.cu).
 ll_status launch_timeout_probe(const LaunchCtx& ctx);

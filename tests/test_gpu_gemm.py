@@ -173,3 +173,60 @@ def test_f16_ragged_padded_lds_sampled(orc):
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     run_gemm(orc, "f16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"], lda=2064, ldb=5008,
              ldc=5008, ldd=5008, rows=_sample_rows(M, 6, 23))
+
+
+def _shifted(t, shift, fill=0.0):
+    """A flat device copy of t that starts `shift` elements into its buffer, so its base
+    address is shift * element size bytes past an aligned boundary."""
+    flat = t.reshape(-1)
+    buf = torch.full((flat.numel() + shift,), fill, dtype=flat.dtype, device=flat.device)
+    buf[shift:] = flat
+    return buf[shift:]
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 72), (1600, 1664, 136)])
+def test_misaligned_base_pointers(orc, M, N, K):
+    """A and B start 2 and 6 bytes past a 16-byte boundary (both are repacked); C and D
+    start 4 bytes past one (the transposing epilogue with scalar accesses).  The second
+    shape runs on CTA pairs."""
+    import linear_layer_gb300 as ll
+    A = wl.operand("f16", M, K, 41)
+    B = wl.operand("f16", K, N, 42)
+    C = wl.f32_normal(M, N, 43)
+    tA, tB, tC = _shifted(up(A), 1), _shifted(up(B), 3), _shifted(up(C), 1)
+    tD = _shifted(torch.empty(M * N, device="cuda"), 1, float("nan"))
+    need = ll.gemm_workspace_size(M, N, K, 1, 1, ll.IN_F16)  # the misaligned-base bound
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ll.gemm_f16(M, N, K, 0.5, tA, K, tB, N, 1.5, tC, N, tD, N, ll.OUT_F32, workspace=ws)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, "device status %s (word %#x)" % (ll.status_string(st), word)
+    ref, absab = orc.gemm("f16", M, N, K, 0.5, A.ravel(), K, B.ravel(), N, 1.5, C.ravel(), N)
+    check_close(tD.reshape(M, N).cpu().numpy(), ref, absab, K, "f32", "f16", "misaligned bases")
+
+
+@pytest.mark.parametrize("ld_pad", [0, 1])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_pair_several_units_per_cta(orc, ld_pad, out):
+    """CTA-pair problem with two whole waves plus half tiles, so each epilogue warp loads
+    the next unit's first chunk of C ahead; 16-byte row pitches of C and D (rows stored
+    per lane) and odd pitches (transposed through shared memory)."""
+    M, N, K = 4096, 2560, 64
+    ld = N + ld_pad
+    run_gemm(orc, "bf16", M, N, K, 0.75, -1.5, out, ldc=ld, ldd=ld, rows=_sample_rows(M, 10, 37))
+
+
+@pytest.mark.parametrize("ld_pad", [0, 1])
+def test_pair_in_place_c_equals_d(orc, ld_pad):
+    """D = alpha * A B + beta * D on CTA pairs, in both epilogue layouts."""
+    import linear_layer_gb300 as ll
+    M, N, K = 2048, 2304, 96
+    ld = N + ld_pad
+    A = wl.operand("bf16", M, K, 51)
+    B = wl.operand("bf16", K, N, 52)
+    C = wl.f32_normal(M, N, 53, ld=ld)
+    tC = up(C)
+    ll.gemm_bf16(M, N, K, 1.0, up(A), K, up(B), N, -0.5, tC, ld, tC, ld, ll.OUT_F32)
+    rows = _sample_rows(M, 8, 41)
+    ref, absab = orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, -0.5, C.ravel(), ld,
+                          rows=rows)
+    check_close(tC.cpu().numpy()[rows, :N], ref, absab, K, "f32", "bf16", "pair in place")
