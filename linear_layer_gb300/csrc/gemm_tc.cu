@@ -190,9 +190,79 @@ __device__ __forceinline__ void store_row(const GemmParams& p, int m, int n, con
   }
 }
 
+// a[j] = alpha * a[j] (+ beta * C[m][n + j]) for one 32-column chunk of row m (< M),
+// C consumed four columns at a time as it arrives.
+__device__ __forceinline__ void combine_c_row(const GemmParams& p, int m, int n, float (&a)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) a[j] *= p.alpha;
+  if (p.beta == 0.0f) return;
+  const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
+  if (n + 32 <= p.N && p.c_vec) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 cv = *reinterpret_cast<const float4*>(crow + j);
+      a[j] = fmaf(p.beta, cv.x, a[j]);
+      a[j + 1] = fmaf(p.beta, cv.y, a[j + 1]);
+      a[j + 2] = fmaf(p.beta, cv.z, a[j + 2]);
+      a[j + 3] = fmaf(p.beta, cv.w, a[j + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < p.N) a[j] = fmaf(p.beta, crow[j], a[j]);
+  }
+}
+
+// Store final values (alpha and beta applied) of one chunk of row m, masked to N.
+__device__ __forceinline__ void store_row_final(const GemmParams& p, int m, int n, const float (&o)[32]) {
+  const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
+  const bool full = n + 32 <= p.N;
+  if (p.d_type == LL_OUT_F32) {
+    float* dp = static_cast<float*>(p.D) + off;
+    if (full && p.d_row16) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n + j < p.N) dp[j] = o[j];
+    }
+  } else {
+    const bool bf = p.d_type == LL_OUT_BF16;
+    uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n + j < p.N)
+        dp[j] = bf ? __bfloat16_as_ushort(__float2bfloat16_rn(o[j])) : __half_as_ushort(__float2half_rn(o[j]));
+  }
+}
+
+// One 32 x 32 chunk of 16-bit D into a 2 KB staging buffer in the layout of a TMA box
+// of 64-byte rows with 64-byte swizzle: 16-byte slot j of row l (= lane) at
+// j ^ ((l >> 1) & 3).  The buffer must be 512-byte aligned.
+__device__ __forceinline__ void stage_row16(uint8_t* buf, int lane, const float (&o)[32], bool bf) {
+  uint4* drow = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = o[8 * j + 2 * i], hi = o[8 * j + 2 * i + 1];
+      if (bf) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+        w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+      } else {
+        __half2 h2 = __floats2half2_rn(lo, hi);
+        w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+    }
+    drow[j ^ ((lane >> 1) & 3)] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+}
+
 // Up to CH consecutive chunks of one row (lane = row m), read straight from the FP32
-// accumulator registers (the FP8 promotion epilogue, which holds CH = 4 chunks): C is
-// consumed four columns at a time as it arrives, which keeps register pressure down.
+// accumulator registers (the FP8 promotion epilogue, which holds CH = 4 chunks).
 template <int CH>
 __device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0,
                                               float (&acc)[CH][32]) {
@@ -201,31 +271,28 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0
   for (int c = 0; c < CH; ++c) {
     const int n = n0 + 32 * c;
     if (n >= p.N) break;
-    const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
+    combine_c_row(p, m, n, acc[c]);
+    if (p.d_type != LL_OUT_F32 && n + 32 <= p.N && p.d_row16) {  // 16-byte vector stores
+      uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
+      const bool bf = p.d_type == LL_OUT_BF16;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) acc[c][j] *= p.alpha;
-    if (p.beta != 0.0f) {
-      if (n + 32 <= p.N && p.c_vec) {
+      for (int j = 0; j < 32; j += 8) {
+        uint32_t w4[4];
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 cv = *reinterpret_cast<const float4*>(crow + j);
-          acc[c][j] = fmaf(p.beta, cv.x, acc[c][j]);
-          acc[c][j + 1] = fmaf(p.beta, cv.y, acc[c][j + 1]);
-          acc[c][j + 2] = fmaf(p.beta, cv.z, acc[c][j + 2]);
-          acc[c][j + 3] = fmaf(p.beta, cv.w, acc[c][j + 3]);
+        for (int i = 0; i < 4; ++i) {
+          if (bf) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[c][j + 2 * i], acc[c][j + 2 * i + 1]);
+            w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+          } else {
+            __half2 h2 = __floats2half2_rn(acc[c][j + 2 * i], acc[c][j + 2 * i + 1]);
+            w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
         }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n + j < p.N) acc[c][j] = fmaf(p.beta, crow[j], acc[c][j]);
+        *reinterpret_cast<uint4*>(dp + j) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
+    } else {
+      store_row_final(p, m, n, acc[c]);
     }
-    const float zero[32] = {};
-    // alpha and beta are applied: store_row with alpha = 1, beta = 0 only casts
-    GemmParams q = p;
-    q.alpha = 1.0f;
-    q.beta = 0.0f;
-    store_row(q, m, n, acc[c], zero);
   }
 }
 
@@ -1010,24 +1077,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               for (int j = 0; j < 8; ++j)
                 drow[j ^ (lane & 7)] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
             } else {
-              // 64-byte rows, 64-byte swizzle: 16-byte slot j of row l at j ^ ((l >> 1) & 3)
-              uint4* drow = reinterpret_cast<uint4*>(ebuf + b * Cfg::EPI_BUF_BYTES + lane * 64);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float lo = o[8 * j + 2 * i], hi = o[8 * j + 2 * i + 1];
-                  if (bf) {
-                    __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-                    w4[i] = *reinterpret_cast<uint32_t*>(&h2);
-                  } else {
-                    __half2 h2 = __floats2half2_rn(lo, hi);
-                    w4[i] = *reinterpret_cast<uint32_t*>(&h2);
-                  }
-                }
-                drow[j ^ ((lane >> 1) & 3)] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-              }
+              stage_row16(ebuf + b * Cfg::EPI_BUF_BYTES, lane, o, bf);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1035,18 +1085,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           } else if (n < p.N && m_w + lane < p.M) {
             // the chunk that crosses column N: a TMA store may write whole 16-byte units
             // past N, so each lane stores its row's valid columns itself
-            const int64_t off = static_cast<int64_t>(m_w + lane) * p.ldd + n;
-            if (out32) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (n + j < p.N) static_cast<float*>(p.D)[off + j] = o[j];
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (n + j < p.N)
-                  reinterpret_cast<uint16_t*>(p.D)[off + j] =
-                      bf ? __bfloat16_as_ushort(__float2bfloat16_rn(o[j])) : __half_as_ushort(__float2half_rn(o[j]));
-            }
+            store_row_final(p, m_w + lane, n, o);
           }
           if (lane == 0) bulk_commit_group();  // one group per chunk (empty without a store)
         }
@@ -1305,9 +1344,9 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   // 16-byte boundaries: 32 x 32 boxes, 128-byte rows (FP32) or 64-byte rows (16-bit)
   memset(&tmC, 0, sizeof(tmC));
   memset(&tmD, 0, sizeof(tmD));
+  const bool o32 = a.d_type == LL_OUT_F32;
   p.epi_tma = !FP8 && p.d_row16 && (a.beta == 0.0f || p.c_vec);
   if (p.epi_tma) {
-    const bool o32 = a.d_type == LL_OUT_F32;
     if (!make_tensor_map_2d(&tmD, a.D, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
                             o32 ? 4 : 2, a.M, a.N, a.ldd, 32, 32,
                             o32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
