@@ -651,16 +651,22 @@ def bench_ragged(args, dev, stream, peaks, peak_src):
     for i in range(3):
         call(i)
     torch.cuda.synchronize(dev)
-    steps = max(5, min(args.steps // 10, 100))
-    total_ms, _ = time_events(call, steps, stream, per_call=False)  # back to back
-    launch_ms = [total_ms / steps]
+    # median of 5 groups of back-to-back calls (one slow group does not set the figure)
+    steps = max(5, min(args.steps // 50, 20))
+    group_ms = []
+    for _ in range(5):
+        total_ms, _ = time_events(call, steps, stream, per_call=False)
+        group_ms.append(total_ms / steps)
+    ms = statistics.median(group_ms)
     st, _ = ll.get_device_status(stream)
     flops = gemm_flops(M, N, K)
-    tflops = flops / (statistics.mean(launch_ms) / 1e3) / 1e12
+    tflops = flops / (ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"metric": "ragged FP16 GEMM TFLOPS (B repack of the 10006-byte pitch included)",
             "value": round(tflops, 1), "unit": "TFLOPS",
-            "ms_per_call": round(statistics.mean(launch_ms), 4),
+            "ms_per_call": round(ms, 4),
+            "ms_per_call_min_max": [round(min(group_ms), 4), round(max(group_ms), 4)],
+            "timing": "median of 5 groups of %d back-to-back calls" % steps,
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
                          "peak_source": peak_src + " bf16_tflops (FP16 = BF16 rate)"},
