@@ -230,3 +230,31 @@ def test_pair_in_place_c_equals_d(orc, ld_pad):
     ref, absab = orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, -0.5, C.ravel(), ld,
                           rows=rows)
     check_close(tC.cpu().numpy()[rows, :N], ref, absab, K, "f32", "bf16", "pair in place")
+
+
+@pytest.mark.parametrize("ld_pad", [0, 8, 3])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_pair_writes_nothing_outside_d(orc, ld_pad, out):
+    """M and N tails that end inside a 32-row / 32-column chunk, on CTA pairs: the rows
+    after D's last row and the padding columns of every row stay untouched, with the
+    TMA epilogue (16-byte row pitches: ld_pad 0 and 8) and the transposing one (odd
+    pitch)."""
+    import linear_layer_gb300 as ll
+    M, N, K = 2000, 2264, 80
+    ldd = N + ld_pad if out == "f32" else N + 2 * ld_pad
+    A = wl.operand("bf16", M, K, 61)
+    B = wl.operand("bf16", K, N, 62)
+    C = wl.f32_normal(M, N, 63, ld=ldd)
+    guard = 40  # rows past M in the same allocation
+    tD = out_tensor(M + guard, ldd, out)
+    ll.gemm_bf16(M, N, K, 1.0, up(A), K, up(B), N, 0.5, up(C), ldd, tD, ldd, out_code(out))
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, "device status %s (word %#x)" % (ll.status_string(st), word)
+    D = tD.float().cpu().numpy()
+    assert np.isnan(D[M:]).all(), "rows past M were written"
+    if ldd > N:
+        assert np.isnan(D[:M, N:]).all(), "padding columns were written"
+    rows = _sample_rows(M, 6, 43)
+    ref, absab = orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, 0.5, C.ravel(), ldd,
+                          rows=rows)
+    check_close(D[rows, :N].astype(np.float64), ref, absab, K, out, "bf16", "guarded D")
