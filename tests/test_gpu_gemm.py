@@ -205,7 +205,7 @@ def test_misaligned_base_pointers(orc, M, N, K):
 
 
 @pytest.mark.parametrize("ld_pad", [0, 1])
-@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
 def test_pair_several_units_per_cta(orc, ld_pad, out):
     """CTA-pair problem with two whole waves plus half tiles, so each epilogue warp loads
     the next unit's first chunk of C ahead; 16-byte row pitches of C and D (rows stored
@@ -258,3 +258,11 @@ def test_pair_writes_nothing_outside_d(orc, ld_pad, out):
     ref, absab = orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, 0.5, C.ravel(), ldd,
                           rows=rows)
     check_close(D[rows, :N].astype(np.float64), ref, absab, K, out, "bf16", "guarded D")
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
+def test_pair_beta_zero_every_output(orc, out):
+    """beta = 0 on CTA pairs (C is not read; the TMA epilogue only stages D), FP16
+    inputs, several units per pair with half tiles, an M tail inside a chunk."""
+    M, N, K = 4000, 2560, 96
+    run_gemm(orc, "f16", M, N, K, -1.25, 0.0, out, rows=_sample_rows(M, 8, 47))
