@@ -631,6 +631,57 @@ def bench_fp8(args, dev, stream, peaks, peak_src):
             "status": ll.status_string(st)}
 
 
+def bench_small(args, dev, stream, peaks, peak_src):
+    """FP16 256^3 with an FP32 output: launch-bound, so timed as a CUDA graph of 200
+    launches; the roofline fraction is informational."""
+    import torch
+
+    import linear_layer_gb300 as ll
+    import workloads as wl
+    cfg = wl.WORKLOADS["f16_gemm_256"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    A, B, _ = wl.gemm_inputs("f16", M, N, K, cfg["beta"])
+    tA, tB = _up(A, dev), _up(B, dev)
+    tD = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+    def call(i):
+        ll.gemm_f16(M, N, K, cfg["alpha"], tA, K, tB, N, cfg["beta"], None, N, tD, N, ll.OUT_F32,
+                    stream=stream)
+
+    for i in range(5):
+        call(i)
+    torch.cuda.synchronize(dev)
+    per_graph = 200
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(per_graph):
+                call(i)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    reps = 10
+
+    def replay(_):
+        with torch.cuda.stream(stream):
+            g.replay()
+
+    total_ms, _ = time_events(replay, reps, stream)
+    launch_s = total_ms / 1e3 / (reps * per_graph)
+    tflops = gemm_flops(M, N, K) / launch_s / 1e12
+    peak = peaks["bf16_tflops"]
+    st, _ = ll.get_device_status(stream)
+    return {"metric": "FP16 GEMM 256^3 (launch-bound) time per launch", "value": round(launch_s * 1e6, 3),
+            "unit": "us", "higher_is_better": False, "tflops": round(tflops, 2),
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 5), "traffic": None,
+                         "kernel": "gemm_tc_kernel (one CTA per 128-row tile)",
+                         "peak_source": peak_src + " bf16_tflops (FP16 = BF16 rate); informational"},
+            "timing": "CUDA graph of %d launches, %d replays; inputs (256 KB) stay in L2" % (per_graph, reps),
+            "status": ll.status_string(st)}
+
+
 def bench_ragged(args, dev, stream, peaks, peak_src):
     import torch
 
@@ -752,7 +803,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the GEMV / FP8 / ragged lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged", "tokens", "w8a16"],
+    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged", "tokens", "w8a16",
+                                           "small"],
                     default="all",
                     help="all = the contract line; otherwise time one other kernel and print its object")
     args = ap.parse_args(argv)
@@ -771,7 +823,8 @@ def main(argv=None):
     stream = torch.cuda.Stream(device=dev)
 
     single = {"gemv": bench_gemv, "gemv_fused": bench_gemv_fused, "fp8": bench_fp8,
-              "ragged": bench_ragged, "tokens": bench_w8a8_tokens, "w8a16": bench_w8a16}.get(args.workload)
+              "ragged": bench_ragged, "tokens": bench_w8a8_tokens, "w8a16": bench_w8a16,
+              "small": bench_small}.get(args.workload)
     if single is not None:
         res = single(args, dev, stream, peaks, peak_src)
         if rank == 0:
@@ -788,6 +841,7 @@ def main(argv=None):
         extra["w8a16_linear_tokens_4096x11008"] = bench_w8a16(args, dev, stream, peaks, peak_src)
         extra["e4m3_gemm_8192"] = bench_fp8(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_4093x5003x2056"] = bench_ragged(args, dev, stream, peaks, peak_src)
+        extra["f16_gemm_256"] = bench_small(args, dev, stream, peaks, peak_src)
     barrier(dev)
     if rank != 0:
         return 0
