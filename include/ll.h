@@ -76,8 +76,10 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
  *
  *   A : M x K, lda >= K (FP16 or BF16)          B : K x N, ldb >= N (same type as A)
  *   C : M x N FP32, ldc >= N; not read when beta == 0 (may then be NULL)
- *   D : M x N, ldd >= N, element type d_type; D may alias C only when
- *       d_type == LL_OUT_F32 and ldd == ldc (each element is read before it is written)
+ *   D : M x N, ldd >= N, element type d_type; D may alias C only as the same matrix
+ *       (D == C, d_type == LL_OUT_F32, ldd == ldc: each element is read before it is
+ *       written); any other overlap of D with A, B or C gives undefined results.
+ *       Nothing outside the M x N elements of D is written (padding columns included).
  *   workspace : device scratch of ws_bytes (see ll_gemm_workspace_size); may be NULL if 0.
  * Every product is accumulated in FP32 over the whole K; alpha * acc + beta * C is
  * evaluated in FP32 and rounded once to d_type (round to nearest even).
