@@ -128,9 +128,9 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
  * counterpart: this entry point exists for integration, not for the method.
  *
  * Some callers cannot provide the workspace ll_gemm_f16 needs for an operand whose
- * row pitch or base address is not a multiple of 16 bytes: code that runs while a
- * stream is being captured into a CUDA graph (cudaMalloc is not allowed there), code
- * in a host callback, or a runtime whose allocator owns all device memory.  This
+ * row pitch or base address is not a multiple of 16 bytes: code in a host callback
+ * (which may not call CUDA's allocator), a runtime whose allocator owns all device
+ * memory and hands none to libraries, or a path that must not allocate at all.  This
  * variant takes the same arguments minus the workspace and repacks such operands
  * into a fixed scratch array inside the library: 16 MiB of device memory that every
  * GPU which loads the library holds until the process exits.  It calls no cudaMalloc,
@@ -144,8 +144,8 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
  *     (once per device, with that device current); make that first call before any
  *     stream capture.
  *   - Every call shares the one scratch array and overwrites what it reads, so calls
- *     that overlap on the GPU (different streams, concurrent graph replays) race:
- *     serialise them.
+ *     that overlap on the GPU (for instance on different streams) race: serialise
+ *     them.
  * Results equal those of ll_gemm_f16 with workspace; errors as for ll_gemm_f16.
  */
 ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const void* A, int64_t lda,

@@ -1,5 +1,5 @@
 """ll_gemm_f16_noalloc, the FP16 GEMM for callers that cannot allocate device memory
-(code running under CUDA-graph stream capture, host callbacks, or runtimes whose
+(code in host callbacks, which may not call CUDA's allocator, or runtimes whose
 allocator owns all device memory), checked against ll_gemm_f16 with a caller-provided
 workspace.
 
