@@ -128,9 +128,10 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
  * counterpart: this entry point exists for integration, not for the method.
  *
  * Some callers cannot provide the workspace ll_gemm_f16 needs for an operand whose
- * row pitch or base address is not a multiple of 16 bytes: code in a host callback
- * (which may not call CUDA's allocator), a runtime whose allocator owns all device
- * memory and hands none to libraries, or a path that must not allocate at all.  This
+ * row pitch or base address is not a multiple of 16 bytes: a runtime whose allocator
+ * owns all device memory and hands none to libraries, a plugin interface that passes
+ * the library neither an allocator nor a workspace, or a latency-critical path where
+ * allocating is not allowed.  This
  * variant takes the same arguments minus the workspace and repacks such operands
  * into a fixed scratch array inside the library: 16 MiB of device memory that every
  * GPU which loads the library holds until the process exits.  It calls no cudaMalloc,

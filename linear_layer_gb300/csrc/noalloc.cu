@@ -3,9 +3,9 @@
 // ll_gemm_f16 needs caller-provided workspace when an operand's row pitch (or base
 // address) is not a multiple of 16 bytes, because such an operand is first repacked
 // into a 16-byte pitch that the TMA tensor maps can describe.  Some callers have no
-// way to provide it: code inside a host callback (which may not call CUDA's
-// allocator), a runtime whose allocator owns all device memory and gives none to a
-// library per call, or a path that must not allocate at all.  This
+// way to provide it: a runtime whose allocator owns all device memory and gives none
+// to a library per call, a plugin interface that passes neither an allocator nor a
+// workspace, or a latency-critical path where allocating is not allowed.  This
 // variant repacks into a fixed scratch array that lives in the library itself:
 // kNoAllocScratchBytes (16 MiB) of device memory, held on every GPU that loads the
 // library until the process exits.  It calls no cudaMalloc / cudaFree and no

@@ -1,7 +1,7 @@
 """ll_gemm_f16_noalloc, the FP16 GEMM for callers that cannot allocate device memory
-(code in host callbacks, which may not call CUDA's allocator, or runtimes whose
-allocator owns all device memory), checked against ll_gemm_f16 with a caller-provided
-workspace.
+(runtimes whose allocator owns all device memory, plugin interfaces that pass
+neither an allocator nor a workspace, latency-critical paths where allocating is not
+allowed), checked against ll_gemm_f16 with a caller-provided workspace.
 
 The new entry point repacks operands whose row pitch is not a multiple of 16 bytes
 into a fixed 16 MiB scratch array inside the library instead of the caller's
