@@ -39,7 +39,7 @@ typedef struct CUstream_st* ll_stream_t;
 typedef enum {
   LL_OK = 0,
   LL_ERR_INVALID_ARG = 1,    /* a size, leading dimension or pointer is invalid       */
-  LL_ERR_MISALIGNED = 2,     /* reserved: misaligned operands are repacked instead    */
+  LL_ERR_MISALIGNED = 2,     /* C, D or a scale pointer not aligned to its element   */
   LL_ERR_UNSUPPORTED = 3,    /* a valid request this build does not implement         */
   LL_ERR_WORKSPACE = 4,      /* workspace too small for the operand repack it needs   */
   LL_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed         */
@@ -85,8 +85,9 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
  * evaluated in FP32 and rounded once to d_type (round to nearest even).
  * M == 0 or N == 0: nothing is done.  K == 0: D = beta * C (alpha is not used).
  * Errors: LL_ERR_INVALID_ARG for negative sizes, ld < width, NULL operands, or
- * beta != 0 with C == NULL; LL_ERR_WORKSPACE if a repack is needed and ws_bytes is
- * smaller than ll_gemm_workspace_size; LL_ERR_CUDA if a launch fails.
+ * beta != 0 with C == NULL; LL_ERR_MISALIGNED if D (or C when read) is not aligned to
+ * its element size; LL_ERR_WORKSPACE if a repack is needed and ws_bytes is smaller
+ * than ll_gemm_workspace_size; LL_ERR_CUDA if a launch fails.
  */
 ll_status ll_gemm_f16(int M, int N, int K, float alpha, const void* A, int64_t lda,
                       const void* B, int64_t ldb, float beta, const float* C, int64_t ldc,

@@ -83,6 +83,14 @@ ll_status gemm_common(ll::GemmArgs a, void* workspace, size_t ws_bytes, ll_strea
     return LL_ERR_INVALID_ARG;  // in place only for FP32 output
   if (a.beta != 0.0f && static_cast<const void*>(a.C) == a.D && a.ldc != a.ldd)
     return LL_ERR_INVALID_ARG;
+  // C, D and the scales are read and written element by element: each must be aligned
+  // to its element size (A and B are repacked from any address)
+  const uintptr_t dsz = a.d_type == LL_OUT_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(a.D) % dsz != 0) return LL_ERR_MISALIGNED;
+  if (a.beta != 0.0f && reinterpret_cast<uintptr_t>(a.C) % 4 != 0) return LL_ERR_MISALIGNED;
+  if ((a.scale_a && reinterpret_cast<uintptr_t>(a.scale_a) % 4 != 0) ||
+      (a.scale_b && reinterpret_cast<uintptr_t>(a.scale_b) % 4 != 0))
+    return LL_ERR_MISALIGNED;
   if (a.K > 0) {
     if (a.A == nullptr || a.B == nullptr || a.lda < a.K || a.ldb < a.N) return LL_ERR_INVALID_ARG;
     if (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) {

@@ -72,6 +72,8 @@ extern "C" ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const
   if (beta != 0.0f && static_cast<const void*>(C) == D && (d_type != LL_OUT_F32 || ldc != ldd))
     return LL_ERR_INVALID_ARG;
   if (K > 0 && (A == nullptr || B == nullptr || lda < K || ldb < N)) return LL_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(D) % (d_type == LL_OUT_F32 ? 4 : 2) != 0) return LL_ERR_MISALIGNED;
+  if (beta != 0.0f && reinterpret_cast<uintptr_t>(C) % 4 != 0) return LL_ERR_MISALIGNED;
 
   ll::GemmArgs a;
   a.in_type = LL_IN_F16;

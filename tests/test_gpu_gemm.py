@@ -266,3 +266,19 @@ def test_pair_beta_zero_every_output(orc, out):
     inputs, several units per pair with half tiles, an M tail inside a chunk."""
     M, N, K = 4000, 2560, 96
     run_gemm(orc, "f16", M, N, K, -1.25, 0.0, out, rows=_sample_rows(M, 8, 47))
+
+
+def test_c_d_must_be_element_aligned():
+    """D (or C when read) off its element alignment is rejected before any launch."""
+    import linear_layer_gb300 as ll
+    A = torch.zeros(64 * 64, dtype=torch.float16, device="cuda")
+    raw = torch.zeros(64 * 64 * 4 + 4, dtype=torch.uint8, device="cuda")
+    bad = raw[1:]  # one byte past a 4-byte boundary
+    good = torch.zeros(64 * 64, dtype=torch.float32, device="cuda")
+    for C, D, beta in [(None, bad, 0.0), (bad, good, 1.0)]:
+        with pytest.raises(ll.LLError) as e:
+            ll.gemm_f16(64, 64, 64, 1.0, A, 64, A, 64, beta, C, 64, D, 64, ll.OUT_F32)
+        assert e.value.status == ll.LL_ERR_MISALIGNED
+    with pytest.raises(ll.LLError) as e:
+        ll.gemm_f16_noalloc(64, 64, 64, 1.0, A, 64, A, 64, 0.0, None, 64, bad, 64, ll.OUT_F32)
+    assert e.value.status == ll.LL_ERR_MISALIGNED
