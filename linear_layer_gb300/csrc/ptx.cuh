@@ -156,6 +156,12 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int32_t 
                : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) from a 16-byte-aligned global address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared; completes `bytes` of tx on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y) {
