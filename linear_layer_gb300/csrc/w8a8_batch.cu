@@ -25,6 +25,9 @@
 //     dequantises its totals and stores y token-major (coalesced along o).
 //   * programmatic dependent launch as in the batch-1 GEMV: weights stream before
 //     griddepcontrol.wait; X, the scales and the outputs are touched only after it.
+//     Before the wait each warp also bulk-prefetches the D steps after its first D into
+//     L2 (measured on the 11008 x 4096 layer: 2 tokens 9.55 -> 8.18 us, 4 tokens
+//     10.08 -> 8.53 us, 8 tokens 12.91 -> 12.21 us).
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -128,6 +131,28 @@ __global__ void __launch_bounds__(kBtThreads, CTAS) w8a8_batch_kernel(const Batc
   int4 w[D][R][U];
 #pragma unroll
   for (int j = 0; j < D; ++j) load_next(w[j]);
+  // the D steps after those go to L2 (one bulk prefetch per row and step) while the
+  // tokens are staged
+  if (lane == 0) {
+    int ql = pl, qg = gl, qk = kl;
+    for (int j = 0; j < D; ++j) {
+      const int n = min(U, min(Lc - qk, ce - ql));
+      if (n <= 0) break;
+      const int kbytes = min(n * 512, p.K - qk * 512);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = (g0 + qg) * R + r;
+        if (row < p.N && kbytes > 0)
+          bulk_prefetch_l2(p.W + static_cast<int64_t>(row) * p.ldw + qk * 512, static_cast<uint32_t>(kbytes));
+      }
+      ql += n;
+      qk += n;
+      if (qk == Lc) {
+        qk = 0;
+        ++qg;
+      }
+    }
+  }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < MT * nch; i += kBtThreads) {
