@@ -18,7 +18,10 @@
 //     reduced partial sums into its own shared-memory slot and the epilogue adds the 8
 //     slots in a fixed order, so results do not depend on timing.
 // Programmatic dependent launch: weights stream before griddepcontrol.wait, activations,
-// scales and outputs are touched only after it.
+// scales and outputs are touched only after it.  Before the wait each warp of the
+// several-token kernel also bulk-prefetches its next D steps into L2 (measured on the
+// 11008 x 4096 layer: 2 tokens 14.19 -> 13.01 us, 4 tokens 18.74 -> 17.60 us; the same
+// for the single-token row kernel changed nothing, it is bound by its instruction stream).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -138,6 +141,28 @@ __global__ void __launch_bounds__(kWoThreads, CTAS) w8a16_kernel(const WoParams 
   int4 w[D][R][U];
 #pragma unroll
   for (int j = 0; j < D; ++j) load_next(w[j]);
+  // the D steps after those go to L2 (one bulk prefetch per row and step) while the
+  // activations are staged
+  if (lane == 0) {
+    int ql = pl, qg = gl, qk = kl;
+    for (int j = 0; j < D; ++j) {
+      const int n = min(U, min(Lc - qk, ce - ql));
+      if (n <= 0) break;
+      const int kbytes = min(n * 512, p.K - qk * 512);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = (g0 + qg) * R + r;
+        if (row < p.N && kbytes > 0)
+          bulk_prefetch_l2(p.W + static_cast<int64_t>(row) * p.ldw + qk * 512, static_cast<uint32_t>(kbytes));
+      }
+      ql += n;
+      qk += n;
+      if (qk == Lc) {
+        qk = 0;
+        ++qg;
+      }
+    }
+  }
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int xp = p.K >> 3;  // 16-byte pieces (8 BF16) per token
