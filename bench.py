@@ -50,7 +50,7 @@ def gemv_bytes(N, K):
 
 KERNEL_SOURCES = {
     "gemm_tc2_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/ptx.cuh"],
-    "gemv_w8a8_kernel": ["linear_layer_gb300/csrc/gemv_w8a8.cu"],
+    "gemv_w8a8_kernel": ["linear_layer_gb300/csrc/gemv_w8a8.cu", "linear_layer_gb300/csrc/ptx.cuh"],
 }
 
 
