@@ -91,3 +91,53 @@ def test_random_fp8(orc, seed):
     check_close(tD.float().cpu().numpy().astype(np.float64)[rows], ref, absab, K, out, "e4m3",
                 what="seed %d %s x %s %dx%dx%d lda %d ldb %d a %g b %g %s" % (
                     seed, a_fmt, b_fmt, M, N, K, lda, ldb, alpha, beta, out))
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_pair_epilogues(orc, seed):
+    """CTA-pair sizes with random C / D pitches (16-byte rows take the TMA epilogue, odd
+    ones the transposing one), M and N tails inside a chunk, beta 0 or not, every output
+    type, and in place (D == C) for some FP32 cases.  Rows past M and padding columns of
+    D must stay untouched."""
+    import linear_layer_gb300 as ll
+    rng = np.random.default_rng(7000 + seed)
+    M = int(rng.integers(1600, 4200))
+    N = int(rng.integers(1600, 4200))
+    K = int(rng.integers(16, 600))
+    kind = "f16" if seed % 2 == 0 else "bf16"
+    pad_a = int(rng.choice([0, 8, 3]))
+    pad_b = int(rng.choice([0, 8, 5]))
+    pad_cd = int(rng.choice([0, 0, 4, 8, 1, 3]))
+    alpha = float(rng.choice([1.0, 0.5, -2.0]))
+    beta = float(rng.choice([0.0, 1.0, -0.75]))
+    out = OUTS[int(rng.integers(0, 3))]
+    in_place = out == "f32" and beta != 0.0 and seed % 3 == 0
+    lda, ldb, ldcd = K + pad_a, N + pad_b, N + pad_cd
+    A = wl.operand(kind, M, K, 800 + seed, ld=lda)
+    B = wl.operand(kind, K, N, 900 + seed, ld=ldb)
+    C = wl.f32_normal(M, N, 1000 + seed, ld=ldcd) if beta != 0.0 else None
+    guard = 8
+    in_type = ll.IN_F16 if kind == "f16" else ll.IN_BF16
+    need = ll.gemm_workspace_size(M, N, K, lda, ldb, in_type)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+    fn = ll.gemm_f16 if kind == "f16" else ll.gemm_bf16
+    if in_place:
+        tC = torch.full((M + guard, ldcd), float("nan"), device="cuda")
+        tC[:M] = up(C)
+        fn(M, N, K, alpha, up(A), lda, up(B), ldb, beta, tC, ldcd, tC, ldcd, ll.OUT_F32, workspace=ws)
+        tD = tC
+    else:
+        tD = out_tensor(M + guard, ldcd, out)
+        fn(M, N, K, alpha, up(A), lda, up(B), ldb, beta, up(C), ldcd, tD, ldcd, out_code(out), workspace=ws)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, word
+    D = tD.float().cpu().numpy()
+    assert np.isnan(D[M:]).all(), "rows past M were written"
+    if ldcd > N:  # (in place: C's padding is NaN too)
+        assert np.isnan(D[:M, N:]).all(), "padding columns were written"
+    rows = _rows(rng, M)
+    ref, absab = orc.gemm(kind, M, N, K, alpha, A.ravel(), lda, B.ravel(), ldb, beta,
+                          None if C is None else C.ravel(), ldcd, rows=rows)
+    check_close(D[rows, :N].astype(np.float64), ref, absab, K, out, kind,
+                what="seed %d %s %dx%dx%d lda %d ldb %d ldcd %d a %g b %g %s%s" % (
+                    seed, kind, M, N, K, lda, ldb, ldcd, alpha, beta, out, " in place" if in_place else ""))
