@@ -298,7 +298,7 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_mm = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
-    e2e_steps = max(3, min(args.steps, 30))
+    e2e_steps = max(3, min(args.steps, 100))  # enough steps that pipeline fill and drain stay small
 
     def run_e2e(nsteps, t0=None, t1=None):
         if t0 is not None:

@@ -1387,12 +1387,17 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   sc.num_m2 = (a.M + 255) / 256;
   sc.num_n = (a.N + Cfg::BN - 1) / Cfg::BN;
   const int T = sc.num_m2 * sc.num_n;
-  const int P = T < max_pairs[dev] ? T : max_pairs[dev];
+  int P = T < max_pairs[dev] ? T : max_pairs[dev];
   const int waves = T / P, rem = T - waves * P;
-  // 16-bit: finish with one half-wave of 256 x 128 halves when that is shorter.
+  // 16-bit: finish with one half-wave of 256 x 128 halves when that is shorter; a
+  // problem whose halves all fit one wave runs as halves only (twice the pairs at work).
   // (FP8 halves would give each CTA 64 one-byte columns, narrower than a 128-byte
   // swizzle row, so FP8 keeps whole tiles.)
-  if (!FP8 && rem > 0 && 2 * rem <= P) {
+  if (!FP8 && 2 * T <= max_pairs[dev]) {
+    sc.full_units = 0;
+    sc.num_units = 2 * T;
+    P = 2 * T;
+  } else if (!FP8 && rem > 0 && 2 * rem <= P) {
     sc.full_units = waves * P;
     sc.num_units = sc.full_units + 2 * rem;
   } else {
@@ -1415,9 +1420,16 @@ static ll_status run_fp8(const GemmArgs& a, const LaunchCtx& ctx, bool pair) {
 }
 
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
-  const int tiles_m = (a.M + 127) / 128;
-  auto tiles = [&](int bn) { return tiles_m * ((a.N + bn - 1) / bn); };
-  const bool pair = ((a.M + 255) / 256) * ((a.N + 255) / 256) >= ctx.num_sms / 4;
+  // CTA pairs from SMs/4 pair tiles on (16-bit: from SMs/8 when M and N both exceed
+  // 128, the problems with at most half a wave of tiles then running as 256 x 128
+  // halves; measured on GB300: 1280^3 267 -> 347 TFLOPS, 1536^3 402 -> 537,
+  // 1536 x 1536 x 4096 494 -> 780, 256 x 8192 x 4096 425 -> 687, while 1024^3 (16 pair
+  // tiles) and M or N of 128 stay faster on the one-CTA kernel)
+  const int pair_tiles = ((a.M + 255) / 256) * ((a.N + 255) / 256);
+  const bool f8 = a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2;
+  const bool pair = f8 ? pair_tiles >= ctx.num_sms / 4
+                       : (pair_tiles >= ctx.num_sms / 4 ||
+                          (pair_tiles >= ctx.num_sms / 8 && a.M > 128 && a.N > 128));
   if (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) {
     const bool a5 = a.in_type == LL_IN_E5M2, b5 = a.b_type == LL_IN_E5M2;
     if (!a5 && !b5) return run_fp8<fmt_pair(0, 0)>(a, ctx, pair);
@@ -1429,13 +1441,8 @@ ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
   const bool bf = a.in_type == LL_IN_BF16;
   // large problems: CTA pairs with 256 x 256 tiles
   if (pair) return bf ? run_pair<false, BF16>(a, ctx) : run_pair<false, F16>(a, ctx);
-  int bn = 64;
-  if (tiles(256) >= ctx.num_sms)
-    bn = 256;
-  else if (tiles(128) >= ctx.num_sms)
-    bn = 128;
-  if (bn == 256) return bf ? run<TileCfg<256, false>, BF16>(a, ctx) : run<TileCfg<256, false>, F16>(a, ctx);
-  if (bn == 128) return bf ? run<TileCfg<128, false>, BF16>(a, ctx) : run<TileCfg<128, false>, F16>(a, ctx);
+  // the rest has fewer tiles than SMs even at 128 x 64 (a wider one-CTA tile would only
+  // be picked with a full wave of it, and such problems run on CTA pairs)
   return bf ? run<TileCfg<64, false>, BF16>(a, ctx) : run<TileCfg<64, false>, F16>(a, ctx);
 }
 

@@ -71,10 +71,11 @@ def test_odd_shapes(orc, M, N, K):
     run_gemm(orc, "bf16", M, N, K, 1.0, 1.0, "f32")
 
 
-def test_many_tiles_every_bn(orc):
-    # shapes that pick the 64-, 128- and 256-wide tile variants
-    for (M, N) in [(256, 256), (2048, 1280), (4096, 2304)]:
-        run_gemm(orc, "f16", M, N, 128, 1.0, 0.0, "f32", rows=[0, 127, 128, M - 1])
+def test_many_tiles_every_path(orc):
+    # one-CTA 128 x 64 tiles, CTA-pair halves only (at most half a wave of pair tiles),
+    # whole pair tiles, and an M of 128 (one-CTA kernel although it has 24 pair tiles)
+    for (M, N) in [(256, 256), (1280, 1280), (2048, 1280), (4096, 2304), (128, 6144)]:
+        run_gemm(orc, "f16", M, N, 128, 1.0, 0.0, "f32", rows=sorted({0, 127, min(128, M - 1), M - 1}))
 
 
 def test_padded_leading_dims(orc):
