@@ -660,9 +660,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
 // ------------------------------------------------------------------ CTA-pair kernel
 //
-// Large problems run on CTA pairs (2-CTA clusters).  A pair owns a 256 x 256 output
-// tile: each CTA loads its 128 rows of A and its half (128 columns) of B into its own
-// shared memory, the even CTA's single MMA thread issues tcgen05.mma with
+// Large 16-bit problems run on CTA pairs (2-CTA clusters).  A pair owns a 256 x 256
+// output tile: each CTA loads its 128 rows of A and its half (128 columns) of B into its
+// own shared memory, the even CTA's single MMA thread issues tcgen05.mma with
 // cta_group::2 (M = 256), and each CTA's TMEM receives its own 128 rows of the
 // accumulator.  Per SM this halves the B traffic (TMA fill and shared-memory reads)
 // of the one-CTA 128 x 256 tile.
@@ -673,51 +673,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 //   empty[s]  (each CTA)  count 1: the MMA commit, multicast to both CTAs.
 //   tfull[b]  (each CTA)  count 1: the MMA commit, multicast to both CTAs.
 //   tempty[b] (even CTA)  one arrival per epilogue warp of each CTA.
-// 16-bit inputs: the accumulator of a tile is double buffered in TMEM (2 x 256
-// columns) and 4 epilogue warps per CTA drain one while the MMAs fill the other.
-// When the rows of C and D start on 16-byte boundaries each lane stores its own row
-// straight from registers (128-byte C reads, 64-byte BF16 writes per lane and chunk),
-// skipping the shared-memory transpose, whose traffic competed with the operand ring
-// (measured +3.5 % on 4096^3).  Other pitches keep the transpose, which turns them
-// into coalesced row segments (per-lane rows would be 4-byte scalar accesses).
+// The accumulator of a tile is double buffered in TMEM (2 x 256 columns) and 4
+// epilogue warps per CTA drain one while the MMAs fill the other (TMA epilogue for
+// 16-byte-aligned C / D rows, a shared-memory transpose otherwise; see the epilogue).
 // Output tiles past the last full wave are split into two 256 x 128 halves when that
-// lets one half-wave finish the problem.
-// FP8 inputs: each 128-K block is accumulated into one of two TMEM partial buffers;
-// a scale warp stages that block's scale_a (this CTA's 128 rows) and scale_b (the
-// tile's two 128-column blocks) into a shared-memory ring with cp.async, and 8
-// promotion warps add scale_a * scale_b * partial into FP32 registers (32 rows x 128
-// columns per warp), then store the tile straight from registers.  The two partial
-// buffers fill TMEM, so a buffer must be read and handed back within one block's MMA
-// time (measured: 16 warps of 64 columns were slower, twice the hand-back arrivals).
-template <int BN_, bool FP8_>
+// lets one half-wave finish the problem, and a problem whose halves all fit one wave
+// runs as halves only.  (FP8 runs on the one-CTA kernel: a pair version of the block
+// promotion, whose MMA waits for the partial-buffer hand-back of 16 warps in two CTAs,
+// measured 3 to 17 % slower at every size from 1792^3 to 8192^3.)
+template <int BN_>
 struct PairCfg {
   static constexpr int BN = BN_;  // pair tile N
-  static constexpr bool FP8 = FP8_;
-  static constexpr int ELT = FP8 ? 1 : 2;
-  static constexpr int BK = 128 / ELT;  // K per stage (one 128-byte row)
-  static constexpr int UMMA_K = 32 / ELT;
+  static constexpr int ELT = 2;
+  static constexpr int BK = 64;   // K per stage (one 128-byte row)
+  static constexpr int UMMA_K = 16;
   static constexpr int KSTEPS = BK / UMMA_K;
   static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BOX_N = 128 / ELT;
+  static constexpr int B_BOX_N = 64;
   static constexpr int B_BOX_BYTES = BK * 128;
   static constexpr int B_BOXES_MAX = BN / 2 / B_BOX_N;  // per CTA
   static constexpr int STAGE_BYTES = A_BYTES + B_BOXES_MAX * B_BOX_BYTES;
-  // 16-bit: 5 operand stages leave room for the epilogue's C / D buffers
-  static constexpr int STAGES = FP8 ? 196608 / STAGE_BYTES : 163840 / STAGE_BYTES;
+  // 5 operand stages leave room for the epilogue's C / D buffers
+  static constexpr int STAGES = 163840 / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int EPI_WARP0 = FP8 ? 3 : 2;  // warps: producer, MMA, [scales], epilogue
-  static constexpr int EPI_WARPS = FP8 ? 8 : 4;
+  static constexpr int EPI_WARP0 = 2;  // warps: producer, MMA, epilogue
+  static constexpr int EPI_WARPS = 4;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
-  // 16-bit epilogue: EPI_BUFS buffers of one 32 x 32 FP32 chunk per warp (the TMA path
-  // cycles through them; the transposing path uses the first as its staging buffer)
-  static constexpr int EPI_BUFS = FP8 ? 0 : 4;
+  // EPI_BUFS buffers of one 32 x 32 FP32 chunk per epilogue warp (the TMA path cycles
+  // through them; the transposing path uses the first as its staging buffer)
+  static constexpr int EPI_BUFS = 4;
   static constexpr int EPI_BUF_BYTES = 32 * 32 * 4;
   static constexpr int EPI_STAGE_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-  static constexpr int SC_SLOTS = FP8 ? 8 : 0;
-  static constexpr int SC_FLOATS = 128 + 4;  // scale_a of 128 rows, scale_b of 2 blocks, pad
-  static constexpr int SC_BYTES = SC_SLOTS * SC_FLOATS * 4;
-  static constexpr int NBARS = 2 * STAGES + 5 + 2 * SC_SLOTS + EPI_WARPS * EPI_BUFS;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + SC_BYTES + NBARS * 8 + 16 + 1024;
+  static constexpr int NBARS = 2 * STAGES + 5 + EPI_WARPS * EPI_BUFS;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + NBARS * 8 + 16 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(TMEM_COLS <= 512, "TMEM budget");
   static_assert(B_BOXES_MAX >= 1, "B half must cover a whole swizzle row");
@@ -736,16 +724,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const GemmParams p, const PairSched sc) {
   constexpr int S = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
-  constexpr int J = Cfg::SC_SLOTS > 0 ? Cfg::SC_SLOTS : 1;  // (FP8 scale ring; unused otherwise)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* epi_stage = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES);
-  float* scales = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES +
-                                               Cfg::SC_BYTES);
-  // bars: full[S], empty[S], tfull[2], tempty[2], drain, sc_full[J], sc_empty[J],
-  //       cfull[EPI_WARPS][EPI_BUFS] (16-bit TMA epilogue: C chunk landed in a buffer)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain,
+  //       cfull[EPI_WARPS][EPI_BUFS] (TMA epilogue: a C chunk landed in a buffer)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
   uint32_t* abort_flag = tmem_slot + 1;
 
@@ -760,11 +745,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * S + b); };
   auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * S + 2 + b); };
   const uint32_t drain_bar = smem_addr(bars + 2 * S + 4);
-  auto sc_full_bar = [&](int j) { return smem_addr(bars + 2 * S + 5 + j); };
-  auto sc_empty_bar = [&](int j) { return smem_addr(bars + 2 * S + 5 + J + j); };
-  auto cfull_bar = [&](int w, int b) {
-    return smem_addr(bars + 2 * S + 5 + 2 * Cfg::SC_SLOTS + w * Cfg::EPI_BUFS + b);
-  };
+  auto cfull_bar = [&](int w, int b) { return smem_addr(bars + 2 * S + 5 + w * Cfg::EPI_BUFS + b); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -776,10 +757,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(tempty_bar(b), 2 * Cfg::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
-    for (int j = 0; j < Cfg::SC_SLOTS; ++j) {
-      mbar_init(sc_full_bar(j), 32);                  // one cp.async arrival per scale lane
-      mbar_init(sc_empty_bar(j), Cfg::EPI_WARPS);     // one arrival per promotion warp
-    }
     for (int w = 0; w < Cfg::EPI_WARPS; ++w)
       for (int b = 0; b < Cfg::EPI_BUFS; ++b) mbar_init(cfull_bar(w, b), 1);
     *abort_flag = 0u;
@@ -870,23 +847,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int m0, n0, ncols;
         unit(u, m0, n0, ncols);
         const uint32_t idesc = make_idesc(AB_FMT, ncols, 256);
-        uint32_t d_tmem = 0;
-        if (!Cfg::FP8) {  // one accumulator per tile
-          const uint32_t ab = acc_it & 1u;
-          if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) break;
-          tc_fence_after();
-          d_tmem = tmem_base + ab * BN;
-        }
+        const uint32_t ab = acc_it & 1u;  // one accumulator per tile
+        if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * BN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (Cfg::FP8) {  // one partial buffer per 128-K block
-            const uint32_t pb = acc_it & 1u;
-            if (!wait_bounded(tempty_bar(pb), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            d_tmem = tmem_base + pb * BN;
-          }
           const int s = it % S;
           if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
             ok = false;
@@ -900,66 +865,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc =
                 smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BOX_BYTES, 1024);
-            if (Cfg::FP8)
-              mma_f8_pair(d_tmem, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
-            else
-              mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair_mc(empty_bar(s), 0x3);
           ++it;
-          if (Cfg::FP8) {
-            mma_commit_pair_mc(tfull_bar(acc_it & 1u), 0x3);
-            ++acc_it;
-          }
         }
         if (!ok) break;
-        if (!Cfg::FP8) {
-          mma_commit_pair_mc(tfull_bar(acc_it & 1u), 0x3);
-          ++acc_it;
-        }
+        mma_commit_pair_mc(tfull_bar(ab), 0x3);
+        ++acc_it;
       }
       mma_commit_pair(drain_bar);
       wait_drain(drain_bar, 0u, p.timeout_ns);
     }
-  } else if (Cfg::FP8 && warp == 2) {
-    // ---------------------------------------------------------------- scale loader (FP8)
-    const int nblk_total = (p.N + 127) / 128;
-    uint32_t seq = 0;
-    bool ok = true;
-    for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
-      int m0, n0, ncols;
-      unit(u, m0, n0, ncols);
-      // lane l copies rows l, l + 32, l + 64, l + 96: each cp.async of the warp writes 32
-      // consecutive words (no bank conflicts)
-      const int row0 = m0 + 128 * static_cast<int>(rank) + lane;
-      const int nb0 = n0 / 128;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int j = seq % J;
-        bool w = wait_bounded(sc_empty_bar(j), ((seq / J) & 1u) ^ 1u, wctx, kRoleProducer);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        float* slot = scales + j * Cfg::SC_FLOATS;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = row0 + 32 * i;
-          const bool v = row < p.M;
-          cp_async_4(smem_addr(slot + lane + 32 * i), v ? p.sA + static_cast<int64_t>(row) * p.ld_sa + kb : p.sA,
-                     v ? 4u : 0u);
-        }
-        if (lane < 2) {
-          const int nbk = nb0 + lane;
-          const bool v = (lane * 128 < ncols) && nbk < nblk_total;
-          cp_async_4(smem_addr(slot + 128 + lane), v ? p.sB + static_cast<int64_t>(kb) * p.ld_sb + nbk : p.sB,
-                     v ? 4u : 0u);
-        }
-        cp_async_mbar_arrive_noinc(sc_full_bar(j));
-        ++seq;
-      }
-    }
-  } else if (!Cfg::FP8) {
+  } else {
     // ---------------------------------------------------------------- epilogue (each CTA)
     const int q = warp & 3;
     const int ew = warp - Cfg::EPI_WARP0;
@@ -975,7 +893,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       // read it.  Chunks wholly outside the matrix are neither loaded nor stored; the
       // chunk that crosses column N is stored by the lanes themselves (a TMA store
       // writes whole 16-byte units and would reach into the columns past N).
-      constexpr int R = Cfg::EPI_BUFS > 2 ? Cfg::EPI_BUFS : 3;  // (FP8 instances never get here)
+      constexpr int R = Cfg::EPI_BUFS;
       constexpr int PF = R - 2;  // C loads in flight ahead; the latest store may still read
       const bool use_c = p.beta != 0.0f;
       const bool out32 = p.d_type == LL_OUT_F32;
@@ -1153,65 +1071,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ++acc_it;
       }
     }
-  } else {
-    // ---------------------------------------------------------------- promotion (FP8, each CTA)
-    constexpr int GROUPS = Cfg::EPI_WARPS / 4;  // warps per TMEM lane quarter
-    constexpr int HALF = BN / GROUPS;           // columns per promotion warp
-    constexpr int CH = HALF / 32;
-    const int ew = warp - Cfg::EPI_WARP0;
-    const int q = warp & 3;
-    const int h = ew >> 2;
-    const int sb_idx = (h * HALF) / 128;  // which of the tile's 128-column scale blocks
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t pit = 0, seq = 0;
-    bool ok = true;
-    for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
-      int m0, n0, ncols;
-      unit(u, m0, n0, ncols);
-      const int m = m0 + 128 * static_cast<int>(rank) + q * 32 + lane;
-      float acc[CH][32];
-#pragma unroll
-      for (int c = 0; c < CH; ++c)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[c][j] = 0.0f;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int j = seq % J;
-        const uint32_t pb = pit & 1u;
-        bool w = wait_bounded(sc_full_bar(j), (seq / J) & 1u, wctx, kRoleEpilogue);
-        w = w && wait_bounded(tfull_bar(pb), (pit >> 1) & 1u, wctx, kRoleEpilogue);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float* slot = scales + j * Cfg::SC_FLOATS;
-        const float s = slot[q * 32 + lane] * slot[128 + sb_idx];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sc_empty_bar(j));
-        // 16 columns per TMEM load keep 128 accumulators + staging within the
-        // register budget
-#pragma unroll
-        for (int c = 0; c < 2 * CH; ++c) {
-          uint32_t r[16];
-          tmem_ld_x16(tmem_base + lane_base + pb * BN + h * HALF + c * 16, r);
-          tmem_ld_wait();
-          if (c == 2 * CH - 1) {  // partial fully read: the MMAs may reuse the buffer
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(pb), 0));
-          }
-#pragma unroll
-          for (int jj = 0; jj < 16; jj += 2)
-            ffma2(acc[c >> 1][(c & 1) * 16 + jj], acc[c >> 1][(c & 1) * 16 + jj + 1],
-                  __uint_as_float(r[jj]), __uint_as_float(r[jj + 1]), s);
-        }
-        ++pit;
-        ++seq;
-      }
-      if (!ok) break;
-      if (h * HALF < ncols) epilogue_rows<CH>(p, m, n0 + h * HALF, acc);
-    }
   }
 
   tc_fence_before();
@@ -1326,16 +1185,15 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
 }
 
 
-template <bool FP8, uint32_t AB_FMT>
+template <uint32_t AB_FMT>
 static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
-  using Cfg = PairCfg<256, FP8>;
+  using Cfg = PairCfg<256>;
   auto kern = gemm_tc2_kernel<Cfg, AB_FMT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
       cudaSuccess)
     return LL_ERR_CUDA;
   const CUtensorMapDataType dt =
-      FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-          : ((AB_FMT & 7u) == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+      (AB_FMT & 7u) == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tmA, tmB, tmC, tmD;
   if (!make_tensor_map_2d(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
   if (!make_tensor_map_2d(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
@@ -1345,7 +1203,7 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   memset(&tmC, 0, sizeof(tmC));
   memset(&tmD, 0, sizeof(tmD));
   const bool o32 = a.d_type == LL_OUT_F32;
-  p.epi_tma = !FP8 && p.d_row16 && (a.beta == 0.0f || p.c_vec);
+  p.epi_tma = p.d_row16 && (a.beta == 0.0f || p.c_vec);
   if (p.epi_tma) {
     if (!make_tensor_map_2d(&tmD, a.D, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
                             o32 ? 4 : 2, a.M, a.N, a.ldd, 32, 32,
@@ -1389,15 +1247,13 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   const int T = sc.num_m2 * sc.num_n;
   int P = T < max_pairs[dev] ? T : max_pairs[dev];
   const int waves = T / P, rem = T - waves * P;
-  // 16-bit: finish with one half-wave of 256 x 128 halves when that is shorter; a
-  // problem whose halves all fit one wave runs as halves only (twice the pairs at work).
-  // (FP8 halves would give each CTA 64 one-byte columns, narrower than a 128-byte
-  // swizzle row, so FP8 keeps whole tiles.)
-  if (!FP8 && 2 * T <= max_pairs[dev]) {
+  // finish with one half-wave of 256 x 128 halves when that is shorter; a problem whose
+  // halves all fit one wave runs as halves only (twice the pairs at work)
+  if (2 * T <= max_pairs[dev]) {
     sc.full_units = 0;
     sc.num_units = 2 * T;
     P = 2 * T;
-  } else if (!FP8 && rem > 0 && 2 * rem <= P) {
+  } else if (rem > 0 && 2 * rem <= P) {
     sc.full_units = waves * P;
     sc.num_units = sc.full_units + 2 * rem;
   } else {
@@ -1413,36 +1269,32 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
 }
 
 template <uint32_t F>
-static ll_status run_fp8(const GemmArgs& a, const LaunchCtx& ctx, bool pair) {
-  if (pair) return run_pair<true, F>(a, ctx);
+static ll_status run_fp8(const GemmArgs& a, const LaunchCtx& ctx) {
   if (a.N > 128) return run<TileCfg<256, true>, F>(a, ctx);
   return run<TileCfg<128, true>, F>(a, ctx);
 }
 
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
-  // CTA pairs from SMs/4 pair tiles on (16-bit: from SMs/8 when M and N both exceed
-  // 128, the problems with at most half a wave of tiles then running as 256 x 128
-  // halves; measured on GB300: 1280^3 267 -> 347 TFLOPS, 1536^3 402 -> 537,
-  // 1536 x 1536 x 4096 494 -> 780, 256 x 8192 x 4096 425 -> 687, while 1024^3 (16 pair
-  // tiles) and M or N of 128 stay faster on the one-CTA kernel)
-  const int pair_tiles = ((a.M + 255) / 256) * ((a.N + 255) / 256);
-  const bool f8 = a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2;
-  const bool pair = f8 ? pair_tiles >= ctx.num_sms / 4
-                       : (pair_tiles >= ctx.num_sms / 4 ||
-                          (pair_tiles >= ctx.num_sms / 8 && a.M > 128 && a.N > 128));
+  // FP8: the one-CTA kernel at every size (it measured 3 to 17 % faster than a CTA-pair
+  // version of the block promotion from 1792^3 to 8192^3)
   if (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) {
     const bool a5 = a.in_type == LL_IN_E5M2, b5 = a.b_type == LL_IN_E5M2;
-    if (!a5 && !b5) return run_fp8<fmt_pair(0, 0)>(a, ctx, pair);
-    if (a5 && b5) return run_fp8<fmt_pair(1, 1)>(a, ctx, pair);
-    if (!a5) return run_fp8<fmt_pair(0, 1)>(a, ctx, pair);
-    return run_fp8<fmt_pair(1, 0)>(a, ctx, pair);
+    if (!a5 && !b5) return run_fp8<fmt_pair(0, 0)>(a, ctx);
+    if (a5 && b5) return run_fp8<fmt_pair(1, 1)>(a, ctx);
+    if (!a5) return run_fp8<fmt_pair(0, 1)>(a, ctx);
+    return run_fp8<fmt_pair(1, 0)>(a, ctx);
   }
+  // 16-bit: CTA pairs from SMs/4 pair tiles on, or from SMs/8 when M and N both exceed
+  // 128 (the problems with at most half a wave of tiles then running as 256 x 128
+  // halves; measured on GB300: 1280^3 265 -> 343 TFLOPS, 1536^3 400 -> 532,
+  // 1536 x 1536 x 4096 494 -> 777, 256 x 8192 x 4096 424 -> 684, while 1024^3 (16 pair
+  // tiles) and M or N of 128 stay faster on the one-CTA kernel); the rest has fewer tiles
+  // than SMs even at 128 x 64
+  const int pair_tiles = ((a.M + 255) / 256) * ((a.N + 255) / 256);
+  const bool pair = pair_tiles >= ctx.num_sms / 4 || (pair_tiles >= ctx.num_sms / 8 && a.M > 128 && a.N > 128);
   constexpr uint32_t F16 = fmt_pair(0, 0), BF16 = fmt_pair(1, 1);
   const bool bf = a.in_type == LL_IN_BF16;
-  // large problems: CTA pairs with 256 x 256 tiles
-  if (pair) return bf ? run_pair<false, BF16>(a, ctx) : run_pair<false, F16>(a, ctx);
-  // the rest has fewer tiles than SMs even at 128 x 64 (a wider one-CTA tile would only
-  // be picked with a full wave of it, and such problems run on CTA pairs)
+  if (pair) return bf ? run_pair<BF16>(a, ctx) : run_pair<F16>(a, ctx);
   return bf ? run<TileCfg<64, false>, BF16>(a, ctx) : run<TileCfg<64, false>, F16>(a, ctx);
 }
 
