@@ -50,6 +50,7 @@ def gemv_bytes(N, K):
 
 KERNEL_SOURCES = {
     "gemm_tc2_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/ptx.cuh"],
+    "gemm_tc_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/ptx.cuh"],
     "gemv_w8a8_kernel": ["linear_layer_gb300/csrc/gemv_w8a8.cu", "linear_layer_gb300/csrc/ptx.cuh"],
 }
 
@@ -279,7 +280,7 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
     peak = peaks[peak_key]
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": measured_traffic(HEADLINE, "gemm_tc2_kernel"),
-                "kernel": "gemm_tc2_kernel<PairCfg<256,false>,9> (CTA pairs, BF16 x BF16)",
+                "kernel": "gemm_tc2_kernel<PairCfg<256>,9> (CTA pairs, BF16 x BF16)",
                 "peak_source": "%s %s" % (peak_src, peak_key),
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": set_bytes,
@@ -623,8 +624,8 @@ def bench_fp8(args, dev, stream, peaks, peak_src):
             "ms_per_launch": round(statistics.mean(launch_ms), 4),
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                         "traffic": measured_traffic("e4m3_gemm_8192", "gemm_tc2_kernel"),
-                         "kernel": "gemm_tc2_kernel<PairCfg<256,true>,0> (CTA pairs)",
+                         "traffic": measured_traffic("e4m3_gemm_8192", "gemm_tc_kernel"),
+                         "kernel": "gemm_tc_kernel<TileCfg<256,true>,0> (one CTA per 128 x 256 tile)",
                          "peak_source": "%s bf16_tflops x %g (nominal FP8:BF16)" % (peak_src, FP8_OVER_BF16),
                          "algorithmic_bytes_per_launch": M * K + K * N + M * KB * 4 + KB * NB * 4 + M * N * 2},
             "timing": "%d launches alternating 2 input sets (A+B 128 MB each)" % steps,
