@@ -71,7 +71,10 @@ struct TileCfg {
   static constexpr int B_BYTES = B_BOXES * B_BOX_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (196608 / STAGE_BYTES) < 8 ? (196608 / STAGE_BYTES) : 8;
-  static constexpr int TMEM_COLS = 2 * BN;
+  // accumulators (16-bit: tiles) or FP8 partial buffers (128-K blocks) in TMEM; FP8
+  // uses all 512 columns, so a 128-column tile has four partial buffers
+  static constexpr int TMEM_COLS = FP8 ? 512 : 2 * BN;
+  static constexpr int NACC = TMEM_COLS / BN;
   static constexpr int EPI_WARPS = FP8 ? 8 : 4;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int EPI_WARP0 = 2;  // first epilogue warp
@@ -403,8 +406,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* epi_stage = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::EPI_STAGE_BYTES);
-  // bars: full[S], empty[S], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  constexpr int NA = Cfg::NACC;
+  // bars: full[S], empty[S], tfull[NA], tempty[NA], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NA + 1);
   uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -413,15 +417,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + S + s); };
   auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * S + b); };
-  auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * S + 2 + b); };
-  const uint32_t drain_bar = smem_addr(bars + 2 * S + 4);
+  auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * S + NA + b); };
+  const uint32_t drain_bar = smem_addr(bars + 2 * S + 2 * NA);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NA; ++b) {
       mbar_init(tfull_bar(b), 1);
       mbar_init(tempty_bar(b), Cfg::EPI_THREADS);
     }
@@ -499,8 +503,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         uint32_t d_tmem = 0;
         if (!Cfg::FP8) {
-          const uint32_t ab = acc_it & 1u;
-          if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) {
+          const uint32_t ab = acc_it % NA;
+          if (!wait_bounded(tempty_bar(ab), ((acc_it / NA) & 1u) ^ 1u, wctx, kRoleMma)) {
             ok = false;
             break;
           }
@@ -509,8 +513,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int kb = 0; kb < KB; ++kb) {
           if (Cfg::FP8) {  // one TMEM partial buffer per 128-K block, alternating
-            const uint32_t pb = acc_it & 1u;
-            if (!wait_bounded(tempty_bar(pb), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) {
+            const uint32_t pb = acc_it % NA;
+            if (!wait_bounded(tempty_bar(pb), ((acc_it / NA) & 1u) ^ 1u, wctx, kRoleMma)) {
               ok = false;
               break;
             }
@@ -539,13 +543,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           mma_commit(empty_bar(s));
           ++it;
           if (Cfg::FP8) {
-            mma_commit(tfull_bar(acc_it & 1u));
+            mma_commit(tfull_bar(acc_it % NA));
             ++acc_it;
           }
         }
         if (!ok) break;
         if (!Cfg::FP8) {
-          mma_commit(tfull_bar(acc_it & 1u));
+          mma_commit(tfull_bar(acc_it % NA));
           ++acc_it;
         }
       }
@@ -562,8 +566,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, num_m, num_n, p.group_m, mb, nb);
-      const uint32_t ab = acc_it & 1u;
-      bool ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
+      const uint32_t ab = acc_it % NA;
+      bool ok = wait_bounded(tfull_bar(ab), (acc_it / NA) & 1u, wctx, kRoleEpilogue);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -618,8 +622,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           sa_next = row_ok ? __ldg(sa_row + kb + 1) : 0.0f;
           sb_next = col_ok ? __ldg(p.sB + static_cast<int64_t>(kb + 1) * p.ld_sb + nblk) : 0.0f;
         }
-        const uint32_t pb = pit & 1u;
-        bool w = wait_bounded(tfull_bar(pb), (pit >> 1) & 1u, wctx, kRoleEpilogue);
+        const uint32_t pb = pit % NA;
+        bool w = wait_bounded(tfull_bar(pb), (pit / NA) & 1u, wctx, kRoleEpilogue);
         w = __all_sync(0xffffffffu, w);
         if (!w) {
           ok = false;
@@ -1268,9 +1272,13 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   return LL_OK;
 }
 
+// 128 x 256 tiles, or 128 x 128 ones (four TMEM partial buffers) when N <= 128 or when
+// the narrower tiles still fit one wave: measured 1536 x 1536 x 4096 923 -> 1105 TFLOPS,
+// while at 2048^3 and above the 256-wide tile is 1.4-1.6x faster
 template <uint32_t F>
 static ll_status run_fp8(const GemmArgs& a, const LaunchCtx& ctx) {
-  if (a.N > 128) return run<TileCfg<256, true>, F>(a, ctx);
+  const int tiles128 = ((a.M + 127) / 128) * ((a.N + 127) / 128);
+  if (a.N > 128 && tiles128 > ctx.num_sms) return run<TileCfg<256, true>, F>(a, ctx);
   return run<TileCfg<128, true>, F>(a, ctx);
 }
 
