@@ -5,8 +5,10 @@
 // ("Tensor Core" chapter, section "Tensor Core 做什么" and table "精度": low-precision
 // inputs, FP32 accumulator; FP8 with per-block scaling factors.)
 //
-// One persistent CTA per SM walks a static list of 128 x BN output tiles in a
-// grouped (L2-friendly) order.  Warp roles:
+// Two kernels: the one-CTA kernel below (small 16-bit problems, and FP8 at every size)
+// and the CTA-pair kernel further down (large 16-bit problems); launch_gemm_tc at the
+// end chooses.  In the one-CTA kernel one persistent CTA per SM walks a static list of
+// 128 x BN output tiles in a grouped (L2-friendly) order.  Warp roles:
 //   warp 0      TMA producer: A (128 x BK, K-major) and B (BK x BN, N-major) tiles,
 //               128-byte swizzle, into a STAGES-deep shared-memory ring (mbarrier
 //               full/empty pairs).  The K tail is zero-filled by TMA out-of-bounds fill.
@@ -19,9 +21,10 @@
 //               chunk is transposed through shared memory so that global C loads and
 //               D stores are row segments (coalesced for any leading dimension).
 //               FP8 inputs: 8 warps promote each 128-K block: the MMAs accumulate one
-//               block into a TMEM partial buffer (two, alternating), the warps read it
-//               and add scale_a[m][kb] * scale_b[kb][n/128] * partial into FP32
-//               registers; at the end of the tile they apply alpha/beta and store.
+//               block into a TMEM partial buffer (NACC of them in turn: two for
+//               256-wide tiles, four for 128-wide ones), the warps read it and add
+//               scale_a[m][kb] * scale_b[kb][n/128] * partial into FP32 registers; at
+//               the end of the tile they apply alpha/beta and store.
 // Every wait is bounded: on expiry the CTA records LL_ERR_DEVICE_TIMEOUT, drains the
 // copies and MMAs it has in flight, frees TMEM and exits.
 #include <cuda_bf16.h>
