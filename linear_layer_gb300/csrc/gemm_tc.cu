@@ -903,6 +903,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       constexpr int R = Cfg::EPI_BUFS;
       constexpr int PF = R - 2;  // C loads in flight ahead; the latest store may still read
       const bool use_c = p.beta != 0.0f;
+      const uint64_t pol_once = l2_evict_first_policy();
       const bool out32 = p.d_type == LL_OUT_F32;
       const bool bf = p.d_type == LL_OUT_BF16;
       // prefetch cursor: the chunk whose C load is issued next
@@ -925,7 +926,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int n = pn + 32 * pc;
         if (n < p.N && pm < p.M) {
           mbar_arrive_expect_tx(cfull_bar(ew, b), Cfg::EPI_BUF_BYTES);
-          tma_load_2d(smem_addr(ebuf + b * Cfg::EPI_BUF_BYTES), &tmC, cfull_bar(ew, b), n, pm);
+          tma_load_2d_hint(smem_addr(ebuf + b * Cfg::EPI_BUF_BYTES), &tmC, cfull_bar(ew, b), n, pm, pol_once);
         } else {
           mbar_arrive(cfull_bar(ew, b));
         }
@@ -1006,7 +1007,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0 && m_w < p.M) tma_store_2d(&tmD, bsm, n, m_w);
+            if (lane == 0 && m_w < p.M) tma_store_2d_hint(&tmD, bsm, n, m_w, pol_once);
           } else if (n < p.N && m_w + lane < p.M) {
             // the chunk that crosses column N: a TMA store may write whole 16-byte units
             // past N, so each lane stores its row's valid columns itself
