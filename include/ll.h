@@ -13,7 +13,8 @@
  *     ELEMENTS, between the starts of consecutive rows; ld >= the row width.
  *   - Every pointer except the ones named "host" is caller-owned DEVICE memory on
  *     the current CUDA device.  The library allocates no device memory per call;
- *     its only device state is one status word per device (see ll_get_device_status).
+ *     its only device state is one status word per device (see ll_get_device_status)
+ *     and the fixed scratch array of ll_gemm_f16_noalloc (16 MiB per device).
  *   - Every entry point is asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  Argument errors are detected on the host and
  *     returned before anything is launched; nothing is written in that case.
