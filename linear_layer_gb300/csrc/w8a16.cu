@@ -278,9 +278,9 @@ __global__ void __launch_bounds__(kWoThreads, CTAS) w8a16_kernel(const WoParams 
 
 // One token, K a multiple of 4096 (exact rows, as the W8A8 GEMV's exact path): warp g of
 // the grid owns rows g, g + G, ...; each lane streams 8 16-byte pieces of a row per batch
-// (4 KB per warp in flight, the next row's first batch requested before the reduction),
-// with the activation staged once per CTA in shared memory.  Measured 4491 vs 3798 GB/s
-// on the 11008 x 4096 layer against the general walk.
+// (4 KB per warp in flight), with the activation staged once per CTA in shared memory.
+// Measured 4491 vs 3798 GB/s on the 11008 x 4096 layer against the general walk; refilling
+// each half-batch's registers as soon as that half is multiplied in took 10.48 -> 10.20 us.
 __global__ void __launch_bounds__(256, 3) w8a16_row_kernel(const WoParams p) {
   extern __shared__ int4 smem[];  // the token's K activations, BF16
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -299,45 +299,64 @@ __global__ void __launch_bounds__(256, 3) w8a16_row_kernel(const WoParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < (p.K >> 3); i += 256) smem[i] = reinterpret_cast<const int4*>(p.X)[i];
   __syncthreads();
-  while (r < p.N) {
-    uint64_t acc2 = 0ull;
-    for (int b = 0;;) {
+  // The registers hold one 4096-element batch (row r, batch b) as two halves of 4
+  // pieces; each half's registers are refilled with the next batch's half as soon as the
+  // half has been multiplied in, so the next weights are in flight during the other
+  // half's work (the products and their order are unchanged).
+  auto ld_half = [&](int rr, int bb, int j0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = b * 256 + lane + 32 * j;  // 16-byte weight piece: K 16 c .. 16 c + 15
-        const int4 lo = smem[2 * c], hi = smem[2 * c + 1];
-        const uint32_t xr[8] = {static_cast<uint32_t>(lo.x), static_cast<uint32_t>(lo.y), static_cast<uint32_t>(lo.z),
-                                static_cast<uint32_t>(lo.w), static_cast<uint32_t>(hi.x), static_cast<uint32_t>(hi.y),
-                                static_cast<uint32_t>(hi.z), static_cast<uint32_t>(hi.w)};
+    for (int j = j0; j < j0 + 4; ++j)
+      w[j] = rr < p.N ? ld_stream(reinterpret_cast<const int4*>(p.W + static_cast<int64_t>(rr) * p.ldw) + bb * 256 + lane + 32 * j)
+                      : make_int4(0, 0, 0, 0);
+  };
+  auto mul_piece = [&](uint64_t& acc2, int bb, int j) {
+    const int c = bb * 256 + lane + 32 * j;  // 16-byte weight piece: K 16 c .. 16 c + 15
+    const int4 lo = smem[2 * c], hi = smem[2 * c + 1];
+    const uint32_t xr[8] = {static_cast<uint32_t>(lo.x), static_cast<uint32_t>(lo.y), static_cast<uint32_t>(lo.z),
+                            static_cast<uint32_t>(lo.w), static_cast<uint32_t>(hi.x), static_cast<uint32_t>(hi.y),
+                            static_cast<uint32_t>(hi.z), static_cast<uint32_t>(hi.w)};
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-          const uint32_t wd = e4 == 0 ? w[j].x : e4 == 1 ? w[j].y : e4 == 2 ? w[j].z : w[j].w;
-          const uint32_t q = wd ^ 0x80808080u;
-          fma_f32x2(acc2, bf16x2_to_f32x2(xr[2 * e4]), bytes_to_f32x2(q, 0));
-          fma_f32x2(acc2, bf16x2_to_f32x2(xr[2 * e4 + 1]), bytes_to_f32x2(q, 2));
-        }
-      }
-      if (++b == nb) break;
-      ld_batch(r, b);
+    for (int e4 = 0; e4 < 4; ++e4) {
+      const uint32_t wd = e4 == 0 ? w[j].x : e4 == 1 ? w[j].y : e4 == 2 ? w[j].z : w[j].w;
+      const uint32_t q = wd ^ 0x80808080u;
+      fma_f32x2(acc2, bf16x2_to_f32x2(xr[2 * e4]), bytes_to_f32x2(q, 0));
+      fma_f32x2(acc2, bf16x2_to_f32x2(xr[2 * e4 + 1]), bytes_to_f32x2(q, 2));
     }
-    const int rn = r + G;
-    ld_batch(rn, 0);  // next row in flight while this one is reduced and stored
-    uint32_t lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(acc2));
-    float v = __fadd_rn(__uint_as_float(lo), __uint_as_float(hi));
+  };
+  uint64_t acc2 = 0ull;
+  int b = 0;
+  while (r < p.N) {
+    int rn = r, bn = b + 1;  // the batch after this one
+    if (bn == nb) {
+      bn = 0;
+      rn = r + G;
+    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (lane == 0) {
-      v = __fmul_rn(v, p.w_scale[r]);
-      if (p.bias) v = __fadd_rn(v, p.bias[r]);
-      if (p.y_type == LL_OUT_F32)
-        static_cast<float*>(p.Y)[r] = v;
-      else if (p.y_type == LL_OUT_BF16)
-        static_cast<__nv_bfloat16*>(p.Y)[r] = __float2bfloat16_rn(v);
-      else
-        static_cast<__half*>(p.Y)[r] = __float2half_rn(v);
+    for (int j = 0; j < 4; ++j) mul_piece(acc2, b, j);
+    ld_half(rn, bn, 0);
+#pragma unroll
+    for (int j = 4; j < 8; ++j) mul_piece(acc2, b, j);
+    ld_half(rn, bn, 4);
+    if (bn == 0) {  // row r complete
+      uint32_t lo, hi;
+      asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(acc2));
+      float v = __fadd_rn(__uint_as_float(lo), __uint_as_float(hi));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) {
+        v = __fmul_rn(v, p.w_scale[r]);
+        if (p.bias) v = __fadd_rn(v, p.bias[r]);
+        if (p.y_type == LL_OUT_F32)
+          static_cast<float*>(p.Y)[r] = v;
+        else if (p.y_type == LL_OUT_BF16)
+          static_cast<__nv_bfloat16*>(p.Y)[r] = __float2bfloat16_rn(v);
+        else
+          static_cast<__half*>(p.Y)[r] = __float2half_rn(v);
+      }
+      acc2 = 0ull;
     }
     r = rn;
+    b = bn;
   }
 }
 
