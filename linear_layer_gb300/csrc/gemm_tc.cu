@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
-        tmem_ld_wait();
+        tmem_ld_wait(r);
         if (c == BN / 32 - 1) {  // the accumulator is in registers: hand TMEM back now
           tc_fence_before();
           mbar_arrive(tempty_bar(ab));
@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int c = 0; c < 2 * CH; ++c) {
           uint32_t r[16];
           tmem_ld_x16(tmem_base + lane_base + pb * BN + h * HALF + c * 16, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
           if (c == 2 * CH - 1) {  // partial fully read: the MMAs may reuse the buffer
             tc_fence_before();
             mbar_arrive(tempty_bar(pb));
@@ -968,7 +968,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           __syncwarp();
           uint32_t r[32];
           tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
           if (c == chunks - 1) {  // accumulator in registers: release it to the MMA
             tc_fence_before();
             __syncwarp();
@@ -1054,7 +1054,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           float v[32];
           load_c_chunk(p, m_base, n0 + (c + 1) * 32, lane, c_odd);
           tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
           store_chunk(p, st, m_base, n0 + c * 32, v, c_even, lane);
@@ -1066,7 +1066,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             load_c_chunk(p, m1 + row_off, n1, lane, c_even);
           }
           tmem_ld_x32(tmem_base + lane_base + ab * BN + (c + 1) * 32, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
           if (c + 2 == chunks) {  // accumulator in registers: release it to the MMA
             tc_fence_before();
             __syncwarp();

@@ -354,8 +354,14 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld_wait() {
+// Wait for this thread's tcgen05.ld copies into r.  The empty statements after the wait
+// read and rewrite each register of r, so every later use of r depends on them and the
+// compiler cannot move such a use above the wait.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
 // a0 += p0 * s, a1 += p1 * s as one packed FP32x2 FMA (two independent FP32 FMAs,

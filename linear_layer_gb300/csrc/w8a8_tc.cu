@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(TcCfg<NP, S8, SA, BR, CQ>::THREADS, 1)
         for (int c16 = 0; c16 < NP / 16; ++c16) {
           uint32_t r[16];
           tmem_ld_x16(tmem_base + lane_base + cb * NP + c16 * 16, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
 #pragma unroll
           for (int j = 0; j < 16; ++j) acc[c16 * 16 + j] += __float2int_rn(__uint_as_float(r[j]));
         }
