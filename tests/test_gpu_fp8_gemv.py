@@ -54,10 +54,12 @@ def test_fp8_unaligned_pitch_repacked(orc):
 
 @pytest.mark.parametrize("M,N,K,alpha,beta,out", [(2400, 2125, 1000, 1.0, 0.0, "bf16"),
                                                  (1200, 2200, 520, 1.0, 0.0, "bf16"),
-                                                 (1300, 2049, 384, 0.5, -1.25, "f32")])
+                                                 (1300, 2049, 384, 0.5, -1.25, "f32"),
+                                                 (2560, 2100, 256, 1.0, 0.0, "bf16")])
 def test_fp8_wide_tiles(orc, M, N, K, alpha, beta, out):
     """Sizes that run 128 x 256 tiles: an odd number of 128-row blocks, more and fewer
-    tiles than SMs, K tails, an N tail inside a 128-column block."""
+    tiles than SMs, K tails, an N tail inside a 128-column block, and a last column block
+    whose second half lies wholly past N."""
     rng = np.random.default_rng(M)
     last = (M - 1) // 128 * 128
     rows = np.array(sorted({0, 127, 128, 255, last - 1, last, M - 1} | set(int(r) for r in rng.integers(0, M, 6))))
