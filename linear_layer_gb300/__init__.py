@@ -108,11 +108,15 @@ def version():
 
 
 def _p(x):
-    """Pointer of a torch tensor (data_ptr), an int, or None."""
+    """Device pointer of a CUDA torch tensor, an int (taken as a device address), or None.
+    A tensor in host memory is refused: the library would use its address as device
+    memory."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_cuda:
+        raise ValueError("linear_layer_gb300: expected a CUDA tensor, got one on %s" % (x.device,))
     return x.data_ptr()
 
 
@@ -140,7 +144,7 @@ def _ws(workspace):
         return None, 0
     if isinstance(workspace, tuple):
         return workspace
-    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    return _p(workspace), workspace.numel() * workspace.element_size()
 
 
 def gemm_f16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, workspace=None,

@@ -65,3 +65,15 @@ def test_calls_without_a_gpu_fail_cleanly(built_lib):
     # no device: the entry point reports an error instead of crashing
     st = ll.lib.ll_linear_w8a8_gemv(4, 16, 16, 16, 16, 16, 16, 16, None, None)
     assert st in (ll.LL_ERR_NO_DEVICE, ll.LL_ERR_CUDA)
+
+
+def test_binding_refuses_host_tensors(built_lib):
+    """A host tensor never reaches the library as a device pointer."""
+    import torch
+    import linear_layer_gb300 as ll
+    host = torch.zeros(16, dtype=torch.int8)
+    with pytest.raises(ValueError):
+        ll.linear_w8a8_gemv(4, 16, host, host, host, 16, host, host)
+    with pytest.raises(ValueError):
+        ll.gemm_f16(1, 1, 1, 1.0, host, 1, host, 1, 0.0, None, 1, host, 1, ll.OUT_F32,
+                    workspace=host)
