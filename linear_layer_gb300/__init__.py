@@ -109,14 +109,18 @@ def version():
 
 def _p(x):
     """Device pointer of a CUDA torch tensor, an int (taken as a device address), or None.
-    A tensor in host memory is refused: the library would use its address as device
-    memory."""
+    A tensor in host memory, or on another GPU than the current one (where every call
+    runs), is refused: the library would use its address as memory of the current GPU."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
     if not x.is_cuda:
         raise ValueError("linear_layer_gb300: expected a CUDA tensor, got one on %s" % (x.device,))
+    import torch
+    if x.get_device() != torch.cuda.current_device():
+        raise ValueError("linear_layer_gb300: tensor on %s, but the calls run on the current device cuda:%d"
+                         % (x.device, torch.cuda.current_device()))
     return x.data_ptr()
 
 
