@@ -1,0 +1,119 @@
+"""Host-side argument checks of the C ABI, on a machine without a GPU.
+
+Every entry point validates its arguments before it looks for a device, so each
+invalid request must come back with its documented status code (and an empty
+request with LL_OK) without a GPU.  The pointers here are fake addresses that no
+kernel may ever see: the module is skipped wherever a GPU could run a launch that a
+faulty check let through (the GPU suite checks the same rejections with real
+tensors)."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.skipif(torch.cuda.is_available(),
+                                reason="fake device addresses: run only where no GPU exists")
+
+P = 0x7F0000000000  # a 256-byte-aligned stand-in address, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def ll():
+    import importlib.util
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("_ll_build", os.path.join(root, "linear_layer_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+    import linear_layer_gb300
+    return linear_layer_gb300
+
+
+def _gemm(ll, M=64, N=64, K=64, A=P, lda=64, B=P, ldb=64, beta=0.0, C=None, ldc=64, D=P + 0x100000,
+          ldd=64, d_type=0, fn="ll_gemm_f16"):
+    return getattr(ll.lib, fn)(M, N, K, 1.0, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, None, 0, None)
+
+
+def _no_device(ll, st):
+    return st in (ll.LL_ERR_NO_DEVICE, ll.LL_ERR_CUDA)
+
+
+def test_gemm_rejections(ll):
+    E, MIS = ll.LL_ERR_INVALID_ARG, ll.LL_ERR_MISALIGNED
+    assert _gemm(ll, M=-1) == E
+    assert _gemm(ll, K=-1) == E
+    assert _gemm(ll, d_type=7) == E
+    assert _gemm(ll, D=None) == E
+    assert _gemm(ll, ldd=63) == E
+    assert _gemm(ll, beta=1.0, C=None) == E                               # C needed when beta != 0
+    assert _gemm(ll, beta=1.0, C=P + 0x100000, d_type=ll.OUT_BF16) == E   # in place only for FP32
+    assert _gemm(ll, beta=1.0, C=P + 0x100000, ldc=64, ldd=65, d_type=ll.OUT_F32) == E
+    assert _gemm(ll, lda=63) == E
+    assert _gemm(ll, A=None) == E
+    assert _gemm(ll, D=P + 0x100002, d_type=ll.OUT_F32) == MIS            # D not on a 4-byte boundary
+    assert _gemm(ll, D=P + 0x100001, d_type=ll.OUT_BF16) == MIS           # nor a 2-byte one
+    assert _gemm(ll, beta=0.5, C=P + 0x200002) == MIS                     # C read: 4-byte aligned
+    assert _gemm(ll, fn="ll_gemm_bf16", ldb=10) == E
+
+
+def test_gemm_empty_requests_need_no_device(ll):
+    assert _gemm(ll, M=0) == ll.LL_OK
+    assert _gemm(ll, N=0, D=None) == ll.LL_OK
+    assert _gemm(ll, M=0, fn="ll_gemm_bf16") == ll.LL_OK
+
+
+def test_gemm_valid_request_reports_the_missing_device(ll):
+    assert _no_device(ll, _gemm(ll))
+    assert _no_device(ll, _gemm(ll, lda=65))  # a repack is needed, but the device check comes first
+
+
+def _fp8(ll, sA=P + 0x300000, ld_sa=1, sB=P + 0x400000, ld_sb=1, K=128, N=128):
+    return ll.lib.ll_gemm_fp8_blockscaled(64, N, K, 1.0, P, K, sA, ld_sa, P, N, sB, ld_sb, 0.0, None, N,
+                                          P + 0x100000, N, ll.OUT_BF16, None, 0, None)
+
+
+def test_fp8_scale_checks(ll):
+    E, MIS = ll.LL_ERR_INVALID_ARG, ll.LL_ERR_MISALIGNED
+    assert _fp8(ll, sA=None) == E
+    assert _fp8(ll, sB=None) == E
+    assert _fp8(ll, K=129, ld_sa=1) == E   # ceil(129 / 128) = 2 K blocks per row of scale_a
+    assert _fp8(ll, N=129, ld_sb=1) == E   # and 2 column blocks per row of scale_b
+    assert _fp8(ll, sA=P + 0x300002) == MIS
+    assert _no_device(ll, _fp8(ll))
+
+
+def test_gemv_checks(ll):
+    E = ll.LL_ERR_INVALID_ARG
+    g = ll.lib.ll_linear_w8a8_gemv
+    assert g(-1, 64, P, P, P, 64, P, P, None, None) == E
+    assert g(16, 131072, P, P, P, 131072, P, P, None, None) == E   # int32 sums could overflow
+    assert g(16, 64, P, None, P, 64, P, P, None, None) == E        # x_scale
+    assert g(16, 64, P, P, P, 63, P, P, None, None) == E           # ldw < K
+    assert g(16, 64, None, P, P, 64, P, P, None, None) == E        # x with K > 0
+    assert g(0, 64, None, None, None, 0, None, None, None, None) == ll.LL_OK
+    assert _no_device(ll, g(16, 64, P, P, P, 64, P, P, None, None))
+    ex = ll.lib.ll_linear_w8a8_gemv_ex
+    assert ex(16, 64, P, P, P, 64, P, None, 5, None, P, None, None) == E              # output type
+    assert ex(16, 64, P, P, P, 64, P, None, ll.GEMV_OUT_I8, None, P, None, None) == E  # INT8 needs s_y
+
+
+def test_token_layer_checks(ll):
+    E = ll.LL_ERR_INVALID_ARG
+    f = ll.lib.ll_linear_w8a8
+    args = dict(M=4, N=16, K=64, X=P, ldx=64, xs=P, W=P, ldw=64, ws=P, bias=None, yt=ll.GEMV_OUT_F16, ys=None,
+                Y=P + 0x100000, ldy=16, Z=None, ldz=16)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["M"], a["N"], a["K"], a["X"], a["ldx"], a["xs"], a["W"], a["ldw"], a["ws"], a["bias"], a["yt"],
+                 a["ys"], a["Y"], a["ldy"], a["Z"], a["ldz"], None)
+    assert call(M=-1) == E
+    assert call(ldx=63) == E
+    assert call(ldy=15) == E
+    assert call(Z=P + 0x200000, ldz=15) == E
+    assert call(yt=ll.GEMV_OUT_I8) == E
+    assert call(M=0) == ll.LL_OK
+    assert _no_device(ll, call())
+    w = ll.lib.ll_linear_w8a16
+    assert w(2, 16, 64, P, 64, P, 64, P, None, 9, P, 16, None) == E        # output type
+    assert w(2, 16, 64, P, 63, P, 64, P, None, ll.OUT_BF16, P, 16, None) == E   # ldx < K
+    assert w(0, 16, 64, P, 64, P, 64, P, None, ll.OUT_BF16, P, 16, None) == ll.LL_OK
