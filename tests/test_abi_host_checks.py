@@ -117,3 +117,20 @@ def test_token_layer_checks(ll):
     assert w(2, 16, 64, P, 64, P, 64, P, None, 9, P, 16, None) == E        # output type
     assert w(2, 16, 64, P, 63, P, 64, P, None, ll.OUT_BF16, P, 16, None) == E   # ldx < K
     assert w(0, 16, 64, P, 64, P, 64, P, None, ll.OUT_BF16, P, 16, None) == ll.LL_OK
+
+
+def test_noalloc_and_quantiser_checks(ll):
+    E, MIS = ll.LL_ERR_INVALID_ARG, ll.LL_ERR_MISALIGNED
+    n = ll.lib.ll_gemm_f16_noalloc
+
+    def call(M=64, D=P + 0x100000, d_type=0, lda=64, beta=0.0, C=None):
+        return n(M, 64, 64, 1.0, P, lda, P, 64, beta, C, 64, D, 64, d_type, None)
+    assert call(M=-1) == E
+    assert call(lda=10) == E
+    assert call(D=P + 0x100002) == MIS
+    assert call(M=0) == ll.LL_OK
+    assert _no_device(ll, call())
+    q = ll.lib.ll_quantize_per_token_f16
+    assert q(-1, 64, P, 64, P, 64, P, None) == E
+    assert q(4, 64, P, 63, P, 64, P, None) == E   # ldx < K
+    assert _no_device(ll, q(4, 64, P, 64, P, 64, P, None))
