@@ -34,6 +34,7 @@ HEADLINE = "bf16_gemm_4096"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor throughput (4.5 : 2.25 PFLOP/s)
 L2_BYTES = 129 * 1000 * 1000
+HEADLINE_GROUPS = 5  # the headline is the median of this many groups of `steps` steps
 
 # algorithmic work per unit (one call) of each workload
 def gemm_flops(M, N, K):
@@ -257,23 +258,30 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
     if st != ll.LL_OK:
         raise RuntimeError("device status after warm-up: %s" % ll.status_string(st))
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(gpu_smi_id(dev.index)) if rank == 0 or True else None
+    sampler = ClockSampler(gpu_smi_id(dev.index))
     sampler.start()
-    barrier(dev)
-    torch.cuda.synchronize(dev)
-    # back to back, as a model runs its layers: programmatic dependent launch lets each
-    # GEMM's prologue overlap the previous one's tail
-    total_ms, _ = time_events(step, args.steps, stream, per_call=False)
-    torch.cuda.synchronize(dev)
-    barrier(dev)
+    # HEADLINE_GROUPS groups of exactly `steps` steps, each bracketed by a barrier and a
+    # synchronize and timed on the device; the reported group is the median one (max over
+    # ranks within each group).  Steps within a group run back to back, as a model runs
+    # its layers: programmatic dependent launch lets each GEMM's prologue overlap the
+    # previous one's tail.
+    group_s = []
+    for _ in range(HEADLINE_GROUPS):
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        total_ms, _ = time_events(step, args.steps, stream, per_call=False)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        group_s.append(reduce_max(total_ms / 1e3, dev))
     clocks = sampler.stop()
     st, word = ll.get_device_status(stream)
     if st != ll.LL_OK:
         raise RuntimeError("device status after timing: %s" % ll.status_string(st))
-    max_s = reduce_max(total_ms / 1e3, dev)
+    max_s = statistics.median(group_s)
+    total_ms = max_s * 1e3
     flops = gemm_flops(M, N, K)
     value = aggregate(flops * args.steps, world, max_s) / 1e12
-    avg_launch_ms = total_ms / args.steps  # average launch duration over the timed region
+    avg_launch_ms = total_ms / args.steps  # average launch duration over the median group
     achieved = flops / (avg_launch_ms / 1e3) / 1e12
     timed_s = total_ms / 1e3
     peak_key = "bf16_tflops_sustained" if timed_s > 2.0 else "bf16_tflops"
@@ -284,7 +292,7 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
                 "peak_source": "%s %s" % (peak_src, peak_key),
                 "algorithmic_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": set_bytes,
-                "duration": "timed region / steps (back-to-back launches)"}
+                "duration": "median group's timed region / steps (back-to-back launches)"}
 
     # end to end through the public API: every step copies its inputs A, B, C from pinned
     # host memory to the device, runs the GEMM and copies D back to pinned host memory.
@@ -342,8 +350,14 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
            "d2h_bytes_per_step": int(hD[0].numel() * 2), "steps": e2e_steps,
            "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 4),
            "pipelining": "copies of step i+1 overlap the GEMM of step i (2 buffer sets, 3 streams)"}
+    spread = {"groups": HEADLINE_GROUPS, "steps_per_group": args.steps,
+              "ms_per_step_min_median_max": [round(min(group_s) * 1e3 / args.steps, 5),
+                                             round(max_s * 1e3 / args.steps, 5),
+                                             round(max(group_s) * 1e3 / args.steps, 5)],
+              "tflops_min_max": [round(flops * args.steps / max(group_s) / 1e12, 1),
+                                 round(flops * args.steps / min(group_s) / 1e12, 1)]}
     out = {"value": value, "ms_per_step": max_s * 1e3 / args.steps, "roofline": roofline,
-           "e2e": e2e, "clocks": clocks, "gpu_launches": args.steps,
+           "e2e": e2e, "clocks": clocks, "gpu_launches": args.steps, "spread": spread,
            "config": {"workload": HEADLINE, "M": M, "N": N, "K": K, "alpha": cfg["alpha"],
                       "beta": cfg["beta"], "out": "bf16", "accumulate": "fp32",
                       "l2": "inputs rotate over %d resident sets (%.0f MB > L2)" % (
@@ -397,16 +411,24 @@ def bench_gemv(args, dev, stream, peaks, peak_src):
     launch_s = total_ms / 1e3 / (reps * per_graph)
     gbs = wbytes / launch_s / 1e9
     peak = peaks["hbm_gbs"]
+    # one launch at a time: an event on each side of every launch (which ends the overlap
+    # with its neighbours), rotating over the weight copies so each launch streams from HBM
+    _, single_ms = time_events(call, 50, stream, per_call=True)
+    us_single = statistics.median(single_ms) * 1e3
     st, _ = ll.get_device_status(stream)
     return {"metric": "W8A8 GEMV HBM GB/s", "value": round(gbs, 1), "unit": "GB/s",
             "us_per_launch": round(launch_s * 1e6, 3),
+            "us_single_launch": round(us_single, 3),
+            "single_launch_GBs": round(wbytes / (us_single * 1e-6) / 1e9, 1),
+            "single_launch_frac": round(wbytes / (us_single * 1e-6) / 1e9 / peak, 4),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4),
                          "traffic": measured_traffic("w8a8_gemv_4096x11008", "gemv_w8a8_kernel"),
                          "kernel": "gemv_w8a8_kernel", "peak_source": peak_src + " hbm_gbs",
                          "algorithmic_bytes_per_launch": wbytes},
-            "timing": "CUDA graph of %d launches over %d weight copies (%.0f MB > L2), %d replays" % (
-                per_graph, ncopies, ncopies * wbytes / 1e6, reps),
+            "timing": "CUDA graph of %d launches over %d weight copies (%.0f MB > L2), %d replays; "
+                      "single launch: median of 50 launches with an event on each side" % (
+                          per_graph, ncopies, ncopies * wbytes / 1e6, reps),
             "status": ll.status_string(st)}
 
 
@@ -613,22 +635,27 @@ def bench_fp8(args, dev, stream, peaks, peak_src):
     for i in range(3):
         call(i)
     torch.cuda.synchronize(dev)
-    steps = max(5, min(args.steps // 10, 100))
-    total_ms, _ = time_events(call, steps, stream, per_call=False)  # back to back
-    launch_ms = [total_ms / steps]
+    steps = max(10, min(args.steps // 10, 100))
+    group_ms = []
+    for _ in range(5):  # median of 5 groups of back-to-back launches
+        total_ms, _ = time_events(call, steps, stream, per_call=False)
+        group_ms.append(total_ms / steps)
+    ms = statistics.median(group_ms)
     st, _ = ll.get_device_status(stream)
     flops = gemm_flops(M, N, K)
-    tflops = flops / (statistics.mean(launch_ms) / 1e3) / 1e12
+    tflops = flops / (ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     return {"metric": "FP8 block-scaled GEMM TFLOPS", "value": round(tflops, 1), "unit": "TFLOPS",
-            "ms_per_launch": round(statistics.mean(launch_ms), 4),
+            "ms_per_launch": round(ms, 4),
+            "ms_per_launch_min_max": [round(min(group_ms), 4), round(max(group_ms), 4)],
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                          "traffic": measured_traffic("e4m3_gemm_8192", "gemm_tc_kernel"),
                          "kernel": "gemm_tc_kernel<TileCfg<256,true>,0> (one CTA per 128 x 256 tile)",
                          "peak_source": "%s bf16_tflops x %g (nominal FP8:BF16)" % (peak_src, FP8_OVER_BF16),
                          "algorithmic_bytes_per_launch": M * K + K * N + M * KB * 4 + KB * NB * 4 + M * N * 2},
-            "timing": "%d launches alternating 2 input sets (A+B 128 MB each)" % steps,
+            "timing": "median of 5 groups of %d back-to-back launches alternating 2 input sets "
+                      "(A+B 128 MB each)" % steps,
             "status": ll.status_string(st)}
 
 
@@ -723,6 +750,30 @@ def bench_ragged(args, dev, stream, peaks, peak_src):
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
                          "peak_source": peak_src + " bf16_tflops (FP16 = BF16 rate)"},
             "status": ll.status_string(st)}
+
+
+def summarize(extra, head):
+    """Short form of every workload's result: value, unit, roofline fraction, traffic."""
+    out = {}
+    for name, r in extra.items():
+        e = {"value": r.get("value"), "unit": r.get("unit")}
+        rf = r.get("roofline")
+        if rf:
+            e["frac"] = rf.get("frac")
+            e["bound"] = rf.get("bound")
+            e["peak"] = rf.get("peak")
+            if rf.get("traffic") is not None:
+                e["traffic"] = rf.get("traffic")
+        for k in ("us_per_launch", "us_single_launch", "single_launch_frac", "ms_per_launch", "ms_per_call"):
+            if k in r:
+                e[k] = r[k]
+        if "per_tokens" in r:
+            e["per_tokens_GBs"] = {m: v["GBs"] for m, v in r["per_tokens"].items()}
+        out[name] = e
+    out["bf16_gemm_4096"] = {"value": round(head["value"], 1), "unit": "TFLOPS",
+                             "frac": head["roofline"]["frac"],
+                             "tflops_min_max": head["spread"]["tflops_min_max"]}
+    return out
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
@@ -852,11 +903,14 @@ def main(argv=None):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) BF16 A, B; FP32 C), resident in HBM",
             "config": head["config"], "roofline": head["roofline"], "e2e": head["e2e"],
-            "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
-            "library": ll.version(), "extra": extra}
+            "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "spread": head["spread"],
+            "library": ll.version(), "detail": extra}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
-    print(json.dumps(line), flush=True)
+    # the last key: one short entry per workload, so that the end of the line (what a log
+    # tail keeps) carries every kernel's figure and roofline fraction
+    line["extra"] = summarize(extra, head)
+    print(json.dumps(line, separators=(",", ":")), flush=True)
     return 0
 
 

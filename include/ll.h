@@ -14,7 +14,32 @@
  *   - Every pointer except the ones named "host" is caller-owned DEVICE memory on
  *     the current CUDA device.  The library allocates no device memory per call;
  *     its only device state is one status word per device (see ll_get_device_status)
- *     and the fixed scratch array of ll_gemm_f16_noalloc (16 MiB per device).
+ *     and the fixed scratch array of ll_gemm_f16_noalloc (16 MiB per device).  The
+ *     device addresses of both are looked up in the calling thread's current CUDA
+ *     context, again whenever that context differs from the one of the last lookup
+ *     (a context made current through the driver API, or the new primary context
+ *     after a device reset).
+ *   - Outputs may not share memory with inputs or with each other: a request whose
+ *     output byte ranges meet another operand's is rejected (LL_ERR_INVALID_ARG)
+ *     before any launch.  Two matrices with the same row pitch are compared row by
+ *     row (column blocks of one matrix are fine); matrices with different pitches
+ *     count as overlapping when their first-to-last byte spans intersect.  The only
+ *     exception is the in-place GEMM, D == C (see ll_gemm_f16).
+ *   - Ordering with programmatic dependent launch.  Every kernel of this library lets
+ *     the next kernel of its stream begin as soon as it has started, and waits for the
+ *     work before it (griddepcontrol.wait) before it reads activations, C or scales or
+ *     writes any output.  The W8A8 and weight-only layers (ll_linear_w8a8*,
+ *     ll_linear_f16_w8a8_gemv, ll_linear_w8a16) read their weights W and w_scale
+ *     BEFORE that wait, to stream them while earlier work drains.  So W and w_scale
+ *     must not be written by any call of this library that may still be running when
+ *     the layer is launched: every library call on the stream since the last kernel
+ *     there that does not come from this library (such a kernel lets nothing after it
+ *     start before it has finished), or since the last host synchronisation of the
+ *     stream.
+ *     Weights of a model are constants, which meets this; to use a library output
+ *     (say the INT8 output of ll_linear_w8a8) as W, launch any other kernel on the
+ *     stream in between, or synchronise.  The GEMMs read nothing before the wait
+ *     (they only prefetch into L2, which is coherent), so they have no such rule.
  *   - Every entry point is asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  Argument errors are detected on the host and
  *     returned before anything is launched; nothing is written in that case.
@@ -79,14 +104,15 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
  *   C : M x N FP32, ldc >= N; not read when beta == 0 (may then be NULL)
  *   D : M x N, ldd >= N, element type d_type; D may alias C only as the same matrix
  *       (D == C, d_type == LL_OUT_F32, ldd == ldc: each element is read before it is
- *       written); any other overlap of D with A, B or C gives undefined results.
+ *       written); any other overlap of D with A, B or C is rejected (LL_ERR_INVALID_ARG).
  *       Nothing outside the M x N elements of D is written (padding columns included).
  *   workspace : device scratch of ws_bytes (see ll_gemm_workspace_size); may be NULL if 0.
+ *       When a repack will write it, it may overlap no operand (LL_ERR_INVALID_ARG).
  * Every product is accumulated in FP32 over the whole K; alpha * acc + beta * C is
  * evaluated in FP32 and rounded once to d_type (round to nearest even).
  * M == 0 or N == 0: nothing is done.  K == 0: D = beta * C (alpha is not used).
- * Errors: LL_ERR_INVALID_ARG for negative sizes, ld < width, NULL operands, or
- * beta != 0 with C == NULL; LL_ERR_MISALIGNED if D (or C when read) is not aligned to
+ * Errors: LL_ERR_INVALID_ARG for negative sizes, ld < width, NULL operands,
+ * beta != 0 with C == NULL, or overlapping memory; LL_ERR_MISALIGNED if D (or C when read) is not aligned to
  * its element size; LL_ERR_WORKSPACE if a repack is needed and ws_bytes is smaller
  * than ll_gemm_workspace_size; LL_ERR_CUDA if a launch fails.
  */
@@ -144,8 +170,8 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
  *     larger requests return LL_ERR_WORKSPACE before anything is launched.
  *     Operands that are already 16-byte aligned use no scratch and have no limit.
  *   - The first call on a device that needs the scratch looks up its device address
- *     (once per device, with that device current); make that first call before any
- *     stream capture.
+ *     (once per device and CUDA context, with that device current); make that first
+ *     call before any stream capture.
  *   - Every call shares the one scratch array and overwrites what it reads, so calls
  *     that overlap on the GPU (for instance on different streams) race: serialise
  *     them.
@@ -195,11 +221,11 @@ ll_status ll_gemm_f8_blockscaled_mixed(int a_type, int b_type, int M, int N, int
  * |z| <= K * 128^2 must fit INT32, i.e. K <= 131071 (checked: LL_ERR_INVALID_ARG).
  * Ordering: the kernel is launched with programmatic dependent launch.  x, x_scale
  * are read and y, z_out written only after all preceding work on the stream has
- * finished; W and w_scale may be read while the immediately preceding
- * ll_linear_w8a8_gemv call on the same stream is still running, so they must not be
- * that call's y / z_out (weights are never outputs of the previous layer).
+ * finished; W and w_scale are read earlier, so they must not be written by a call of
+ * this library that may still be running (the ordering rule at the top of this file).
  * N == 0: nothing is done.  K == 0: z = 0 and y = fp16(0 * s_x * s_W[o]).
- * Errors: LL_ERR_INVALID_ARG for negative sizes, ldw < K or NULL pointers.
+ * Errors: LL_ERR_INVALID_ARG for negative sizes, ldw < K, NULL pointers, or outputs
+ * that overlap an input or each other.
  */
 ll_status ll_linear_w8a8_gemv(int N, int K, const int8_t* x, const float* x_scale,
                               const int8_t* W, int64_t ldw, const float* w_scale, void* y,
@@ -244,12 +270,12 @@ ll_status ll_linear_w8a8_gemv_ex(int N, int K, const int8_t* x, const float* x_s
  * Every weight byte is read from memory once per group of up to 16 tokens: larger M
  * runs as consecutive groups.  M == 1 is exactly ll_linear_w8a8_gemv_ex.  Results are
  * bit-identical to M calls of ll_linear_w8a8_gemv_ex, one per token.
- * Ordering: programmatic dependent launch as ll_linear_w8a8_gemv (W and w_scale may be
- * read before the preceding kernel of the stream has finished; X, the scales and the
- * outputs only after).
+ * Ordering: programmatic dependent launch as ll_linear_w8a8_gemv (W and w_scale are
+ * read before the preceding work of the stream has finished; X, the other scales and
+ * the outputs only after).
  * M == 0 or N == 0: nothing.  Errors: LL_ERR_INVALID_ARG for negative sizes,
  * K > 131071, ldx < K, ldw < K, ldy < N, ldz < N with z_out, NULL pointers, an unknown
- * y_type or a NULL y_scale with INT8 output.
+ * y_type, a NULL y_scale with INT8 output, or outputs that overlap an input or each other.
  */
 ll_status ll_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, const float* x_scale,
                          const int8_t* W, int64_t ldw, const float* w_scale, const float* bias,
@@ -274,7 +300,7 @@ ll_status ll_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, cons
  * decode-sized M (up to 4 tokens per weight pass; larger M runs as several passes).
  * Ordering: programmatic dependent launch as ll_linear_w8a8_gemv.
  * M == 0 or N == 0: nothing.  Errors: LL_ERR_INVALID_ARG for negative sizes, ldx < K,
- * ldw < K, ldy < N, NULL pointers or an unknown y_type.
+ * ldw < K, ldy < N, NULL pointers, an unknown y_type, or Y overlapping an input.
  */
 ll_status ll_linear_w8a16(int M, int N, int K, const void* X, int64_t ldx, const int8_t* W, int64_t ldw,
                           const float* w_scale, const float* bias, int y_type, void* Y, int64_t ldy,
@@ -288,7 +314,8 @@ ll_status ll_linear_w8a16(int M, int N, int K, const void* X, int64_t ldx, const
  *   q[i][k]  = clamp(rint(x[i][k] / scale[i]), -127, 127)   (FP32 division, ties to even)
  *
  *   x : M x K FP16 (ldx >= K)    q : M x K int8 (ldq >= K)    scale : M FP32
- * M == 0: nothing.  Errors: LL_ERR_INVALID_ARG for negative sizes, ld < K, NULL pointers.
+ * M == 0: nothing.  Errors: LL_ERR_INVALID_ARG for negative sizes, ld < K, NULL pointers,
+ * or q / scale overlapping x or each other.
  */
 ll_status ll_quantize_per_token_f16(int M, int K, const void* x, int64_t ldx, int8_t* q,
                                     int64_t ldq, float* scale, ll_stream_t stream);
@@ -302,7 +329,8 @@ ll_status ll_quantize_per_token_f16(int M, int K, const void* x, int64_t ldx, in
  *   x       : K FP16 (the activation of one token)
  *   x_q     : K int8, written with the quantised activation (required)
  *   x_scale : one FP32, written with its scale (required)
- *   other arguments, ordering and errors as ll_linear_w8a8_gemv_ex.
+ *   other arguments, ordering and errors as ll_linear_w8a8_gemv_ex (x_q and x_scale
+ *   are outputs and may overlap nothing else).
  */
 ll_status ll_linear_f16_w8a8_gemv(int N, int K, const void* x, int8_t* x_q, float* x_scale,
                                   const int8_t* W, int64_t ldw, const float* w_scale,

@@ -14,6 +14,7 @@ namespace {
 struct DeviceState {
   bool ready = false;
   bool supported = false;
+  unsigned long long context_id = 0;  // context the cached addresses belong to
   uint32_t* status = nullptr;
   int num_sms = 0;
   uint64_t timeout_ns = 2000000000ull;
@@ -23,15 +24,54 @@ constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique ID of the calling thread's current CUDA context, 0 when there is none (or the
+// driver cannot tell).  IDs are never reused within a process, so a new context (a
+// device reset, or another context made current) never matches a cached one.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    cudaGetLastError();
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_cur(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 ll_status current_ctx(ll_stream_t stream, ll::LaunchCtx& ctx) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return LL_ERR_NO_DEVICE;
   }
+  unsigned long long cid = current_context_id();
+  if (cid == 0) {
+    // no context bound to this thread yet: cudaSetDevice makes the device's primary
+    // context current (it initialises it if needed)
+    if (cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return LL_ERR_NO_DEVICE;
+    }
+    cid = current_context_id();
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& st = g_dev[dev];
-  if (!st.ready) {
+  if (!st.ready || st.context_id != cid) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -40,6 +80,7 @@ ll_status current_ctx(ll_stream_t stream, ll::LaunchCtx& ctx) {
       return LL_ERR_CUDA;
     }
     st.supported = (major == 10 && minor == 3);
+    st.status = nullptr;
     if (st.supported) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_ll_status_word) != cudaSuccess) {
@@ -49,6 +90,7 @@ ll_status current_ctx(ll_stream_t stream, ll::LaunchCtx& ctx) {
       st.status = static_cast<uint32_t*>(p);
     }
     st.num_sms = sms;
+    st.context_id = cid;
     st.ready = true;
   }
   if (!st.supported) return LL_ERR_NO_DEVICE;
@@ -56,6 +98,8 @@ ll_status current_ctx(ll_stream_t stream, ll::LaunchCtx& ctx) {
   ctx.status = st.status;
   ctx.timeout_ns = st.timeout_ns;
   ctx.num_sms = st.num_sms;
+  ctx.device = dev;
+  ctx.context_id = cid;
   return LL_OK;
 }
 
@@ -67,11 +111,59 @@ bool pitch_ok(const void* p, int64_t ld, int esize) {
   return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * esize) % 16 == 0);
 }
 
+// Workspace bytes for one repacked operand, with room to align the workspace start.
 size_t repack_bytes(int rows, int cols, int esize) {
   return static_cast<size_t>(rows) * static_cast<size_t>(round_up(static_cast<int64_t>(cols) * esize, 16)) + 256;
 }
 
-ll_status gemm_common(ll::GemmArgs a, void* workspace, size_t ws_bytes, ll_stream_t stream) {
+// floor(a / b) for b > 0
+int64_t floor_div(int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// last byte offset + 1 of an extent, saturating
+uint64_t extent_span(const ll::Extent& e) {
+  const uint64_t rows1 = static_cast<uint64_t>(e.rows - 1), pitch = static_cast<uint64_t>(e.pitch);
+  const uint64_t width = static_cast<uint64_t>(e.width);
+  if (rows1 != 0 && pitch > (UINT64_MAX - width) / rows1) return UINT64_MAX;
+  return rows1 * pitch + width;
+}
+
+bool extent_empty(const ll::Extent& e) { return e.base == nullptr || e.rows <= 0 || e.width <= 0; }
+
+}  // namespace
+
+bool ll::extents_overlap(const Extent& x0, const Extent& y0) {
+  if (extent_empty(x0) || extent_empty(y0)) return false;
+  Extent x = x0, y = y0;
+  if (x.rows == 1) x.pitch = y.rows == 1 ? x.width : y.pitch;
+  if (y.rows == 1) y.pitch = x.pitch;
+  const uint64_t xb = reinterpret_cast<uintptr_t>(x.base), yb = reinterpret_cast<uintptr_t>(y.base);
+  const uint64_t xs = extent_span(x), ys = extent_span(y);
+  const bool x_before = xs <= UINT64_MAX - xb ? xb + xs <= yb : false;
+  const bool y_before = ys <= UINT64_MAX - yb ? yb + ys <= xb : false;
+  if (x_before || y_before) return false;  // disjoint spans
+  if (x.pitch != y.pitch || x.pitch <= 0) return true;
+  // same pitch p: row r2 of y starts d + (r2 - r1) * p bytes after row r1 of x; the two
+  // rows share a byte when -y.width < d + t * p < x.width for t = r2 - r1
+  const int64_t p = x.pitch;
+  const int64_t d = static_cast<int64_t>(yb - xb);
+  int64_t t_lo = floor_div(-y.width - d, p) + 1;
+  int64_t t_hi = -floor_div(d - x.width, p) - 1;
+  if (t_lo < -(x.rows - 1)) t_lo = -(x.rows - 1);
+  if (t_hi > y.rows - 1) t_hi = y.rows - 1;
+  return t_lo <= t_hi;
+}
+
+bool ll::outputs_overlap(const Extent* outs, int n_out, const Extent* ins, int n_in) {
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = i + 1; j < n_out; ++j)
+      if (extents_overlap(outs[i], outs[j])) return true;
+    for (int j = 0; j < n_in; ++j)
+      if (extents_overlap(outs[i], ins[j])) return true;
+  }
+  return false;
+}
+
+ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) {
   if (a.M < 0 || a.N < 0 || a.K < 0) return LL_ERR_INVALID_ARG;
   if (a.d_type != LL_OUT_F32 && a.d_type != LL_OUT_BF16 && a.d_type != LL_OUT_F16)
     return LL_ERR_INVALID_ARG;
@@ -85,51 +177,97 @@ ll_status gemm_common(ll::GemmArgs a, void* workspace, size_t ws_bytes, ll_strea
     return LL_ERR_INVALID_ARG;
   // C, D and the scales are read and written element by element: each must be aligned
   // to its element size (A and B are repacked from any address)
-  const uintptr_t dsz = a.d_type == LL_OUT_F32 ? 4 : 2;
+  const int64_t dsz = a.d_type == LL_OUT_F32 ? 4 : 2;
   if (reinterpret_cast<uintptr_t>(a.D) % dsz != 0) return LL_ERR_MISALIGNED;
   if (a.beta != 0.0f && reinterpret_cast<uintptr_t>(a.C) % 4 != 0) return LL_ERR_MISALIGNED;
   if ((a.scale_a && reinterpret_cast<uintptr_t>(a.scale_a) % 4 != 0) ||
       (a.scale_b && reinterpret_cast<uintptr_t>(a.scale_b) % 4 != 0))
     return LL_ERR_MISALIGNED;
+  const bool f8 = a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2;
+  const int64_t kb = (a.K + 127) / 128, nb = (a.N + 127) / 128;
   if (a.K > 0) {
     if (a.A == nullptr || a.B == nullptr || a.lda < a.K || a.ldb < a.N) return LL_ERR_INVALID_ARG;
-    if (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) {
-      const int64_t kb = (a.K + 127) / 128, nb = (a.N + 127) / 128;
-      if (a.scale_a == nullptr || a.scale_b == nullptr || a.ld_sa < kb || a.ld_sb < nb)
-        return LL_ERR_INVALID_ARG;
+    if (f8 && (a.scale_a == nullptr || a.scale_b == nullptr || a.ld_sa < kb || a.ld_sb < nb))
+      return LL_ERR_INVALID_ARG;
+  }
+  // D may share bytes with no input other than itself as C (in place, checked above);
+  // a workspace that a repack will write may share bytes with nothing
+  const int64_t es = in_esize(a.in_type);
+  const bool c_read = a.beta != 0.0f;
+  const bool in_place = c_read && static_cast<const void*>(a.C) == a.D;
+  const Extent D{a.D, a.M, a.N * dsz, a.ldd * dsz};
+  Extent ins[5] = {
+      {a.K > 0 ? a.A : nullptr, a.M, a.K * es, a.lda * es},
+      {a.K > 0 ? a.B : nullptr, a.K, a.N * es, a.ldb * es},
+      {c_read && !in_place ? a.C : nullptr, a.M, a.N * 4, a.ldc * 4},
+      {a.K > 0 && f8 ? a.scale_a : nullptr, a.M, kb * 4, a.ld_sa * 4},
+      {a.K > 0 && f8 ? a.scale_b : nullptr, kb, nb * 4, a.ld_sb * 4},
+  };
+  if (outputs_overlap(&D, 1, ins, 5)) return LL_ERR_INVALID_ARG;
+  if (a.K > 0 && ws != nullptr && ws_bytes > 0) {
+    const RepackPlan plan = plan_repack(a);
+    if (plan.a || plan.b) {
+      const Extent W{ws, 1, static_cast<int64_t>(ws_bytes), static_cast<int64_t>(ws_bytes)};
+      Extent all[6] = {D, ins[0], ins[1], ins[2], ins[3], ins[4]};
+      if (in_place) all[3] = Extent{a.C, a.M, a.N * 4, a.ldc * 4};
+      if (outputs_overlap(&W, 1, all, 6)) return LL_ERR_INVALID_ARG;
     }
   }
+  return LL_OK;
+}
+
+ll::RepackPlan ll::plan_repack(const GemmArgs& a) {
+  const int es = in_esize(a.in_type);
+  RepackPlan pl;
+  pl.a = !pitch_ok(a.A, a.lda, es);
+  pl.b = !pitch_ok(a.B, a.ldb, es);
+  pl.lda_p = round_up(a.K, 16 / es);
+  pl.ldb_p = round_up(a.N, 16 / es);
+  pl.a_bytes = pl.a ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.lda_p * es, 256)) : 0;
+  pl.b_bytes = pl.b ? static_cast<size_t>(static_cast<int64_t>(a.K) * pl.ldb_p * es) : 0;
+  return pl;
+}
+
+ll_status ll::launch_gemm_planned(GemmArgs a, const RepackPlan& plan, void* scratch, const LaunchCtx& ctx) {
+  const int es = in_esize(a.in_type);
+  unsigned char* w = static_cast<unsigned char*>(scratch);
+  // every byte the GEMM reads from the scratch is written here first (pad columns are
+  // zeroed), so nothing an earlier call left there reaches this one
+  if (plan.a) {
+    const ll_status st = launch_repack(a.A, a.lda, w, plan.lda_p, a.M, a.K, es, ctx);
+    if (st != LL_OK) return st;
+    a.A = w;
+    a.lda = plan.lda_p;
+  }
+  if (plan.b) {
+    const ll_status st = launch_repack(a.B, a.ldb, w + plan.a_bytes, plan.ldb_p, a.K, a.N, es, ctx);
+    if (st != LL_OK) return st;
+    a.B = w + plan.a_bytes;
+    a.ldb = plan.ldb_p;
+  }
+  return launch_gemm_tc(a, ctx);
+}
+
+namespace {
+
+ll_status gemm_common(const ll::GemmArgs& a, void* workspace, size_t ws_bytes, ll_stream_t stream) {
+  ll_status st = ll::validate_gemm(a, workspace, ws_bytes);
+  if (st != LL_OK || a.M == 0 || a.N == 0) return st;
   ll::LaunchCtx ctx;
-  ll_status st = current_ctx(stream, ctx);
+  st = current_ctx(stream, ctx);
   if (st != LL_OK) return st;
   if (a.K == 0) return ll::launch_scale_c(a, ctx);
-
-  const int es = in_esize(a.in_type);
-  const bool repack_a = !pitch_ok(a.A, a.lda, es);
-  const bool repack_b = !pitch_ok(a.B, a.ldb, es);
-  size_t need = 0;
-  if (repack_a) need += repack_bytes(a.M, a.K, es);
-  if (repack_b) need += repack_bytes(a.K, a.N, es);
-  if (need > 0) {
+  const ll::RepackPlan plan = ll::plan_repack(a);
+  void* base = nullptr;
+  if (plan.a || plan.b) {
+    const int es = in_esize(a.in_type);
+    size_t need = 0;
+    if (plan.a) need += repack_bytes(a.M, a.K, es);
+    if (plan.b) need += repack_bytes(a.K, a.N, es);
     if (workspace == nullptr || ws_bytes < need) return LL_ERR_WORKSPACE;
-    uintptr_t w = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255);
-    if (repack_a) {
-      const int64_t ld = round_up(a.K, 16 / es);
-      st = ll::launch_repack(a.A, a.lda, reinterpret_cast<void*>(w), ld, a.M, a.K, es, ctx);
-      if (st != LL_OK) return st;
-      a.A = reinterpret_cast<void*>(w);
-      a.lda = ld;
-      w += static_cast<uintptr_t>(round_up(static_cast<int64_t>(a.M) * ld * es, 256));
-    }
-    if (repack_b) {
-      const int64_t ld = round_up(a.N, 16 / es);
-      st = ll::launch_repack(a.B, a.ldb, reinterpret_cast<void*>(w), ld, a.K, a.N, es, ctx);
-      if (st != LL_OK) return st;
-      a.B = reinterpret_cast<void*>(w);
-      a.ldb = ld;
-    }
+    base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
   }
-  return ll::launch_gemm_tc(a, ctx);
+  return ll::launch_gemm_planned(a, plan, base, ctx);
 }
 
 }  // namespace
@@ -137,6 +275,29 @@ ll_status gemm_common(ll::GemmArgs a, void* workspace, size_t ws_bytes, ll_strea
 ll_status ll::current_launch_ctx(ll_stream_t stream, ll::LaunchCtx& ctx) {
   return current_ctx(stream, ctx);
 }
+
+namespace {
+
+// Outputs of a batch-1 W8A8 GEMV call (y, z_out, and for the fused quantiser x_q and its
+// scale) against each other and against every input.
+bool gemv_outputs_overlap(int N, int K, const void* x, int x_esize, const float* x_scale, const int8_t* W,
+                          int64_t ldw, const float* w_scale, const float* bias, const float* y_scale, const void* y,
+                          int y_esize, const int32_t* z_out, const int8_t* x_q, const float* xs_out) {
+  const int64_t n = N, k = K;
+  const ll::Extent outs[4] = {{y, 1, n * y_esize, n * y_esize},
+                              {z_out, 1, n * 4, n * 4},
+                              {K > 0 ? x_q : nullptr, 1, k, k},
+                              {xs_out, 1, 4, 4}};
+  const ll::Extent ins[6] = {{K > 0 ? x : nullptr, 1, k * x_esize, k * x_esize},
+                             {x_scale, 1, 4, 4},
+                             {K > 0 ? W : nullptr, n, k, ldw},
+                             {w_scale, 1, n * 4, n * 4},
+                             {bias, 1, n * 4, n * 4},
+                             {y_scale, 1, 4, 4}};
+  return ll::outputs_overlap(outs, 4, ins, 6);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -231,6 +392,9 @@ ll_status ll_linear_w8a8_gemv(int N, int K, const int8_t* x, const float* x_scal
   if (N == 0) return LL_OK;
   if (x_scale == nullptr || w_scale == nullptr || y == nullptr || ldw < K) return LL_ERR_INVALID_ARG;
   if (K > 0 && (x == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
+  if (gemv_outputs_overlap(N, K, x, 1, x_scale, W, ldw, w_scale, nullptr, nullptr, y, 2, z_out, nullptr,
+                           nullptr))
+    return LL_ERR_INVALID_ARG;
   ll::LaunchCtx ctx;
   ll_status st = current_ctx(stream, ctx);
   if (st != LL_OK) return st;
@@ -247,6 +411,9 @@ ll_status ll_linear_w8a8_gemv_ex(int N, int K, const int8_t* x, const float* x_s
   if (x_scale == nullptr || w_scale == nullptr || y == nullptr || ldw < K) return LL_ERR_INVALID_ARG;
   if (K > 0 && (x == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
   if (y_type == LL_GEMV_OUT_I8 && y_scale == nullptr) return LL_ERR_INVALID_ARG;
+  if (gemv_outputs_overlap(N, K, x, 1, x_scale, W, ldw, w_scale, bias, y_type == LL_GEMV_OUT_I8 ? y_scale : nullptr,
+                           y, y_type == LL_GEMV_OUT_I8 ? 1 : 2, z_out, nullptr, nullptr))
+    return LL_ERR_INVALID_ARG;
   ll::LaunchCtx ctx;
   ll_status st = current_ctx(stream, ctx);
   if (st != LL_OK) return st;
@@ -265,6 +432,9 @@ ll_status ll_linear_f16_w8a8_gemv(int N, int K, const void* x, int8_t* x_q, floa
     return LL_ERR_INVALID_ARG;
   if (K > 0 && (x == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
   if (y_type == LL_GEMV_OUT_I8 && y_scale == nullptr) return LL_ERR_INVALID_ARG;
+  if (gemv_outputs_overlap(N, K, x, 2, nullptr, W, ldw, w_scale, bias, y_type == LL_GEMV_OUT_I8 ? y_scale : nullptr,
+                           y, y_type == LL_GEMV_OUT_I8 ? 1 : 2, z_out, x_q, x_scale))
+    return LL_ERR_INVALID_ARG;
   ll::LaunchCtx ctx;
   ll_status st = current_ctx(stream, ctx);
   if (st != LL_OK) return st;
@@ -284,6 +454,17 @@ ll_status ll_linear_w8a8(int M, int N, int K, const int8_t* X, int64_t ldx, cons
   if (K > 0 && (X == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
   if (z_out != nullptr && ldz < N) return LL_ERR_INVALID_ARG;
   if (y_type == LL_GEMV_OUT_I8 && y_scale == nullptr) return LL_ERR_INVALID_ARG;
+  {
+    const int64_t ysz = y_type == LL_GEMV_OUT_I8 ? 1 : 2;
+    const ll::Extent outs[2] = {{Y, M, N * ysz, ldy * ysz}, {z_out, M, N * 4, ldz * 4}};
+    const ll::Extent ins[5] = {{K > 0 ? X : nullptr, M, K, ldx},
+                               {x_scale, 1, int64_t(M) * 4, int64_t(M) * 4},
+                               {K > 0 ? W : nullptr, N, K, ldw},
+                               {w_scale, 1, int64_t(N) * 4, int64_t(N) * 4},
+                               {bias, 1, int64_t(N) * 4, int64_t(N) * 4}};
+    const ll::Extent ys{y_type == LL_GEMV_OUT_I8 ? y_scale : nullptr, 1, 4, 4};
+    if (ll::outputs_overlap(outs, 2, ins, 5) || ll::outputs_overlap(outs, 2, &ys, 1)) return LL_ERR_INVALID_ARG;
+  }
   ll::LaunchCtx ctx;
   ll_status st = current_ctx(stream, ctx);
   if (st != LL_OK) return st;
@@ -299,6 +480,15 @@ ll_status ll_linear_w8a16(int M, int N, int K, const void* X, int64_t ldx, const
   if (M == 0 || N == 0) return LL_OK;
   if (w_scale == nullptr || Y == nullptr || ldy < N || ldw < K || ldx < K) return LL_ERR_INVALID_ARG;
   if (K > 0 && (X == nullptr || W == nullptr)) return LL_ERR_INVALID_ARG;
+  {
+    const int64_t ysz = y_type == LL_OUT_F32 ? 4 : 2;
+    const ll::Extent out{Y, M, N * ysz, ldy * ysz};
+    const ll::Extent ins[4] = {{K > 0 ? X : nullptr, M, int64_t(K) * 2, ldx * 2},
+                               {K > 0 ? W : nullptr, N, K, ldw},
+                               {w_scale, 1, int64_t(N) * 4, int64_t(N) * 4},
+                               {bias, 1, int64_t(N) * 4, int64_t(N) * 4}};
+    if (ll::outputs_overlap(&out, 1, ins, 4)) return LL_ERR_INVALID_ARG;
+  }
   ll::LaunchCtx ctx;
   ll_status st = current_ctx(stream, ctx);
   if (st != LL_OK) return st;
@@ -310,6 +500,11 @@ ll_status ll_quantize_per_token_f16(int M, int K, const void* x, int64_t ldx, in
   if (M < 0 || K < 0 || ldx < K || ldq < K) return LL_ERR_INVALID_ARG;
   if (M == 0) return LL_OK;
   if (scale == nullptr || (K > 0 && (x == nullptr || q == nullptr))) return LL_ERR_INVALID_ARG;
+  {
+    const ll::Extent outs[2] = {{K > 0 ? q : nullptr, M, K, ldq}, {scale, 1, int64_t(M) * 4, int64_t(M) * 4}};
+    const ll::Extent in{K > 0 ? x : nullptr, M, int64_t(K) * 2, ldx * 2};
+    if (ll::outputs_overlap(outs, 2, &in, 1)) return LL_ERR_INVALID_ARG;
+  }
   ll::LaunchCtx ctx;
   ll_status st = current_ctx(stream, ctx);
   if (st != LL_OK) return st;

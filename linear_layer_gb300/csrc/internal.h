@@ -14,6 +14,8 @@ struct LaunchCtx {
   uint32_t* status;     // device status word of the current device
   uint64_t timeout_ns;  // limit of one bounded wait
   int num_sms;          // SM count of the current device
+  int device;           // ordinal of the current device
+  unsigned long long context_id;  // unique ID of the current CUDA context (0 if unknown)
 };
 
 struct GemmArgs {
@@ -37,8 +39,45 @@ struct GemmArgs {
 };
 
 // Launch context of the current device (status word, SM count, wait limit) for `stream`;
-// LL_ERR_NO_DEVICE unless an sm_103 device is current (abi.cu).
+// LL_ERR_NO_DEVICE unless an sm_103 device is current (abi.cu).  Device addresses of the
+// library's own __device__ variables are looked up again whenever the current CUDA
+// context differs from the one they were found in (a context made current through the
+// driver API, or a new primary context after a device reset).
 ll_status current_launch_ctx(ll_stream_t stream, LaunchCtx& ctx);
+
+// A matrix as a set of byte ranges: `rows` rows of `width` bytes, `pitch` bytes apart
+// (pitch >= width), from `base`.  A NULL base or an empty shape is an empty set.
+struct Extent {
+  const void* base;
+  int64_t rows, width, pitch;
+};
+
+// True when two extents may share a byte.  Exact when the extents have the same pitch
+// (or one of them is a single row); otherwise any intersection of their first-to-last
+// byte spans counts as shared.
+bool extents_overlap(const Extent& x, const Extent& y);
+
+// True when an output extent shares a byte with another output or with an input.
+bool outputs_overlap(const Extent* outs, int n_out, const Extent* ins, int n_in);
+
+// Host-side checks of a GEMM request that need no device (sizes, types, pitches,
+// pointers, alignment, aliasing; the workspace only enters through ws/ws_bytes and is
+// checked against the operands when it will be written).  LL_OK or the error to return.
+ll_status validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes);
+
+// Where the operand repack of a GEMM puts A and B: A (when repacked) at the 256-byte-
+// aligned start of the scratch, B after it.  a_bytes = roundup(M * lda_p * esize, 256)
+// and b_bytes = K * ldb_p * esize with the pitches rounded up to 16 bytes.
+struct RepackPlan {
+  bool a, b;
+  int64_t lda_p, ldb_p;  // elements
+  size_t a_bytes, b_bytes;
+};
+RepackPlan plan_repack(const GemmArgs& a);
+
+// Repack per `plan` into `scratch` (256-byte aligned, at least a_bytes + b_bytes), then
+// launch the GEMM on the repacked operands.  `scratch` may be NULL when nothing is repacked.
+ll_status launch_gemm_planned(GemmArgs a, const RepackPlan& plan, void* scratch, const LaunchCtx& ctx);
 
 // tcgen05 GEMM (gemm_tc.cu).  Requires A, B 16-byte aligned with 16-byte-multiple pitches.
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx);

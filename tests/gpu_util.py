@@ -1,4 +1,5 @@
-"""Helpers shared by the GPU parity tests: device upload and the tolerance bar.
+"""Helpers shared by the GPU parity tests: device upload, the tolerance bar, and the
+all-rows check of full-size results.
 
 Tolerance (floating point): each element satisfies, before the output cast,
     |D - D_ref| <= 1e-2 * sqrt(K / 256) * (|A||B|)_ij + 1e-6
@@ -55,3 +56,41 @@ def check_close(D, ref, absab, K, out, in_kind, what=""):
         rel = np.linalg.norm(D - ref) / nref
         bar = FROB[in_kind] + U_OUT[out] * (1.0 + FROB[in_kind])
         assert rel <= bar, "%s: relative Frobenius error %g > %g" % (what, rel, bar)
+
+
+def check_all_rows(D, oracle_rows, M, N, K, out, in_kind, what="", chunk=512):
+    """Compare every element of D[:M, :N] with the oracle, `chunk` rows at a time
+    (oracle_rows(rows) -> (ref, absab) for those rows), at the per-element bound of
+    check_close; the relative Frobenius bar is applied to the whole matrix."""
+    D = np.asarray(D)
+    num = 0.0
+    den = 0.0
+    for r0 in range(0, M, chunk):
+        rows = np.arange(r0, min(M, r0 + chunk), dtype=np.int32)
+        ref, absab = oracle_rows(rows)
+        Dc = D[rows, :N].astype(np.float64)
+        bound = 1e-2 * np.sqrt(max(K, 1) / 256.0) * absab + 1e-6 + U_OUT[out] * np.abs(ref)
+        err = np.abs(Dc - ref)
+        bad = ~(err <= bound)
+        if bad.any():
+            idx = np.argwhere(bad)[:5]
+            i, j = idx[0]
+            raise AssertionError("%s: %d elements outside tolerance in rows %d..%d, e.g. (%d, %d): got %s "
+                                 "want %s bound %s" % (what, int(bad.sum()), r0, rows[-1], r0 + i, j, Dc[i, j],
+                                                       ref[i, j], bound[i, j]))
+        num += float(np.sum((Dc - ref) ** 2))
+        den += float(np.sum(ref ** 2))
+    if den > 0:
+        rel = np.sqrt(num / den)
+        bar = FROB[in_kind] + U_OUT[out] * (1.0 + FROB[in_kind])
+        assert rel <= bar, "%s: relative Frobenius error %g > %g" % (what, rel, bar)
+
+
+def assert_fully_written(tD, M, N, what=""):
+    """D was pre-filled with NaN and the inputs are finite: every element of D[:M, :N] must
+    have been written (a skipped tile would leave NaN)."""
+    import torch
+    nan = torch.isnan(tD[:M, :N].float())
+    if bool(nan.any()):
+        idx = torch.nonzero(nan)[:5].tolist()
+        raise AssertionError("%s: %d elements of D never written, e.g. %s" % (what, int(nan.sum()), idx))

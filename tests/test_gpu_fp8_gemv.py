@@ -1,11 +1,11 @@
-"""GPU parity of the FP8 block-scaled GEMM (tolerance bar) and of the W8A8 GEMV
-(bit-exact z and y) against the CPU oracle, through the C ABI."""
+"""GPU parity of the FP8 block-scaled GEMM (tolerance bar; the full-size workload on every
+element) and of the W8A8 GEMV (bit-exact z and y) against the CPU oracle, through the C ABI."""
 import numpy as np
 import pytest
 import torch
 
 import workloads as wl
-from gpu_util import check_close, out_code, out_tensor, up
+from gpu_util import assert_fully_written, check_all_rows, check_close, out_code, out_tensor, up
 
 pytestmark = pytest.mark.gpu
 
@@ -24,13 +24,19 @@ def run_fp8(orc, M, N, K, alpha=1.0, beta=0.0, out="bf16", pad=0, rows=None, see
                             up(C), ldc, tD, ldd, out_code(out), workspace=ws)
     st, word = ll.get_device_status()
     assert st == ll.LL_OK, "device status %s (word %#x)" % (ll.status_string(st), word)
-    D = tD.float().cpu().numpy().astype(np.float64)
-    if rows is None:
-        rows = np.arange(M)
-    ref, absab = orc.gemm_fp8_blockscaled(M, N, K, alpha, A.ravel(), lda, sA.ravel(), KB, B.ravel(),
-                                          ldb, sB.ravel(), NB, beta,
-                                          None if C is None else C.ravel(), ldc, rows=rows)
-    check_close(D[rows], ref, absab, K, out, "e4m3", what="fp8 %dx%dx%d" % (M, N, K))
+    what = "fp8 %dx%dx%d" % (M, N, K)
+    assert_fully_written(tD, M, N, what)
+    D = tD.float().cpu().numpy()
+    Cf = None if C is None else C.ravel()
+
+    def oracle_rows(r):
+        return orc.gemm_fp8_blockscaled(M, N, K, alpha, A.ravel(), lda, sA.ravel(), KB, B.ravel(), ldb,
+                                        sB.ravel(), NB, beta, Cf, ldc, rows=r)
+    if rows is None:  # every element, a chunk of rows at a time
+        check_all_rows(D, oracle_rows, M, N, K, out, "e4m3", what)
+    else:
+        ref, absab = oracle_rows(rows)
+        check_close(D[rows].astype(np.float64), ref, absab, K, out, "e4m3", what=what)
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (200, 300, 389), (1, 1, 1), (257, 513, 640),
@@ -60,18 +66,13 @@ def test_fp8_wide_tiles(orc, M, N, K, alpha, beta, out):
     """Sizes that run 128 x 256 tiles: an odd number of 128-row blocks, more and fewer
     tiles than SMs, K tails, an N tail inside a 128-column block, and a last column block
     whose second half lies wholly past N."""
-    rng = np.random.default_rng(M)
-    last = (M - 1) // 128 * 128
-    rows = np.array(sorted({0, 127, 128, 255, last - 1, last, M - 1} | set(int(r) for r in rng.integers(0, M, 6))))
-    run_fp8(orc, M, N, K, alpha, beta, out, rows=rows)
+    run_fp8(orc, M, N, K, alpha, beta, out)
 
 
-def test_fp8_8192_full_size_sampled(orc):
+def test_fp8_8192_full_size(orc):
+    """The FP8 workload at full size, every element (about 1.1e12 oracle multiply-adds)."""
     cfg = wl.WORKLOADS["e4m3_gemm_8192"]
-    M = cfg["M"]
-    rng = np.random.default_rng(29)
-    rows = np.array(sorted({0, 127, 128, M // 2, M - 1} | set(int(r) for r in rng.integers(0, M, 5))))
-    run_fp8(orc, M, cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"], cfg["out"], rows=rows)
+    run_fp8(orc, cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"], cfg["out"])
 
 
 # ------------------------------------------------------------------ W8A8 GEMV

@@ -1,16 +1,16 @@
 """GPU parity of the FP16 / BF16 tcgen05 GEMM against the CPU oracle, through the C ABI.
 
-Small cases are compared on every element; the full-size workloads (BF16 4096^3 and
-the ragged FP16 4093 x 5003 x 2056 with tight leading dimensions) on sampled rows
-that cover the first and last rows of tiles and the M tail, in the launch
-configuration the benchmark times.
+Every test compares every element, the full-size workloads included (BF16 4096^3,
+and the ragged FP16 4093 x 5003 x 2056 with tight and with padded leading
+dimensions, in the launch configuration the benchmark times).  D is pre-filled with
+NaN and every test checks that all of D[:M, :N] was written.
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads as wl
-from gpu_util import check_close, out_code, out_tensor, up
+from gpu_util import assert_fully_written, check_all_rows, check_close, out_code, out_tensor, up
 
 pytestmark = pytest.mark.gpu
 
@@ -41,12 +41,16 @@ def run_gemm(orc, kind, M, N, K, alpha, beta, out, lda=None, ldb=None, ldc=None,
     fn(M, N, K, alpha, tA, lda, tB, ldb, beta, tC, ldc, tD, ldd, out_code(out), workspace=ws)
     st, word = ll.get_device_status()
     assert st == ll.LL_OK, "device status %s (word %#x)" % (ll.status_string(st), word)
+    what = "%s %dx%dx%d" % (kind, M, N, K)
+    assert_fully_written(tD, M, N, what)
     D = _dec_out(tD)
-    if rows is None:
-        rows = np.arange(M)
-    ref, absab = orc.gemm(kind, M, N, K, alpha, A.ravel(), lda, B.ravel(), ldb, beta,
-                          None if C is None else C.ravel(), ldc, rows=rows)
-    check_close(D[rows, :N], ref, absab, K, out, kind, what="%s %dx%dx%d" % (kind, M, N, K))
+    Cf = None if C is None else C.ravel()
+    if rows is None:  # every element, a chunk of rows at a time
+        check_all_rows(D, lambda r: orc.gemm(kind, M, N, K, alpha, A.ravel(), lda, B.ravel(), ldb, beta, Cf,
+                                             ldc, rows=r), M, N, K, out, kind, what)
+    else:
+        ref, absab = orc.gemm(kind, M, N, K, alpha, A.ravel(), lda, B.ravel(), ldb, beta, Cf, ldc, rows=rows)
+        check_close(D[rows, :N], ref, absab, K, out, kind, what=what)
     if ldd > N:  # padding columns of D are never written
         assert torch.isnan(tD[:, N:].float()).all()
     return D
@@ -75,7 +79,7 @@ def test_many_tiles_every_path(orc):
     # one-CTA 128 x 64 tiles, CTA-pair halves only (at most half a wave of pair tiles),
     # whole pair tiles, and an M of 128 (one-CTA kernel although it has 24 pair tiles)
     for (M, N) in [(256, 256), (1280, 1280), (2048, 1280), (4096, 2304), (128, 6144)]:
-        run_gemm(orc, "f16", M, N, 128, 1.0, 0.0, "f32", rows=sorted({0, 127, min(128, M - 1), M - 1}))
+        run_gemm(orc, "f16", M, N, 128, 1.0, 0.0, "f32")
 
 
 def test_padded_leading_dims(orc):
@@ -140,18 +144,11 @@ def test_invalid_args_rejected_before_launch():
     ll.gemm_f16(4, 0, 4, 1.0, t, 4, t, 4, 0.0, None, 4, D, 4, ll.OUT_F32)
 
 
-def _sample_rows(M, extra, seed):
-    rng = np.random.default_rng(seed)
-    base = {0, 1, 127, 128, 255, 256, M // 2, M - 2, M - 1}
-    base |= set(int(r) for r in rng.integers(0, M, extra))
-    return np.array(sorted(r for r in base if 0 <= r < M))
-
-
-def test_bf16_4096_full_size_sampled(orc):
+def test_bf16_4096_full_size(orc):
+    """The headline workload at full size, every element."""
     cfg = wl.WORKLOADS["bf16_gemm_4096"]
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
-    run_gemm(orc, "bf16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"],
-             rows=_sample_rows(M, 12, 17))
+    run_gemm(orc, "bf16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"])
 
 
 def test_bf16_4096_fp32_output_strict_bar(orc):
@@ -159,21 +156,21 @@ def test_bf16_4096_fp32_output_strict_bar(orc):
     # applies to the accumulator before any cast, with no allowance for it
     cfg = wl.WORKLOADS["bf16_gemm_4096"]
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
-    run_gemm(orc, "bf16", M, N, K, cfg["alpha"], cfg["beta"], "f32", rows=_sample_rows(M, 6, 31))
+    run_gemm(orc, "bf16", M, N, K, cfg["alpha"], cfg["beta"], "f32")
 
 
-def test_f16_ragged_tight_lds_full_size_sampled(orc):
+def test_f16_ragged_tight_lds_full_size(orc):
+    """The ragged workload with tight leading dimensions (B repacked), every element."""
     cfg = wl.WORKLOADS["f16_gemm_4093x5003x2056"]
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
-    run_gemm(orc, "f16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"],
-             rows=_sample_rows(M, 12, 19))
+    run_gemm(orc, "f16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"])
 
 
-def test_f16_ragged_padded_lds_sampled(orc):
+def test_f16_ragged_padded_lds_full_size(orc):
     cfg = wl.WORKLOADS["f16_gemm_4093x5003x2056"]
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     run_gemm(orc, "f16", M, N, K, cfg["alpha"], cfg["beta"], cfg["out"], lda=2064, ldb=5008,
-             ldc=5008, ldd=5008, rows=_sample_rows(M, 6, 23))
+             ldc=5008, ldd=5008)
 
 
 def _shifted(t, shift, fill=0.0):
@@ -213,7 +210,7 @@ def test_pair_several_units_per_cta(orc, ld_pad, out):
     per lane) and odd pitches (transposed through shared memory)."""
     M, N, K = 4096, 2560, 64
     ld = N + ld_pad
-    run_gemm(orc, "bf16", M, N, K, 0.75, -1.5, out, ldc=ld, ldd=ld, rows=_sample_rows(M, 10, 37))
+    run_gemm(orc, "bf16", M, N, K, 0.75, -1.5, out, ldc=ld, ldd=ld)
 
 
 @pytest.mark.parametrize("ld_pad", [0, 1])
@@ -227,10 +224,9 @@ def test_pair_in_place_c_equals_d(orc, ld_pad):
     C = wl.f32_normal(M, N, 53, ld=ld)
     tC = up(C)
     ll.gemm_bf16(M, N, K, 1.0, up(A), K, up(B), N, -0.5, tC, ld, tC, ld, ll.OUT_F32)
-    rows = _sample_rows(M, 8, 41)
-    ref, absab = orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, -0.5, C.ravel(), ld,
-                          rows=rows)
-    check_close(tC.cpu().numpy()[rows, :N], ref, absab, K, "f32", "bf16", "pair in place")
+    assert_fully_written(tC, M, N, "pair in place")
+    check_all_rows(tC.cpu().numpy(), lambda r: orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, -0.5,
+                                                        C.ravel(), ld, rows=r), M, N, K, "f32", "bf16", "pair in place")
 
 
 @pytest.mark.parametrize("ld_pad", [0, 8, 3])
@@ -255,10 +251,9 @@ def test_pair_writes_nothing_outside_d(orc, ld_pad, out):
     assert np.isnan(D[M:]).all(), "rows past M were written"
     if ldd > N:
         assert np.isnan(D[:M, N:]).all(), "padding columns were written"
-    rows = _sample_rows(M, 6, 43)
-    ref, absab = orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, 0.5, C.ravel(), ldd,
-                          rows=rows)
-    check_close(D[rows, :N].astype(np.float64), ref, absab, K, out, "bf16", "guarded D")
+    assert_fully_written(tD, M, N, "guarded D")
+    check_all_rows(D, lambda r: orc.gemm("bf16", M, N, K, 1.0, A.ravel(), K, B.ravel(), N, 0.5, C.ravel(), ldd,
+                                         rows=r), M, N, K, out, "bf16", "guarded D")
 
 
 @pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
@@ -266,7 +261,7 @@ def test_pair_beta_zero_every_output(orc, out):
     """beta = 0 on CTA pairs (C is not read; the TMA epilogue only stages D), FP16
     inputs, several units per pair with half tiles, an M tail inside a chunk."""
     M, N, K = 4000, 2560, 96
-    run_gemm(orc, "f16", M, N, K, -1.25, 0.0, out, rows=_sample_rows(M, 8, 47))
+    run_gemm(orc, "f16", M, N, K, -1.25, 0.0, out)
 
 
 def test_c_d_must_be_element_aligned():

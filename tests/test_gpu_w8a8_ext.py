@@ -106,3 +106,38 @@ def test_ex_rejects_bad_arguments():
         ll.linear_w8a8_gemv_ex(4, 16, t8, f, t8, 16, f, None, ll.GEMV_OUT_I8, None, t8)  # no y_scale
     with pytest.raises(ll.LLError):
         ll.quantize_per_token_f16(2, 16, f, 8, t8, 16, f)  # ldx < K
+
+
+def test_int8_layer_output_as_next_weights_under_the_ordering_rule(orc):
+    """The ordering rule for weights (programmatic dependent launch): a W8A8 layer reads W
+    before it waits for the work before it, so W may not be an output of a library call
+    that could still be running.  Here the INT8 output of ll_linear_w8a8 becomes the
+    weight matrix of the next GEMV, with a kernel that does not come from the library
+    in between, as the rule asks; the GEMV must see the finished matrix, bit for bit,
+    and the result must equal the same GEMV on a copy that was synchronised first."""
+    import linear_layer_gb300 as ll
+    M, N, K = 48, 4096, 1024                 # producer: 48 tokens x 4096 channels, K 1024
+    X, sx, W, sW = wl.batch_w8a8_inputs(M, N, K)
+    s_y = np.float32(0.5)
+    _, Yq_ref = orc.linear_w8a8(M, N, K, X, K, sx, W, K, sW, out_int8=True, s_y=s_y)
+    x2 = wl.int8_uniform((N,), 77)            # consumer: W' = Y (48 x 4096), x' of 4096
+    s_w2 = wl.scales_uniform(M, 78)
+    z_ref, y_ref = orc.gemv_w8a8(M, N, x2, np.float32(0.01), Yq_ref, N, s_w2)
+    stream = torch.cuda.Stream()
+    tX, tsx, tW, tsW = up(X), up(sx), up(W), up(sW)
+    tsy = torch.tensor([s_y], device="cuda")
+    tx2, tsx2, tsw2 = up(x2), torch.tensor([0.01], dtype=torch.float32, device="cuda"), up(s_w2)
+    other = torch.zeros(1 << 20, device="cuda")
+    for rep in range(3):
+        Y = torch.full((M, N), 99, dtype=torch.int8, device="cuda")
+        y = torch.full((M,), float("nan"), dtype=torch.float16, device="cuda")
+        z = torch.zeros(M, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        ll.linear_w8a8(M, N, K, tX, K, tsx, tW, K, tsW, None, ll.GEMV_OUT_I8, tsy, Y, N, stream=stream)
+        with torch.cuda.stream(stream):
+            other.add_(1.0)                   # a kernel that does not come from this library
+        ll.linear_w8a8_gemv(M, N, tx2, tsx2, Y, N, tsw2, y, z, stream=stream)
+        stream.synchronize()
+        assert np.array_equal(Y.cpu().numpy(), Yq_ref), rep
+        assert np.array_equal(z.cpu().numpy().astype(np.int64), z_ref), rep
+        assert np.array_equal(y.cpu().numpy().view(np.uint16), y_ref.view(np.uint16)), rep
