@@ -17,6 +17,10 @@ Functions and the passages they follow:
   factors per tensor, row or block; 1x128 blocks of A, 128x128 blocks of B.
 * ``decode_e5m2`` / ``gemm_f8_blockscaled_mixed`` -- "Tensor Core" chapter, table
   "精度": FP8 E5M2 1/5/2 (wider range, used for gradients) beside E4M3.
+* ``decode_ue8m0`` / ``gemm_mx_f8`` -- "Tensor Core" chapter, the table of formats per
+  generation (Blackwell: block-scaled formats such as MXFP4 / NVFP4): OCP microscaling,
+  one E8M0 scale 2^(e-127) shared by 32 consecutive K elements of a row of A or a
+  column of B (the pages name the formats only).
 * ``gemv_w8a8`` -- "NVIDIA A100: chip to SIMT", sections 5.1-5.2: int8 x int8
   summed exactly, then y = fp16(float(z) * s_x * s_W[o]).
 * ``quantize_per_token_f16`` -- same page, 5.1: the activation is quantised per token
@@ -47,6 +51,8 @@ def lib():
         L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
         L.orc_decode_e5m2.restype = ctypes.c_double
         L.orc_decode_e5m2.argtypes = [ctypes.c_uint8]
+        L.orc_decode_ue8m0.restype = ctypes.c_double
+        L.orc_decode_ue8m0.argtypes = [ctypes.c_uint8]
         L.orc_encode_f16_rn.restype = ctypes.c_uint16
         L.orc_encode_f16_rn.argtypes = [ctypes.c_double]
         vp = ctypes.c_void_p
@@ -63,6 +69,10 @@ def lib():
         L.orc_gemm_f8_blockscaled_mixed.restype = ctypes.c_int
         L.orc_gemm_f8_blockscaled_mixed.argtypes = [ctypes.c_int, ctypes.c_int] + \
             L.orc_gemm_fp8_blockscaled.argtypes
+        L.orc_gemm_mx_f8.restype = ctypes.c_int
+        L.orc_gemm_mx_f8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_double, vp, i64, vp, i64, vp, i64, vp, i64, ctypes.c_double, vp,
+                                     i64, vp, ctypes.c_int, vp, vp]
         L.orc_quantize_per_token_f16.restype = ctypes.c_int
         L.orc_quantize_per_token_f16.argtypes = [ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp]
         L.orc_gemv_w8a8_ex.restype = ctypes.c_int
@@ -100,6 +110,10 @@ def decode_e4m3(bits: int) -> float:
 
 def decode_e5m2(bits: int) -> float:
     return lib().orc_decode_e5m2(int(bits) & 0xFF)
+
+
+def decode_ue8m0(bits: int) -> float:
+    return lib().orc_decode_ue8m0(int(bits) & 0xFF)
 
 
 def encode_f16_rn(v: float) -> int:
@@ -171,6 +185,27 @@ def gemm_f8_blockscaled_mixed(a_fmt, b_fmt, M, N, K, alpha, A, lda, sA, ld_sa, B
                                              _ptr(D), _ptr(S))
     if rc != 0:
         raise ValueError("orc_gemm_f8_blockscaled_mixed failed with code %d" % rc)
+    return D, S
+
+
+def gemm_mx_f8(a_fmt, b_fmt, M, N, K, alpha, A, lda, SA, ld_sa, B, ldb, SB, ld_sb, beta=0.0, C=None, ldc=0,
+               rows=None, want_absab=True):
+    """MX block-scaled 8-bit GEMM: element formats "e4m3" / "e5m2", E8M0 scale codes SA
+    (M x ld_sa, one per row and 32-wide K block) and SB (ceil(K/32) x ld_sb, one per column
+    and K block).  Returns (D double [len(rows), N], absab)."""
+    rows = _rows(M, rows)
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    SA = np.ascontiguousarray(SA, dtype=np.uint8)
+    SB = np.ascontiguousarray(SB, dtype=np.uint8)
+    C = None if C is None else np.ascontiguousarray(C, dtype=np.float32)
+    D = np.zeros((len(rows), N), dtype=np.float64)
+    S = np.zeros((len(rows), N), dtype=np.float64) if want_absab else None
+    rc = lib().orc_gemm_mx_f8(F8[a_fmt], F8[b_fmt], M, N, K, float(alpha), _ptr(A), lda, _ptr(SA), ld_sa,
+                              _ptr(B), ldb, _ptr(SB), ld_sb, float(beta), _ptr(C), ldc, _ptr(rows), len(rows),
+                              _ptr(D), _ptr(S))
+    if rc != 0:
+        raise ValueError("orc_gemm_mx_f8 failed with code %d" % rc)
     return D, S
 
 

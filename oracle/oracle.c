@@ -257,6 +257,71 @@ int orc_gemm_f8_blockscaled_mixed(int a_fmt, int b_fmt, int M, int N, int K, dou
   return 0;
 }
 
+/* ------------------------------------------------------------------ MX block-scaled GEMM */
+
+/*
+ * OCP microscaling (MX) shared scale E8M0: an 8-bit biased exponent with no sign and no
+ * mantissa, X = 2^(e - 127) for e = 0..254; the code 255 is NaN.  ("Tensor Core"
+ * chapter, table of tensor-core formats per generation: Blackwell adds block-scaled
+ * formats such as MXFP4 / NVFP4; the pages name the formats only.)
+ */
+double orc_decode_ue8m0(uint8_t e) {
+  if (e == 255) return NAN;
+  return ldexp(1.0, (int)e - 127);
+}
+
+/*
+ * MX block-scaled 8-bit GEMM: every 32 consecutive elements along K of a row of A, and
+ * of a column of B, share one E8M0 scale:
+ *   D_ref[i][j] = alpha * sum_k (XA[i][k/32] * dec(A[i][k])) * (XB[k/32][j] * dec(B[k][j]))
+ *                 + beta * C[i][j]
+ * A row-major M x K (lda), element format a_fmt (0 = E4M3, 1 = E5M2); B row-major K x N
+ * (ldb), format b_fmt; SA E8M0 codes M x ceil(K/32) (ld_sa), one per row and 32-wide K
+ * block; SB E8M0 codes ceil(K/32) x N (ld_sb), one per column and 32-wide K block (a
+ * last block shorter than 32 keeps its scale).  Scaled elements are exact in double and
+ * every sum is a plain double loop.  absab[i][j] = sum_k |scaled a| * |scaled b|.
+ */
+int orc_gemm_mx_f8(int a_fmt, int b_fmt, int M, int N, int K, double alpha, const uint8_t* A, int64_t lda,
+                   const uint8_t* SA, int64_t ld_sa, const uint8_t* B, int64_t ldb, const uint8_t* SB,
+                   int64_t ld_sb, double beta, const float* C, int64_t ldc, const int32_t* rows, int nrows,
+                   double* D_ref, double* absab) {
+  if (M < 0 || N < 0 || K < 0 || nrows < 0) return 1;
+  for (int r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= M) return 2;
+  if (beta != 0.0 && C == NULL) return 3;
+  /* B scaled once: Bs[k][j] = XB[k/32][j] * dec(B[k][j]) */
+  double* Bs = (double*)malloc(sizeof(double) * ((size_t)K * (size_t)N + 1));
+  if (!Bs) return 4;
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t j = 0; j < N; ++j)
+      Bs[k * N + j] = orc_decode_ue8m0(SB[(k / 32) * ld_sb + j]) * decode_f8(b_fmt, B[k * ldb + j]);
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    const int64_t i = rows[r];
+    double* acc = (double*)calloc((size_t)N + 1, sizeof(double));
+    double* aab = (double*)calloc((size_t)N + 1, sizeof(double));
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = orc_decode_ue8m0(SA[i * ld_sa + k / 32]) * decode_f8(a_fmt, A[i * lda + k]);
+      const double* brow = Bs + k * N;
+      for (int64_t j = 0; j < N; ++j) {
+        acc[j] += a * brow[j];
+        aab[j] += fabs(a) * fabs(brow[j]);
+      }
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      double d = alpha * acc[j];
+      if (beta != 0.0) d += beta * (double)C[i * ldc + j];
+      if (D_ref) D_ref[(int64_t)r * N + j] = d;
+      if (absab) absab[(int64_t)r * N + j] = aab[j];
+    }
+    free(acc);
+    free(aab);
+  }
+  free(Bs);
+  return 0;
+}
+
 /* ------------------------------------------------------------------ W8A8 GEMV */
 
 /*

@@ -196,3 +196,41 @@ def gemv_inputs(N, K, ldw=None):
         W = Wp
     s_W = scales_uniform(N, SEED_SCALE)
     return x, s_x, W, s_W
+
+F8_EMAX = {"e4m3": 8, "e5m2": 15}  # exponent of the largest power of two below the format's maximum
+
+
+def mx_quant(rows, cols, seed, block_axis, ld=None, fmt="e4m3", spread=4):
+    """OCP microscaling (MX) quantisation of seeded N(0, 1) draws, each 32-element block
+    first multiplied by 2^u (u uniform in [-spread, spread]) so the block scales differ:
+    32 consecutive elements along `block_axis` (1: along a row, A's K; 0: down a column,
+    B's K) share the E8M0 code e = clamp(floor(log2(amax)) - emax + 127, 0, 254), and each
+    element is v / 2^(e - 127) rounded to the element format (saturating at its maximum).
+
+    Returns (codes uint8 rows x ld, scale codes uint8: rows x ceil(cols / 32) for
+    block_axis 1, ceil(rows / 32) x cols for block_axis 0)."""
+    ld = cols if ld is None else ld
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal(size=(rows, cols), dtype=np.float32).astype(np.float64)
+    if block_axis == 1:
+        nb = -(-cols // 32)
+        u = rng.integers(-spread, spread + 1, size=(rows, nb))
+        v = v * np.ldexp(1.0, u[:, np.arange(cols) // 32])
+        amax = np.zeros((rows, nb))
+        for b in range(nb):
+            amax[:, b] = np.max(np.abs(v[:, 32 * b:32 * b + 32]), axis=1) if cols else 0
+    else:
+        nb = -(-rows // 32)
+        u = rng.integers(-spread, spread + 1, size=(nb, cols))
+        v = v * np.ldexp(1.0, u[np.arange(rows) // 32, :])
+        amax = np.zeros((nb, cols))
+        for b in range(nb):
+            amax[b, :] = np.max(np.abs(v[32 * b:32 * b + 32, :]), axis=0) if rows else 0
+    with np.errstate(divide="ignore"):
+        x = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - F8_EMAX[fmt], -127)
+    codes_s = np.clip(x + 127, 0, 254).astype(np.uint8)
+    scale = np.ldexp(1.0, codes_s.astype(np.int64) - 127)
+    full = scale[:, np.arange(cols) // 32] if block_axis == 1 else scale[np.arange(rows) // 32, :]
+    q = np.clip(v / full, -F8_MAX[fmt], F8_MAX[fmt]).astype(np.float32)
+    codes = _to_f8_bits(q, fmt)
+    return _pad(codes, ld, NAN_BITS["e4m3"], np.uint8), codes_s
