@@ -20,7 +20,8 @@ Functions and the passages they follow:
 * ``decode_ue8m0`` / ``gemm_mx_f8`` -- "Tensor Core" chapter, the table of formats per
   generation (Blackwell: block-scaled formats such as MXFP4 / NVFP4): OCP microscaling,
   one E8M0 scale 2^(e-127) shared by 32 consecutive K elements of a row of A or a
-  column of B (the pages name the formats only).
+  column of B, scales stored K-block-contiguous per row of A / column of B (the pages
+  name the formats only).
 * ``gemv_w8a8`` -- "NVIDIA A100: chip to SIMT", sections 5.1-5.2: int8 x int8
   summed exactly, then y = fp16(float(z) * s_x * s_W[o]).
 * ``quantize_per_token_f16`` -- same page, 5.1: the activation is quantised per token
@@ -191,7 +192,7 @@ def gemm_f8_blockscaled_mixed(a_fmt, b_fmt, M, N, K, alpha, A, lda, sA, ld_sa, B
 def gemm_mx_f8(a_fmt, b_fmt, M, N, K, alpha, A, lda, SA, ld_sa, B, ldb, SB, ld_sb, beta=0.0, C=None, ldc=0,
                rows=None, want_absab=True):
     """MX block-scaled 8-bit GEMM: element formats "e4m3" / "e5m2", E8M0 scale codes SA
-    (M x ld_sa, one per row and 32-wide K block) and SB (ceil(K/32) x ld_sb, one per column
+    (M x ld_sa, one per row of A and 32-wide K block) and SB (N x ld_sb, one per column of B
     and K block).  Returns (D double [len(rows), N], absab)."""
     rows = _rows(M, rows)
     A = np.ascontiguousarray(A, dtype=np.uint8)

@@ -273,12 +273,12 @@ double orc_decode_ue8m0(uint8_t e) {
 /*
  * MX block-scaled 8-bit GEMM: every 32 consecutive elements along K of a row of A, and
  * of a column of B, share one E8M0 scale:
- *   D_ref[i][j] = alpha * sum_k (XA[i][k/32] * dec(A[i][k])) * (XB[k/32][j] * dec(B[k][j]))
+ *   D_ref[i][j] = alpha * sum_k (XA[i][k/32] * dec(A[i][k])) * (XB[j][k/32] * dec(B[k][j]))
  *                 + beta * C[i][j]
  * A row-major M x K (lda), element format a_fmt (0 = E4M3, 1 = E5M2); B row-major K x N
- * (ldb), format b_fmt; SA E8M0 codes M x ceil(K/32) (ld_sa), one per row and 32-wide K
- * block; SB E8M0 codes ceil(K/32) x N (ld_sb), one per column and 32-wide K block (a
- * last block shorter than 32 keeps its scale).  Scaled elements are exact in double and
+ * (ldb), format b_fmt; SA E8M0 codes M x ceil(K/32) (ld_sa), one per row of A and 32-wide
+ * K block; SB E8M0 codes N x ceil(K/32) (ld_sb), one per column of B and 32-wide K block
+ * (a last block shorter than 32 keeps its scale).  Scaled elements are exact in double and
  * every sum is a plain double loop.  absab[i][j] = sum_k |scaled a| * |scaled b|.
  */
 int orc_gemm_mx_f8(int a_fmt, int b_fmt, int M, int N, int K, double alpha, const uint8_t* A, int64_t lda,
@@ -294,7 +294,7 @@ int orc_gemm_mx_f8(int a_fmt, int b_fmt, int M, int N, int K, double alpha, cons
   if (!Bs) return 4;
   for (int64_t k = 0; k < K; ++k)
     for (int64_t j = 0; j < N; ++j)
-      Bs[k * N + j] = orc_decode_ue8m0(SB[(k / 32) * ld_sb + j]) * decode_f8(b_fmt, B[k * ldb + j]);
+      Bs[k * N + j] = orc_decode_ue8m0(SB[j * ld_sb + k / 32]) * decode_f8(b_fmt, B[k * ldb + j]);
 
 #pragma omp parallel for schedule(dynamic, 1)
   for (int r = 0; r < nrows; ++r) {

@@ -3,6 +3,7 @@ formats per generation: Blackwell adds block-scaled formats such as MXFP4 / NVFP
 as OCP microscaling: one E8M0 scale 2^(e-127) per 32 consecutive K elements of a row of A
 or a column of B).
 
+Scales are stored K-block-contiguous: SA[i][kb] per row of A, SB[j][kb] per column of B.
 The E8M0 decoder is checked on all 256 codes against ldexp; unit scales reduce the GEMM
 to the plain 8-bit GEMM (checked against the separate block-scaled oracle function with
 unit FP32 scales, and against numpy on torch-decoded codes); a power of two per row and
@@ -28,7 +29,7 @@ def _scaled(A, SA, B, SB, M, N, K, a_fmt, b_fmt):
     """Operands with their block scales applied, from torch's decoders and numpy."""
     kb = np.arange(K) // 32
     Ad = _dec(A[:, :K], a_fmt) * np.ldexp(1.0, SA[:, kb].astype(np.int64) - 127)
-    Bd = _dec(B[:, :N], b_fmt) * np.ldexp(1.0, SB[kb][:, :N].astype(np.int64) - 127)
+    Bd = _dec(B[:, :N], b_fmt) * np.ldexp(1.0, SB[:N, kb].T.astype(np.int64) - 127)
     return Ad, Bd
 
 
@@ -47,9 +48,9 @@ def test_unit_scales_reduce_to_the_plain_8bit_gemm(orc):
         B, _ = wl.mx_quant(K, N, 12, 0, fmt=b_fmt)
         KB = -(-K // 32)
         SA = np.full((M, KB), 127, np.uint8)
-        SB = np.full((KB, N), 127, np.uint8)
+        SB = np.full((N, KB), 127, np.uint8)
         D, _ = orc.gemm_mx_f8(a_fmt, b_fmt, M, N, K, 1.0, A.ravel(), K, SA.ravel(), KB, B.ravel(), N,
-                              SB.ravel(), N)
+                              SB.ravel(), KB)
         # the separate FP8 block-scaled oracle function with unit FP32 scales
         kb128, nb128 = -(-K // 128), -(-N // 128)
         D2, _ = orc.gemm_f8_blockscaled_mixed(a_fmt, b_fmt, M, N, K, 1.0, A.ravel(), K,
@@ -66,15 +67,15 @@ def test_power_of_two_row_and_column_scales_are_exact(orc):
     B, _ = wl.mx_quant(K, N, 22, 0)
     KB = K // 32
     ones_a = np.full((M, KB), 127, np.uint8)
-    ones_b = np.full((KB, N), 127, np.uint8)
+    ones_b = np.full((N, KB), 127, np.uint8)
     D1, _ = orc.gemm_mx_f8("e4m3", "e4m3", M, N, K, 1.0, A.ravel(), K, ones_a.ravel(), KB, B.ravel(), N,
-                           ones_b.ravel(), N)
+                           ones_b.ravel(), KB)
     t = np.arange(M) % 7 - 3          # 2^t per row of A (same for every K block)
     u = np.arange(N) % 5 - 2          # 2^u per column of B
     SA = np.repeat((127 + t)[:, None], KB, axis=1).astype(np.uint8)
-    SB = np.repeat((127 + u)[None, :], KB, axis=0).astype(np.uint8)
+    SB = np.repeat((127 + u)[:, None], KB, axis=1).astype(np.uint8)
     D2, _ = orc.gemm_mx_f8("e4m3", "e4m3", M, N, K, 1.0, A.ravel(), K, SA.ravel(), KB, B.ravel(), N,
-                           SB.ravel(), N)
+                           SB.ravel(), KB)
     np.testing.assert_array_equal(D2, D1 * np.ldexp(1.0, t[:, None] + u[None, :]))
 
 
@@ -88,11 +89,11 @@ def test_random_block_scales_ragged_tails_against_numpy(orc):
         # pad the scale matrices too, with codes that would be wrong if read
         SAp = np.full((M, KB + 2), 200, np.uint8)
         SAp[:, :KB] = SA
-        SBp = np.full((KB, N + 3), 200, np.uint8)
-        SBp[:, :N] = SB
+        SBp = np.full((N, KB + 3), 200, np.uint8)
+        SBp[:, :KB] = SB
         C = wl.f32_normal(M, N, seed + 200)
         D, absab = orc.gemm_mx_f8(a_fmt, b_fmt, M, N, K, 0.75, A.ravel(), K + pad, SAp.ravel(), KB + 2,
-                                  B.ravel(), N + pad, SBp.ravel(), N + 3, -1.5, C.ravel(), N)
+                                  B.ravel(), N + pad, SBp.ravel(), KB + 3, -1.5, C.ravel(), N)
         Ad, Bd = _scaled(A, SA, B, SB, M, N, K, a_fmt, b_fmt)
         ref = 0.75 * (Ad @ Bd) - 1.5 * C.astype(np.float64)
         scale = np.abs(Ad) @ np.abs(Bd)
@@ -101,8 +102,8 @@ def test_random_block_scales_ragged_tails_against_numpy(orc):
         # the scales vary along K and across rows / columns, so a scale taken from the wrong
         # block, row or column would change the result
         if KB > 1:
-            assert (SA != SA[:, :1]).any() and (SB != SB[:1, :]).any()
-        assert (SA != SA[:1, :]).any() and (SB != SB[:, :1]).any()
+            assert (SA != SA[:, :1]).any() and (SB != SB[:, :1]).any()
+        assert (SA != SA[:1, :]).any() and (SB != SB[:1, :]).any()
 
 
 def test_small_case_exact_rationals(orc):
@@ -111,13 +112,13 @@ def test_small_case_exact_rationals(orc):
     B, SB = wl.mx_quant(K, N, 42, 0)
     KB = SA.shape[1]
     D, _ = orc.gemm_mx_f8("e4m3", "e4m3", M, N, K, 1.0, A.ravel(), K, SA.ravel(), KB, B.ravel(), N,
-                          SB.ravel(), N)
+                          SB.ravel(), KB)
     Ad = _dec(A, "e4m3")
     Bd = _dec(B, "e4m3")
     for i in range(M):
         for j in range(N):
             exact = sum(Fraction(Ad[i, k]) * Fraction(2) ** (int(SA[i, k // 32]) - 127) *
-                        Fraction(Bd[k, j]) * Fraction(2) ** (int(SB[k // 32, j]) - 127) for k in range(K))
+                        Fraction(Bd[k, j]) * Fraction(2) ** (int(SB[j, k // 32]) - 127) for k in range(K))
             assert abs(Fraction(D[i, j]) - exact) <= abs(exact) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 200)
 
 

@@ -208,7 +208,8 @@ def mx_quant(rows, cols, seed, block_axis, ld=None, fmt="e4m3", spread=4):
     element is v / 2^(e - 127) rounded to the element format (saturating at its maximum).
 
     Returns (codes uint8 rows x ld, scale codes uint8: rows x ceil(cols / 32) for
-    block_axis 1, ceil(rows / 32) x cols for block_axis 0)."""
+    block_axis 1; for block_axis 0 (B, K x N) cols x ceil(rows / 32), one row of scales per
+    column of B, K blocks contiguous)."""
     ld = cols if ld is None else ld
     rng = np.random.default_rng(seed)
     v = rng.standard_normal(size=(rows, cols), dtype=np.float32).astype(np.float64)
@@ -233,4 +234,6 @@ def mx_quant(rows, cols, seed, block_axis, ld=None, fmt="e4m3", spread=4):
     full = scale[:, np.arange(cols) // 32] if block_axis == 1 else scale[np.arange(rows) // 32, :]
     q = np.clip(v / full, -F8_MAX[fmt], F8_MAX[fmt]).astype(np.float32)
     codes = _to_f8_bits(q, fmt)
+    if block_axis == 0:
+        codes_s = np.ascontiguousarray(codes_s.T)
     return _pad(codes, ld, NAN_BITS["e4m3"], np.uint8), codes_s
