@@ -50,8 +50,12 @@ def gemv_bytes(N, K):
 
 
 KERNEL_SOURCES = {
-    "gemm_tc2_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/ptx.cuh"],
-    "gemm_tc_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/ptx.cuh"],
+    "gemm_mx_kernel": ["linear_layer_gb300/csrc/gemm_mx.cu", "linear_layer_gb300/csrc/gemm_common.cuh",
+                       "linear_layer_gb300/csrc/ptx.cuh"],
+    "gemm_tc2_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/gemm_common.cuh",
+                        "linear_layer_gb300/csrc/ptx.cuh"],
+    "gemm_tc_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/gemm_common.cuh",
+                       "linear_layer_gb300/csrc/ptx.cuh"],
     "gemv_w8a8_kernel": ["linear_layer_gb300/csrc/gemv_w8a8.cu", "linear_layer_gb300/csrc/ptx.cuh"],
 }
 
@@ -659,6 +663,54 @@ def bench_fp8(args, dev, stream, peaks, peak_src):
             "status": ll.status_string(st)}
 
 
+def bench_mx(args, dev, stream, peaks, peak_src):
+    """MX block-scaled FP8 GEMM 8192^3 (E4M3, E8M0 scale per 32 K elements, BF16 out)."""
+    import torch
+
+    import linear_layer_gb300 as ll
+    import workloads as wl
+    cfg = wl.WORKLOADS["mxf8_gemm_8192"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    A, SA = wl.mx_quant(M, K, wl.SEED_A, 1)
+    B, SB = wl.mx_quant(K, N, wl.SEED_B, 0)
+    KB = SA.shape[1]
+    tA, tSA, tB, tSB = _up(A, dev), _up(SA, dev), _up(B, dev), _up(SB, dev)
+    sets = [(tA, tSA, tB, tSB, torch.empty((M, N), dtype=torch.bfloat16, device=dev))]
+    sets.append((tA.clone(), tSA.clone(), tB.clone(), tSB.clone(),
+                 torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+
+    def call(i):
+        a, sa, b, sb, d = sets[i % 2]
+        ll.gemm_mxf8(ll.IN_E4M3, ll.IN_E4M3, M, N, K, 1.0, a, K, sa, KB, b, N, sb, KB, 0.0, None, N, d, N,
+                     ll.OUT_BF16, stream=stream)
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize(dev)
+    steps = max(10, min(args.steps // 10, 100))
+    group_ms = []
+    for _ in range(5):  # median of 5 groups of back-to-back launches
+        total_ms, _ = time_events(call, steps, stream, per_call=False)
+        group_ms.append(total_ms / steps)
+    ms = statistics.median(group_ms)
+    st, _ = ll.get_device_status(stream)
+    flops = gemm_flops(M, N, K)
+    tflops = flops / (ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    return {"metric": "MX block-scaled FP8 GEMM TFLOPS", "value": round(tflops, 1), "unit": "TFLOPS",
+            "ms_per_launch": round(ms, 4),
+            "ms_per_launch_min_max": [round(min(group_ms), 4), round(max(group_ms), 4)],
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "traffic": measured_traffic("mxf8_gemm_8192", "gemm_mx_kernel"),
+                         "kernel": "gemm_mx_kernel<0> (one CTA per 128 x 256 tile, hardware block scaling)",
+                         "peak_source": "%s bf16_tflops x %g (nominal FP8:BF16)" % (peak_src, FP8_OVER_BF16),
+                         "algorithmic_bytes_per_launch": M * K + K * N + M * KB + N * KB + M * N * 2},
+            "timing": "median of 5 groups of %d back-to-back launches alternating 2 input sets "
+                      "(A+B 128 MB each)" % steps,
+            "status": ll.status_string(st)}
+
+
 def bench_small(args, dev, stream, peaks, peak_src):
     """FP16 256^3 with an FP32 output: launch-bound, so timed as a CUDA graph of 200
     launches; the roofline fraction is informational."""
@@ -855,7 +907,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the GEMV / FP8 / ragged lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "ragged", "tokens", "w8a16",
+    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "mx", "ragged", "tokens", "w8a16",
                                            "small"],
                     default="all",
                     help="all = the contract line; otherwise time one other kernel and print its object")
@@ -874,7 +926,7 @@ def main(argv=None):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=dev)
 
-    single = {"gemv": bench_gemv, "gemv_fused": bench_gemv_fused, "fp8": bench_fp8,
+    single = {"gemv": bench_gemv, "gemv_fused": bench_gemv_fused, "fp8": bench_fp8, "mx": bench_mx,
               "ragged": bench_ragged, "tokens": bench_w8a8_tokens, "w8a16": bench_w8a16,
               "small": bench_small}.get(args.workload)
     if single is not None:
@@ -892,6 +944,7 @@ def main(argv=None):
         extra["w8a8_linear_tokens_4096x11008"] = bench_w8a8_tokens(args, dev, stream, peaks, peak_src)
         extra["w8a16_linear_tokens_4096x11008"] = bench_w8a16(args, dev, stream, peaks, peak_src)
         extra["e4m3_gemm_8192"] = bench_fp8(args, dev, stream, peaks, peak_src)
+        extra["mxf8_gemm_8192"] = bench_mx(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_4093x5003x2056"] = bench_ragged(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_256"] = bench_small(args, dev, stream, peaks, peak_src)
     barrier(dev)

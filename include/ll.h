@@ -199,6 +199,41 @@ ll_status ll_gemm_f8_blockscaled_mixed(int a_type, int b_type, int M, int N, int
                                        int d_type, void* workspace, size_t ws_bytes,
                                        ll_stream_t stream);
 
+/*
+ * MX block-scaled 8-bit GEMM (OCP microscaling): every 32 consecutive K elements of a row
+ * of A, and of a column of B, share one E8M0 scale X = 2^(e - 127):
+ *
+ *   D[i][j] = alpha * sum_k (2^(scale_a[i][k/32] - 127) A[i][k])
+ *                         * (2^(scale_b[j][k/32] - 127) B[k][j])  + beta * C[i][j]
+ *
+ * Defined by: "Tensor Core" chapter, the table of tensor-core formats per generation
+ * (Blackwell adds block-scaled formats such as MXFP4 / NVFP4), with the MX layout of the
+ * OCP microscaling format (32-element blocks, E8M0 shared exponent), applied here to
+ * 8-bit elements (MXFP8).  The tensor cores apply the scales (no software promotion).
+ *
+ *   a_type, b_type : LL_IN_E4M3 or LL_IN_E5M2 (element formats of A and of B)
+ *   A       : M x K codes, lda >= K          B : K x N codes, ldb >= N
+ *   scale_a : M x ld_sa E8M0 codes (uint8), ld_sa >= ceil(K/32): row i holds the scales of
+ *             row i of A, one per 32-wide K block (a shorter last block keeps its scale)
+ *   scale_b : N x ld_sb E8M0 codes, ld_sb >= ceil(K/32): row j holds the scales of column j
+ *             of B, one per 32-wide K block
+ *   C, D, stream: as for ll_gemm_f16.  The code 255 (NaN) is not supported.
+ *   workspace : as for ll_gemm_f16, sized by ll_gemm_mxf8_workspace_size: the scale
+ *             matrices are read in place when their base is 16-byte aligned and their
+ *             pitch a multiple of 16 bytes, and repacked into the workspace otherwise.
+ * Accumulation is FP32 over the whole K; alpha / beta and the output cast as ll_gemm_f16.
+ * Errors: as ll_gemm_fp8_blockscaled; LL_ERR_INVALID_ARG for other a_type / b_type or
+ * scale pitches below ceil(K/32).
+ */
+/* Workspace bytes an ll_gemm_mxf8 call needs (assuming 16-byte-aligned bases; see
+ * ll_gemm_workspace_size for misaligned ones): operand repacks plus scale repacks. */
+size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int64_t ld_sa, int64_t ld_sb);
+
+ll_status ll_gemm_mxf8(int a_type, int b_type, int M, int N, int K, float alpha, const uint8_t* A, int64_t lda,
+                       const uint8_t* scale_a, int64_t ld_sa, const uint8_t* B, int64_t ldb, const uint8_t* scale_b,
+                       int64_t ld_sb, float beta, const float* C, int64_t ldc, void* D, int64_t ldd, int d_type,
+                       void* workspace, size_t ws_bytes, ll_stream_t stream);
+
 /* ------------------------------------------------------------------ W8A8 GEMV */
 
 /*

@@ -12,6 +12,8 @@ gemm_f16             ll_gemm_f16
 gemm_bf16            ll_gemm_bf16
 gemm_fp8_blockscaled ll_gemm_fp8_blockscaled
 gemm_f8_blockscaled_mixed ll_gemm_f8_blockscaled_mixed
+gemm_mxf8            ll_gemm_mxf8
+gemm_mxf8_workspace_size ll_gemm_mxf8_workspace_size
 linear_w8a8_gemv     ll_linear_w8a8_gemv
 linear_w8a8_gemv_ex  ll_linear_w8a8_gemv_ex
 linear_w8a8          ll_linear_w8a8
@@ -38,7 +40,8 @@ OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 
 # every symbol the header declares
 EXPORTS = ["ll_gemm_workspace_size", "ll_gemm_f16", "ll_gemm_bf16", "ll_gemm_fp8_blockscaled",
-           "ll_gemm_f16_noalloc", "ll_gemm_f8_blockscaled_mixed",
+           "ll_gemm_f16_noalloc", "ll_gemm_f8_blockscaled_mixed", "ll_gemm_mxf8",
+           "ll_gemm_mxf8_workspace_size",
            "ll_linear_w8a8_gemv", "ll_linear_w8a8_gemv_ex", "ll_linear_f16_w8a8_gemv",
            "ll_linear_w8a8", "ll_linear_w8a16",
            "ll_quantize_per_token_f16", "ll_get_device_status", "ll_set_wait_timeout_ns",
@@ -70,6 +73,10 @@ def _load():
                                           f32, vp, i64, vp, i64, i32, vp, ctypes.c_size_t, vp]
     L.ll_gemm_f8_blockscaled_mixed.restype = i32
     L.ll_gemm_f8_blockscaled_mixed.argtypes = [i32, i32] + L.ll_gemm_fp8_blockscaled.argtypes
+    L.ll_gemm_mxf8_workspace_size.restype = ctypes.c_size_t
+    L.ll_gemm_mxf8_workspace_size.argtypes = [i32, i32, i32, i64, i64, i64, i64]
+    L.ll_gemm_mxf8.restype = i32
+    L.ll_gemm_mxf8.argtypes = [i32, i32] + L.ll_gemm_fp8_blockscaled.argtypes
     L.ll_linear_w8a8_gemv.restype = i32
     L.ll_linear_w8a8_gemv.argtypes = [i32, i32, vp, vp, vp, i64, vp, vp, vp, vp]
     L.ll_linear_w8a8_gemv_ex.restype = i32
@@ -192,6 +199,20 @@ def gemm_f8_blockscaled_mixed(a_type, b_type, M, N, K, alpha, A, lda, scale_a, l
                                                    ld_sb, beta, _p(C), ldc, _p(D), ldd, d_type, w,
                                                    wb, _stream(stream)),
                   "ll_gemm_f8_blockscaled_mixed")
+
+
+def gemm_mxf8_workspace_size(M, N, K, lda, ldb, ld_sa, ld_sb):
+    return lib.ll_gemm_mxf8_workspace_size(M, N, K, lda, ldb, ld_sa, ld_sb)
+
+
+def gemm_mxf8(a_type, b_type, M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb, scale_b, ld_sb, beta, C, ldc,
+              D, ldd, d_type, workspace=None, stream=None):
+    """MX block-scaled 8-bit GEMM: scale_a (M x ld_sa) and scale_b (N x ld_sb) hold E8M0
+    codes, one per 32-wide K block of a row of A / a column of B."""
+    w, wb = _ws(workspace)
+    return _check(lib.ll_gemm_mxf8(a_type, b_type, M, N, K, alpha, _p(A), lda, _p(scale_a), ld_sa, _p(B), ldb,
+                                   _p(scale_b), ld_sb, beta, _p(C), ldc, _p(D), ldd, d_type, w, wb,
+                                   _stream(stream)), "ll_gemm_mxf8")
 
 
 def linear_w8a8_gemv(N, K, x, x_scale, W, ldw, w_scale, y, z_out=None, stream=None):

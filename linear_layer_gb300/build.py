@@ -16,8 +16,8 @@ BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "liblinear_layer_gb300.so")
 
-SOURCES = ["abi.cu", "gemm_tc.cu", "gemv_w8a8.cu", "aux.cu", "noalloc.cu", "w8a8_batch.cu", "w8a8_tc.cu", "w8a16.cu"]
-HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"),
+SOURCES = ["abi.cu", "gemm_tc.cu", "gemm_mx.cu", "gemv_w8a8.cu", "aux.cu", "noalloc.cu", "w8a8_batch.cu", "w8a8_tc.cu", "w8a16.cu"]
+HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "gemm_common.cuh"),
            os.path.join(ROOT, "include", "ll.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -183,11 +183,14 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
   if ((a.scale_a && reinterpret_cast<uintptr_t>(a.scale_a) % 4 != 0) ||
       (a.scale_b && reinterpret_cast<uintptr_t>(a.scale_b) % 4 != 0))
     return LL_ERR_MISALIGNED;
-  const bool f8 = a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2;
+  const bool f8 = (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) && !a.mx;  // FP32 128-blocks
   const int64_t kb = (a.K + 127) / 128, nb = (a.N + 127) / 128;
+  const int64_t kb32 = (a.K + 31) / 32;  // MX: E8M0 blocks of 32 along K
   if (a.K > 0) {
     if (a.A == nullptr || a.B == nullptr || a.lda < a.K || a.ldb < a.N) return LL_ERR_INVALID_ARG;
     if (f8 && (a.scale_a == nullptr || a.scale_b == nullptr || a.ld_sa < kb || a.ld_sb < nb))
+      return LL_ERR_INVALID_ARG;
+    if (a.mx && (a.mx_sa == nullptr || a.mx_sb == nullptr || a.ld_mx_sa < kb32 || a.ld_mx_sb < kb32))
       return LL_ERR_INVALID_ARG;
   }
   // D may share bytes with no input other than itself as C (in place, checked above);
@@ -203,10 +206,14 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
       {a.K > 0 && f8 ? a.scale_a : nullptr, a.M, kb * 4, a.ld_sa * 4},
       {a.K > 0 && f8 ? a.scale_b : nullptr, kb, nb * 4, a.ld_sb * 4},
   };
+  if (a.mx) {
+    ins[3] = Extent{a.K > 0 ? a.mx_sa : nullptr, a.M, kb32, a.ld_mx_sa};
+    ins[4] = Extent{a.K > 0 ? a.mx_sb : nullptr, a.N, kb32, a.ld_mx_sb};
+  }
   if (outputs_overlap(&D, 1, ins, 5)) return LL_ERR_INVALID_ARG;
   if (a.K > 0 && ws != nullptr && ws_bytes > 0) {
     const RepackPlan plan = plan_repack(a);
-    if (plan.a || plan.b) {
+    if (plan.a || plan.b || plan.sa || plan.sb) {
       const Extent W{ws, 1, static_cast<int64_t>(ws_bytes), static_cast<int64_t>(ws_bytes)};
       Extent all[6] = {D, ins[0], ins[1], ins[2], ins[3], ins[4]};
       if (in_place) all[3] = Extent{a.C, a.M, a.N * 4, a.ldc * 4};
@@ -225,6 +232,12 @@ ll::RepackPlan ll::plan_repack(const GemmArgs& a) {
   pl.ldb_p = round_up(a.N, 16 / es);
   pl.a_bytes = pl.a ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.lda_p * es, 256)) : 0;
   pl.b_bytes = pl.b ? static_cast<size_t>(static_cast<int64_t>(a.K) * pl.ldb_p * es) : 0;
+  const int64_t nkb = (a.K + 31) / 32;
+  pl.sa = a.mx && !pitch_ok(a.mx_sa, a.ld_mx_sa, 1);
+  pl.sb = a.mx && !pitch_ok(a.mx_sb, a.ld_mx_sb, 1);
+  pl.ld_sa_p = pl.ld_sb_p = round_up(nkb, 16);
+  pl.sa_bytes = pl.sa ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.ld_sa_p, 256)) : 0;
+  pl.sb_bytes = pl.sb ? static_cast<size_t>(round_up(static_cast<int64_t>(a.N) * pl.ld_sb_p, 256)) : 0;
   return pl;
 }
 
@@ -245,6 +258,21 @@ ll_status ll::launch_gemm_planned(GemmArgs a, const RepackPlan& plan, void* scra
     a.B = w + plan.a_bytes;
     a.ldb = plan.ldb_p;
   }
+  unsigned char* ws = w + plan.a_bytes + static_cast<size_t>(round_up(static_cast<int64_t>(plan.b_bytes), 256));
+  const int nkb = (a.K + 31) / 32;
+  if (plan.sa) {
+    const ll_status st = launch_repack(a.mx_sa, a.ld_mx_sa, ws, plan.ld_sa_p, a.M, nkb, 1, ctx);
+    if (st != LL_OK) return st;
+    a.mx_sa = ws;
+    a.ld_mx_sa = plan.ld_sa_p;
+    ws += plan.sa_bytes;
+  }
+  if (plan.sb) {
+    const ll_status st = launch_repack(a.mx_sb, a.ld_mx_sb, ws, plan.ld_sb_p, a.N, nkb, 1, ctx);
+    if (st != LL_OK) return st;
+    a.mx_sb = ws;
+    a.ld_mx_sb = plan.ld_sb_p;
+  }
   return launch_gemm_tc(a, ctx);
 }
 
@@ -259,11 +287,14 @@ ll_status gemm_common(const ll::GemmArgs& a, void* workspace, size_t ws_bytes, l
   if (a.K == 0) return ll::launch_scale_c(a, ctx);
   const ll::RepackPlan plan = ll::plan_repack(a);
   void* base = nullptr;
-  if (plan.a || plan.b) {
+  if (plan.a || plan.b || plan.sa || plan.sb) {
     const int es = in_esize(a.in_type);
+    const int nkb = (a.K + 31) / 32;
     size_t need = 0;
     if (plan.a) need += repack_bytes(a.M, a.K, es);
     if (plan.b) need += repack_bytes(a.K, a.N, es);
+    if (plan.sa) need += repack_bytes(a.M, nkb, 1);
+    if (plan.sb) need += repack_bytes(a.N, nkb, 1);
     if (workspace == nullptr || ws_bytes < need) return LL_ERR_WORKSPACE;
     base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
   }
@@ -310,6 +341,15 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
   return need;
 }
 
+size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int64_t ld_sa, int64_t ld_sb) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const int nkb = (K + 31) / 32;
+  size_t need = ll_gemm_workspace_size(M, N, K, lda, ldb, LL_IN_E4M3);
+  if (ld_sa % 16 != 0) need += repack_bytes(M, nkb, 1);
+  if (ld_sb % 16 != 0) need += repack_bytes(N, nkb, 1);
+  return need;
+}
+
 static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, const void* A,
                                int64_t lda, const void* B, int64_t ldb, float beta, const float* C,
                                int64_t ldc, void* D, int64_t ldd, int d_type) {
@@ -334,6 +374,11 @@ static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, co
   a.ld_sa = 0;
   a.scale_b = nullptr;
   a.ld_sb = 0;
+  a.mx = 0;
+  a.mx_sa = nullptr;
+  a.ld_mx_sa = 0;
+  a.mx_sb = nullptr;
+  a.ld_mx_sb = 0;
   return a;
 }
 
@@ -382,6 +427,22 @@ ll_status ll_gemm_f8_blockscaled_mixed(int a_type, int b_type, int M, int N, int
   a.ld_sa = ld_sa;
   a.scale_b = scale_b;
   a.ld_sb = ld_sb;
+  return gemm_common(a, workspace, ws_bytes, stream);
+}
+
+ll_status ll_gemm_mxf8(int a_type, int b_type, int M, int N, int K, float alpha, const uint8_t* A, int64_t lda,
+                       const uint8_t* scale_a, int64_t ld_sa, const uint8_t* B, int64_t ldb, const uint8_t* scale_b,
+                       int64_t ld_sb, float beta, const float* C, int64_t ldc, void* D, int64_t ldd, int d_type,
+                       void* workspace, size_t ws_bytes, ll_stream_t stream) {
+  auto f8 = [](int t) { return t == LL_IN_E4M3 || t == LL_IN_E5M2; };
+  if (!f8(a_type) || !f8(b_type)) return LL_ERR_INVALID_ARG;
+  ll::GemmArgs a = dense_args(a_type, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type);
+  a.b_type = b_type;
+  a.mx = 1;
+  a.mx_sa = scale_a;
+  a.ld_mx_sa = ld_sa;
+  a.mx_sb = scale_b;
+  a.ld_mx_sb = ld_sb;
   return gemm_common(a, workspace, ws_bytes, stream);
 }
 

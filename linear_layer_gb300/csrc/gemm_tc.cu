@@ -33,30 +33,10 @@
 #include <cstring>
 #include <mutex>
 
-#include "internal.h"
-#include "ptx.cuh"
+#include "gemm_common.cuh"
 
 namespace ll {
 
-struct GemmParams {
-  int M, N, K;
-  float alpha, beta;
-  const float* C;
-  int64_t ldc;
-  void* D;
-  int64_t ldd;
-  int d_type;
-  int c_vec, d_vec;  // rows of C / D may be accessed with 4-element vectors
-  int d_row16;       // rows of D start on 16-byte boundaries
-  int epi_tma;       // CTA-pair 16-bit epilogue through TMA (C and D rows 16-byte aligned)
-  const float* sA;
-  int64_t ld_sa;
-  const float* sB;
-  int64_t ld_sb;
-  uint32_t* status;
-  uint64_t timeout_ns;
-  int group_m;
-};
 
 template <int BN_, bool FP8_>
 struct TileCfg {
@@ -92,157 +72,6 @@ struct TileCfg {
   static_assert(STAGES >= 2, "need at least two stages");
 };
 
-// Operand formats of an MMA, packed as a | (b << 3): kind::f16 0 = FP16, 1 = BF16;
-// kind::f8f6f4 0 = E4M3, 1 = E5M2.
-__host__ __device__ constexpr uint32_t fmt_pair(uint32_t a, uint32_t b) { return a | (b << 3); }
-
-// tcgen05 instruction descriptor (kind::f16 / kind::f8f6f4): D = F32 (bits 4-5 = 1),
-// A/B format (bits 7-9 / 10-12), A K-major (bit 15 = 0), B MN-major (bit 16 = 1),
-// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t fmts, int n, int m) {
-  return (1u << 4) | ((fmts & 7u) << 7) | (((fmts >> 3) & 7u) << 10) | (1u << 16) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mb,
-                                            int& nb) {
-  const int span = group_m * num_n;
-  const int g = t / span;
-  const int first_m = g * group_m;
-  const int gsz = min(num_m - first_m, group_m);
-  const int r = t - g * span;
-  mb = first_m + r % gsz;
-  nb = r / gsz;
-}
-
-// Epilogue.  A chunk is 32 rows of a tile (lane t of the warp holds row m + t of the
-// accumulator) by 32 columns n .. n + 31:
-//   D[m][n] = alpha * acc[m][n] + beta * C[m][n]   (C not read when beta == 0)
-// evaluated as fma(beta, C, alpha * acc) in FP32 and rounded once to the output type,
-// identically in both layouts below, so the two agree bit for bit.  Each chunk is split
-// into a C load into registers and a store, so that a caller can load the next chunk's
-// C while it stores this one.  C may alias D only as the same matrix (same base and
-// pitch): a thread then reads every element before it writes it, and loads of a later
-// chunk never touch elements stored earlier.
-//
-// Row layout (rows of C and D on 16-byte boundaries): each lane reads and writes its
-// own row segment straight from registers.
-__device__ __forceinline__ void load_c_row(const GemmParams& p, int m, int n, float (&cv)[32]) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) cv[j] = 0.0f;
-  if (p.beta == 0.0f || m >= p.M || n >= p.N) return;
-  const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
-  if (n + 32 <= p.N && p.c_vec) {
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const float4 t = *reinterpret_cast<const float4*>(crow + j);
-      cv[j] = t.x;
-      cv[j + 1] = t.y;
-      cv[j + 2] = t.z;
-      cv[j + 3] = t.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n + j < p.N) cv[j] = crow[j];
-  }
-}
-
-__device__ __forceinline__ void store_row(const GemmParams& p, int m, int n, const float (&acc)[32],
-                                          const float (&cv)[32]) {
-  if (m >= p.M || n >= p.N) return;
-  const bool full = n + 32 <= p.N;
-  float o[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    o[j] = p.alpha * acc[j];
-    if (p.beta != 0.0f) o[j] = fmaf(p.beta, cv[j], o[j]);
-  }
-  const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
-  if (p.d_type == LL_OUT_F32) {
-    float* dp = static_cast<float*>(p.D) + off;
-    if (full && p.d_row16) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n + j < p.N) dp[j] = o[j];
-    }
-  } else {
-    const bool bf = p.d_type == LL_OUT_BF16;
-    uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
-    uint32_t w[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (bf) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-        w[j] = *reinterpret_cast<uint32_t*>(&h2);
-      } else {
-        __half2 h2 = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
-        w[j] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-    }
-    if (full && p.d_row16) {
-#pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        *reinterpret_cast<uint4*>(dp + 2 * j) = make_uint4(w[j], w[j + 1], w[j + 2], w[j + 3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n + j < p.N) dp[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
-    }
-  }
-}
-
-// a[j] = alpha * a[j] (+ beta * C[m][n + j]) for one 32-column chunk of row m (< M),
-// C consumed four columns at a time as it arrives.
-__device__ __forceinline__ void combine_c_row(const GemmParams& p, int m, int n, float (&a)[32]) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) a[j] *= p.alpha;
-  if (p.beta == 0.0f) return;
-  const float* crow = p.C + static_cast<int64_t>(m) * p.ldc + n;
-  if (n + 32 <= p.N && p.c_vec) {
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const float4 cv = *reinterpret_cast<const float4*>(crow + j);
-      a[j] = fmaf(p.beta, cv.x, a[j]);
-      a[j + 1] = fmaf(p.beta, cv.y, a[j + 1]);
-      a[j + 2] = fmaf(p.beta, cv.z, a[j + 2]);
-      a[j + 3] = fmaf(p.beta, cv.w, a[j + 3]);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n + j < p.N) a[j] = fmaf(p.beta, crow[j], a[j]);
-  }
-}
-
-// Store final values (alpha and beta applied) of one chunk of row m, masked to N.
-__device__ __forceinline__ void store_row_final(const GemmParams& p, int m, int n, const float (&o)[32]) {
-  const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
-  const bool full = n + 32 <= p.N;
-  if (p.d_type == LL_OUT_F32) {
-    float* dp = static_cast<float*>(p.D) + off;
-    if (full && p.d_row16) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(dp + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (n + j < p.N) dp[j] = o[j];
-    }
-  } else {
-    const bool bf = p.d_type == LL_OUT_BF16;
-    uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + off;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (n + j < p.N)
-        dp[j] = bf ? __bfloat16_as_ushort(__float2bfloat16_rn(o[j])) : __half_as_ushort(__float2half_rn(o[j]));
-  }
-}
 
 // One 32 x 32 chunk of 16-bit D into a 2 KB staging buffer in the layout of a TMA box
 // of 64-byte rows with 64-byte swizzle: 16-byte slot j of row l (= lane) at
@@ -264,41 +93,6 @@ __device__ __forceinline__ void stage_row16(uint8_t* buf, int lane, const float 
       }
     }
     drow[j ^ ((lane >> 1) & 3)] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-  }
-}
-
-// Up to CH consecutive chunks of one row (lane = row m), read straight from the FP32
-// accumulator registers (the FP8 promotion epilogue, which holds CH = 4 chunks).
-template <int CH>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int m, int n0,
-                                              float (&acc)[CH][32]) {
-  if (m >= p.M) return;
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int n = n0 + 32 * c;
-    if (n >= p.N) break;
-    combine_c_row(p, m, n, acc[c]);
-    if (p.d_type != LL_OUT_F32 && n + 32 <= p.N && p.d_row16) {  // 16-byte vector stores
-      uint16_t* dp = reinterpret_cast<uint16_t*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
-      const bool bf = p.d_type == LL_OUT_BF16;
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (bf) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[c][j + 2 * i], acc[c][j + 2 * i + 1]);
-            w4[i] = *reinterpret_cast<uint32_t*>(&h2);
-          } else {
-            __half2 h2 = __floats2half2_rn(acc[c][j + 2 * i], acc[c][j + 2 * i + 1]);
-            w4[i] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-        }
-        *reinterpret_cast<uint4*>(dp + j) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-    } else {
-      store_row_final(p, m, n, acc[c]);
-    }
   }
 }
 
@@ -1126,34 +920,6 @@ bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType 
   return r == CUDA_SUCCESS;
 }
 
-static GemmParams make_params(const GemmArgs& a, const LaunchCtx& ctx) {
-  GemmParams p;
-  p.M = a.M;
-  p.N = a.N;
-  p.K = a.K;
-  p.alpha = a.alpha;
-  p.beta = a.beta;
-  p.C = a.C;
-  p.ldc = a.ldc;
-  p.D = a.D;
-  p.ldd = a.ldd;
-  p.d_type = a.d_type;
-  const int dsize = a.d_type == LL_OUT_F32 ? 4 : 2;
-  p.c_vec = a.C != nullptr && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && ((a.ldc * 4) % 16 == 0);
-  // vector stores: 16 bytes (FP32) or 8 bytes (BF16 / FP16) per lane, at 4-column steps
-  p.d_vec = (reinterpret_cast<uintptr_t>(a.D) % (4 * dsize) == 0) && ((a.ldd * dsize) % (4 * dsize) == 0);
-  p.d_row16 = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * dsize) % 16 == 0);
-  p.epi_tma = 0;
-  p.sA = a.scale_a;
-  p.ld_sa = a.ld_sa;
-  p.sB = a.scale_b;
-  p.ld_sb = a.ld_sb;
-  p.status = ctx.status;
-  p.timeout_ns = ctx.timeout_ns;
-  p.group_m = 8;
-
-  return p;
-}
 
 constexpr int kMaxDev = 64;
 
@@ -1171,7 +937,7 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
   if (!make_tensor_map_2d(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
   if (!make_tensor_map_2d(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
 
-  GemmParams p = make_params(a, ctx);
+  GemmParams p = make_gemm_params(a, ctx);
 
   const int num_tiles = ((a.M + 127) / 128) * ((a.N + Cfg::BN - 1) / Cfg::BN);
   const int grid = num_tiles < ctx.num_sms ? num_tiles : ctx.num_sms;
@@ -1205,7 +971,7 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   CUtensorMap tmA, tmB, tmC, tmD;
   if (!make_tensor_map_2d(&tmA, a.A, dt, Cfg::ELT, a.M, a.K, a.lda, Cfg::BK, 128)) return LL_ERR_CUDA;
   if (!make_tensor_map_2d(&tmB, a.B, dt, Cfg::ELT, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK)) return LL_ERR_CUDA;
-  GemmParams p = make_params(a, ctx);
+  GemmParams p = make_gemm_params(a, ctx);
   // 16-bit epilogue through TMA when the rows of D (and of C, if read) start on
   // 16-byte boundaries: 32 x 32 boxes, 128-byte rows (FP32) or 64-byte rows (16-bit)
   memset(&tmC, 0, sizeof(tmC));
@@ -1287,6 +1053,7 @@ static ll_status run_fp8(const GemmArgs& a, const LaunchCtx& ctx) {
 }
 
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx) {
+  if (a.mx) return launch_gemm_mx(a, ctx);  // hardware block scaling (gemm_mx.cu)
   // FP8: the one-CTA kernel at every size (it measured 3 to 17 % faster than a CTA-pair
   // version of the block promotion from 1792^3 to 8192^3)
   if (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) {

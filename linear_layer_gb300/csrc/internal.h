@@ -36,6 +36,11 @@ struct GemmArgs {
   int64_t ld_sa;
   const float* scale_b;
   int64_t ld_sb;
+  int mx;                 // MX block scaling (E8M0 per 32 K elements) instead of FP32 128-blocks
+  const uint8_t* mx_sa;   // MX: M x ld_mx_sa scale codes of A, one per row and 32-wide K block
+  int64_t ld_mx_sa;
+  const uint8_t* mx_sb;   // MX: N x ld_mx_sb scale codes of B, one per column and K block
+  int64_t ld_mx_sb;
 };
 
 // Launch context of the current device (status word, SM count, wait limit) for `stream`;
@@ -67,11 +72,17 @@ ll_status validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes);
 
 // Where the operand repack of a GEMM puts A and B: A (when repacked) at the 256-byte-
 // aligned start of the scratch, B after it.  a_bytes = roundup(M * lda_p * esize, 256)
-// and b_bytes = K * ldb_p * esize with the pitches rounded up to 16 bytes.
+// and b_bytes = K * ldb_p * esize with the pitches rounded up to 16 bytes; MX scale
+// codes follow B (each region rounded up to 256 bytes).
 struct RepackPlan {
   bool a, b;
   int64_t lda_p, ldb_p;  // elements
   size_t a_bytes, b_bytes;
+  // MX scale codes (bytes, K-block-contiguous rows): repacked to 16-byte pitches after B,
+  // each at a 256-byte boundary, when their base or pitch is not 16-byte aligned
+  bool sa, sb;
+  int64_t ld_sa_p, ld_sb_p;
+  size_t sa_bytes, sb_bytes;
 };
 RepackPlan plan_repack(const GemmArgs& a);
 
@@ -81,6 +92,10 @@ ll_status launch_gemm_planned(GemmArgs a, const RepackPlan& plan, void* scratch,
 
 // tcgen05 GEMM (gemm_tc.cu).  Requires A, B 16-byte aligned with 16-byte-multiple pitches.
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx);
+
+// MX block-scaled 8-bit GEMM on tcgen05 with hardware block scaling (gemm_mx.cu); the same
+// operand requirements.
+ll_status launch_gemm_mx(const GemmArgs& a, const LaunchCtx& ctx);
 
 // D = beta * C (or 0) for K == 0 (aux.cu).
 ll_status launch_scale_c(const GemmArgs& a, const LaunchCtx& ctx);

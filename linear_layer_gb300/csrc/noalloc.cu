@@ -80,6 +80,11 @@ extern "C" ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const
   a.ld_sa = 0;
   a.scale_b = nullptr;
   a.ld_sb = 0;
+  a.mx = 0;
+  a.mx_sa = nullptr;
+  a.ld_mx_sa = 0;
+  a.mx_sb = nullptr;
+  a.ld_mx_sb = 0;
 
   // the same argument rules as ll_gemm_f16 (the scratch cannot alias caller memory)
   ll_status st = ll::validate_gemm(a, nullptr, 0);

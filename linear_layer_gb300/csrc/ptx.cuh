@@ -294,6 +294,28 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// D[tmem] (+)= (XA o A[smem]) x (XB o B[smem]) with hardware block scaling: 8-bit
+// floating-point inputs, one E8M0 scale per 32 K elements of each row of A and column of B,
+// read from TMEM at sfa_tmem / sfb_tmem (the byte of each 32-bit TMEM word is chosen by
+// the scale-factor IDs of the instruction descriptor).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 32-row x 16-byte shared-memory block into TMEM columns taddr .. taddr + 3 of all
+// four 32-lane quarters (lane 32q + r, column c receives bytes 4c .. 4c + 3 of row r).
+// Asynchronous; ordered before the tcgen05.mma instructions this thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 2-CTA MMA (M = 256 over the CTA pair): issued by one thread of the even CTA; A rows
 // 0-127 / 128-255 and B columns [0, N/2) / [N/2, N) come from the two CTAs' shared
 // memory at the same offsets, and each CTA's TMEM receives its 128 rows of D.
@@ -388,6 +410,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
   d |= 2ull << 61;
+  return d;
+}
+
+// Shared-memory matrix descriptor of an unswizzled block whose 8-row x 16-byte core
+// matrices lie 128 bytes apart (rows of 16 bytes, packed): layout type 0 (no swizzle),
+// stride-dimension offset 128 bytes.
+__device__ __forceinline__ uint64_t smem_desc_plain16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= 1ull << 46;
   return d;
 }
 

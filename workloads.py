@@ -30,7 +30,8 @@ SEED_A, SEED_B, SEED_C, SEED_SCALE, SEED_X, SEED_SX = 1, 2, 3, 4, 5, 6
 
 NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "e4m3": 0x7F}
 
-# The five workloads of the linear layer (named by what they are, with sizes).
+# The workloads of the linear layer (named by what they are, with sizes): the five
+# configurations of the path and the MX block-scaled FP8 GEMM of the FP8 size.
 WORKLOADS = {
     "f16_gemm_256": dict(op="gemm", kind="f16", M=256, N=256, K=256, alpha=1.0, beta=0.0,
                          out="f32"),
@@ -40,6 +41,8 @@ WORKLOADS = {
     "f16_gemm_4093x5003x2056": dict(op="gemm", kind="f16", M=4093, N=5003, K=2056, alpha=0.5,
                                     beta=-1.25, out="f32"),
     "e4m3_gemm_8192": dict(op="fp8", kind="e4m3", M=8192, N=8192, K=8192, alpha=1.0, beta=0.0,
+                           out="bf16"),
+    "mxf8_gemm_8192": dict(op="gemm_mx", kind="e4m3", M=8192, N=8192, K=8192, alpha=1.0, beta=0.0,
                            out="bf16"),
 }
 
