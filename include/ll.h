@@ -218,16 +218,17 @@ ll_status ll_gemm_f8_blockscaled_mixed(int a_type, int b_type, int M, int N, int
  *   scale_b : N x ld_sb E8M0 codes, ld_sb >= ceil(K/32): row j holds the scales of column j
  *             of B, one per 32-wide K block
  *   C, D, stream: as for ll_gemm_f16.  The code 255 (NaN) is not supported.
- *   workspace : as for ll_gemm_f16, sized by ll_gemm_mxf8_workspace_size: the scale
- *             matrices are read in place when their base is 16-byte aligned and their
- *             pitch a multiple of 16 bytes, and repacked into the workspace otherwise.
+ *   workspace : required, sized by ll_gemm_mxf8_workspace_size: the call first rearranges
+ *             the scale codes into the blocks the tensor cores' scale copies read (a few
+ *             MB: 4 MiB at 8192^3), plus any operand repack as for ll_gemm_f16.  The
+ *             scale matrices may start at any address and have any pitch >= ceil(K/32).
  * Accumulation is FP32 over the whole K; alpha / beta and the output cast as ll_gemm_f16.
  * Errors: as ll_gemm_fp8_blockscaled; LL_ERR_INVALID_ARG for other a_type / b_type or
  * scale pitches below ceil(K/32).
  */
-/* Workspace bytes an ll_gemm_mxf8 call needs (assuming 16-byte-aligned bases; see
- * ll_gemm_workspace_size for misaligned ones): operand repacks plus scale repacks. */
-size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int64_t ld_sa, int64_t ld_sb);
+/* Workspace bytes an ll_gemm_mxf8 call needs: the rearranged scale codes, plus the operand
+ * repacks of ll_gemm_workspace_size (assuming 16-byte-aligned A and B; see there). */
+size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb);
 
 ll_status ll_gemm_mxf8(int a_type, int b_type, int M, int N, int K, float alpha, const uint8_t* A, int64_t lda,
                        const uint8_t* scale_a, int64_t ld_sa, const uint8_t* B, int64_t ldb, const uint8_t* scale_b,

@@ -74,7 +74,7 @@ def _load():
     L.ll_gemm_f8_blockscaled_mixed.restype = i32
     L.ll_gemm_f8_blockscaled_mixed.argtypes = [i32, i32] + L.ll_gemm_fp8_blockscaled.argtypes
     L.ll_gemm_mxf8_workspace_size.restype = ctypes.c_size_t
-    L.ll_gemm_mxf8_workspace_size.argtypes = [i32, i32, i32, i64, i64, i64, i64]
+    L.ll_gemm_mxf8_workspace_size.argtypes = [i32, i32, i32, i64, i64]
     L.ll_gemm_mxf8.restype = i32
     L.ll_gemm_mxf8.argtypes = [i32, i32] + L.ll_gemm_fp8_blockscaled.argtypes
     L.ll_linear_w8a8_gemv.restype = i32
@@ -201,8 +201,8 @@ def gemm_f8_blockscaled_mixed(a_type, b_type, M, N, K, alpha, A, lda, scale_a, l
                   "ll_gemm_f8_blockscaled_mixed")
 
 
-def gemm_mxf8_workspace_size(M, N, K, lda, ldb, ld_sa, ld_sb):
-    return lib.ll_gemm_mxf8_workspace_size(M, N, K, lda, ldb, ld_sa, ld_sb)
+def gemm_mxf8_workspace_size(M, N, K, lda, ldb):
+    return lib.ll_gemm_mxf8_workspace_size(M, N, K, lda, ldb)
 
 
 def gemm_mxf8(a_type, b_type, M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb, scale_b, ld_sb, beta, C, ldc,

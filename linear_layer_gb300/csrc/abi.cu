@@ -213,7 +213,7 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
   if (outputs_overlap(&D, 1, ins, 5)) return LL_ERR_INVALID_ARG;
   if (a.K > 0 && ws != nullptr && ws_bytes > 0) {
     const RepackPlan plan = plan_repack(a);
-    if (plan.a || plan.b || plan.sa || plan.sb) {
+    if (plan.a || plan.b || plan.mx) {
       const Extent W{ws, 1, static_cast<int64_t>(ws_bytes), static_cast<int64_t>(ws_bytes)};
       Extent all[6] = {D, ins[0], ins[1], ins[2], ins[3], ins[4]};
       if (in_place) all[3] = Extent{a.C, a.M, a.N * 4, a.ldc * 4};
@@ -232,12 +232,9 @@ ll::RepackPlan ll::plan_repack(const GemmArgs& a) {
   pl.ldb_p = round_up(a.N, 16 / es);
   pl.a_bytes = pl.a ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.lda_p * es, 256)) : 0;
   pl.b_bytes = pl.b ? static_cast<size_t>(static_cast<int64_t>(a.K) * pl.ldb_p * es) : 0;
-  const int64_t nkb = (a.K + 31) / 32;
-  pl.sa = a.mx && !pitch_ok(a.mx_sa, a.ld_mx_sa, 1);
-  pl.sb = a.mx && !pitch_ok(a.mx_sb, a.ld_mx_sb, 1);
-  pl.ld_sa_p = pl.ld_sb_p = round_up(nkb, 16);
-  pl.sa_bytes = pl.sa ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.ld_sa_p, 256)) : 0;
-  pl.sb_bytes = pl.sb ? static_cast<size_t>(round_up(static_cast<int64_t>(a.N) * pl.ld_sb_p, 256)) : 0;
+  pl.mx = a.mx != 0;
+  pl.xa_bytes = pl.xb_bytes = 0;
+  if (pl.mx) pl.xb_bytes = mx_scale_block_bytes(a.M, a.N, a.K, &pl.xa_bytes) - pl.xa_bytes;
   return pl;
 }
 
@@ -258,20 +255,12 @@ ll_status ll::launch_gemm_planned(GemmArgs a, const RepackPlan& plan, void* scra
     a.B = w + plan.a_bytes;
     a.ldb = plan.ldb_p;
   }
-  unsigned char* ws = w + plan.a_bytes + static_cast<size_t>(round_up(static_cast<int64_t>(plan.b_bytes), 256));
-  const int nkb = (a.K + 31) / 32;
-  if (plan.sa) {
-    const ll_status st = launch_repack(a.mx_sa, a.ld_mx_sa, ws, plan.ld_sa_p, a.M, nkb, 1, ctx);
+  if (plan.mx) {  // the scale codes, rearranged into the blocks the MX kernels fetch
+    unsigned char* xa = w + plan.a_bytes + static_cast<size_t>(round_up(static_cast<int64_t>(plan.b_bytes), 256));
+    const ll_status st = launch_mx_scale_tiles(a, xa, xa + plan.xa_bytes, ctx);
     if (st != LL_OK) return st;
-    a.mx_sa = ws;
-    a.ld_mx_sa = plan.ld_sa_p;
-    ws += plan.sa_bytes;
-  }
-  if (plan.sb) {
-    const ll_status st = launch_repack(a.mx_sb, a.ld_mx_sb, ws, plan.ld_sb_p, a.N, nkb, 1, ctx);
-    if (st != LL_OK) return st;
-    a.mx_sb = ws;
-    a.ld_mx_sb = plan.ld_sb_p;
+    a.mx_sat = xa;
+    a.mx_sbt = xa + plan.xa_bytes;
   }
   return launch_gemm_tc(a, ctx);
 }
@@ -287,14 +276,12 @@ ll_status gemm_common(const ll::GemmArgs& a, void* workspace, size_t ws_bytes, l
   if (a.K == 0) return ll::launch_scale_c(a, ctx);
   const ll::RepackPlan plan = ll::plan_repack(a);
   void* base = nullptr;
-  if (plan.a || plan.b || plan.sa || plan.sb) {
+  if (plan.a || plan.b || plan.mx) {
     const int es = in_esize(a.in_type);
-    const int nkb = (a.K + 31) / 32;
     size_t need = 0;
     if (plan.a) need += repack_bytes(a.M, a.K, es);
     if (plan.b) need += repack_bytes(a.K, a.N, es);
-    if (plan.sa) need += repack_bytes(a.M, nkb, 1);
-    if (plan.sb) need += repack_bytes(a.N, nkb, 1);
+    if (plan.mx) need += plan.xa_bytes + plan.xb_bytes + 512;
     if (workspace == nullptr || ws_bytes < need) return LL_ERR_WORKSPACE;
     base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
   }
@@ -341,13 +328,9 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
   return need;
 }
 
-size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int64_t ld_sa, int64_t ld_sb) {
+size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  const int nkb = (K + 31) / 32;
-  size_t need = ll_gemm_workspace_size(M, N, K, lda, ldb, LL_IN_E4M3);
-  if (ld_sa % 16 != 0) need += repack_bytes(M, nkb, 1);
-  if (ld_sb % 16 != 0) need += repack_bytes(N, nkb, 1);
-  return need;
+  return ll_gemm_workspace_size(M, N, K, lda, ldb, LL_IN_E4M3) + ll::mx_scale_block_bytes(M, N, K, nullptr) + 512;
 }
 
 static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, const void* A,
@@ -379,6 +362,8 @@ static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, co
   a.ld_mx_sa = 0;
   a.mx_sb = nullptr;
   a.ld_mx_sb = 0;
+  a.mx_sat = nullptr;
+  a.mx_sbt = nullptr;
   return a;
 }
 

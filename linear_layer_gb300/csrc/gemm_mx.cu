@@ -8,26 +8,30 @@
 // The tensor cores apply the scales themselves (tcgen05.mma kind::mxf8f6f4.block_scale),
 // so unlike the FP32 128-block path there is no software promotion between K blocks.
 //
-// One persistent CTA per SM walks 128 x 256 output tiles in the grouped order.  Roles:
-//   warp 0      operand producer: TMA copies of A (128 rows x 128 K, K-major) and B (128 K
-//               x 256 columns, N-major), 128-byte swizzle, into a 4-stage ring.
-//   warp 2      scale blocks: every four stages a TMA copy brings the next 16 K blocks of
-//               scale codes of the tile's 128 rows of A and 256 columns of B (their own
-//               K-block-contiguous layout; three group buffers, requested two groups
-//               ahead); the 32 lanes reorder each stage's codes into three 32 x 16-byte
-//               blocks (row r of a block holds at byte 4j + b the code of item 32j + r for
-//               K block b) in the stage's slot and arrive on its full barrier.
+// The scale codes are first rearranged (mx_scale_tile_kernel, into the caller's workspace)
+// into the blocks tcgen05.cp copies into TMEM: for every 128 rows of A (128 columns of B)
+// and every 128-K stage, 32 rows of 16 bytes where row r holds at byte 4j + b the code of
+// item 32j + r for the stage's K block b.  The GEMM kernels then fetch each stage's blocks
+// by TMA together with its operands, so scale codes reach shared memory the same way the
+// operands do (asynchronously, completing on the stage's barrier).  TMEM then holds, per
+// stage, A's codes with row m at lane m, column m / 32, and B's with column n at lanes
+// 32 q + n % 32 of every lane quarter q, column 4 + n / 32; the scale-factor IDs of the
+// instruction descriptor (B bits 4-5, A bits 29-30) pick K block kk's byte of those words.
+//
+// One-CTA kernel (gemm_mx_kernel): one persistent CTA per SM walks 128 x 256 output tiles
+// in the grouped order.  Roles:
+//   warp 0      producer: TMA copies of A (128 rows x 128 K, K-major) and B (128 K x 256
+//               columns, N-major), 128-byte swizzle, and of the stage's three scale blocks
+//               into a 4-stage ring.
 //   warp 1      TMEM allocator and MMA issuer.  Per stage, three tcgen05.cp copies put the
 //               scale blocks into TMEM (replicated over the four lane quarters), then four
-//               K = 32 MMAs each select their K block's byte of the scale words through
-//               the scale-factor IDs of the instruction descriptor.
-//   warps 3-10  epilogue.  They drain the tile's 128 x 256 FP32 accumulator from TMEM into
+//               K = 32 tcgen05.mma .kind::mxf8f6f4.block_scale.
+//   warps 2-9   epilogue.  They drain the tile's 128 x 256 FP32 accumulator from TMEM into
 //               registers (32 rows x 128 columns per warp), hand TMEM back at once so the
 //               next tile's MMAs run, then apply alpha / beta and store D from registers.
-// TMEM: the accumulator in columns 0-255; stage s's scales in columns 256 + 16 s: A's in
-// the first 4 (row m at lane m, column m / 32), B's in the next 8 (column n at lanes
-// 32 q + n % 32 of every quarter q, column 4 + n / 32).  Every wait is bounded; on expiry
-// the CTA records LL_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+// TMEM: the accumulator in columns 0-255; stage s's scales in columns 256 + 16 s (A's in
+// the first 4, B's in the next 8).  Every wait is bounded; on expiry the CTA records
+// LL_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
 #include <cstring>
 
 #include "gemm_common.cuh"
@@ -46,20 +50,13 @@ struct MxCfg {
   static constexpr int SF_BLOCK = 512;                                 // 32 rows x 16 bytes
   static constexpr int SF_STAGE_BYTES = 3 * SF_BLOCK;                  // A, B columns 0-127, 128-255
   static constexpr int STAGES = 4;
-  // scale codes arrive by TMA as boxes of 16 K blocks (four stages) x the tile's rows of A
-  // (128) and columns of B (256), in their natural K-block-contiguous layout, into two
-  // group buffers; the producer reorders each stage's words into the tcgen05.cp blocks
-  static constexpr int SG_KB = 16;                    // K blocks per group
-  static constexpr int SG_A = BM * SG_KB, SG_B = BN * SG_KB;
-  static constexpr int SG_BYTES = SG_A + SG_B;        // 6 KB
-  static constexpr int SG_BUFS = 3;                   // groups requested two ahead
-  static constexpr int EPI_WARP0 = 3, EPI_WARPS = 8;
+  static constexpr int EPI_WARP0 = 2, EPI_WARPS = 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   static constexpr int TMEM_COLS = 512;
   static constexpr int SF_COL0 = BN, SF_COLS = 16;
-  static constexpr int NBARS = 2 * STAGES + 3 + SG_BUFS;  // full, empty, tfull, tempty, drain, sgfull
-  static constexpr int SMEM = STAGES * (STAGE_BYTES + SF_STAGE_BYTES) + SG_BUFS * SG_BYTES + NBARS * 8 + 16 + 1024;
+  static constexpr int NBARS = 2 * STAGES + 3;  // full, empty, tfull, tempty, drain
+  static constexpr int SMEM = STAGES * (STAGE_BYTES + SF_STAGE_BYTES) + NBARS * 8 + 16 + 1024;
   static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
@@ -74,10 +71,66 @@ __host__ __device__ constexpr uint32_t make_idesc_mx(uint32_t fmts, int n, int m
 
 __host__ __device__ constexpr uint32_t sf_ids(uint32_t kk) { return (kk << 4) | (kk << 29); }
 
+// ------------------------------------------------------------------ scale blocks
+//
+// Block (blk, kb) of a code matrix (rows of K-block-contiguous codes, `ld` bytes apart)
+// holds rows 128 blk .. 128 blk + 127 and K blocks 4 kb .. 4 kb + 3: 512 bytes, 16-byte row r
+// holding at byte 4j + b the code of row 128 blk + 32j + r for K block 4 kb + b.  Codes of
+// rows past `rows` or K blocks past `nkb` are written as 127 (2^0; their operand elements
+// are zero).  Blocks are stored in the order the kernels fetch them:
+//   A (cols256 = 0): block (blk, kb) at ((blk * KB) + kb) * 512
+//   B (cols256 = 1): block (blk, kb) at (((blk / 2) * KB + kb) * 2 + blk % 2) * 512
+// so that the two blocks of a 256-column tile's stage are adjacent.  One CTA of 128
+// threads per (blk, four stages): each thread loads one row's 16 codes, the block is
+// transposed through shared memory, and each warp writes one 512-byte block.
+__global__ void __launch_bounds__(128) mx_scale_tile_kernel(const uint8_t* __restrict__ src, int64_t ld, int rows,
+                                                            int nkb, int KB, int cols256,
+                                                            uint8_t* __restrict__ dst) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ __align__(16) uint8_t sm[128 * 16];
+  const int t = threadIdx.x;
+  const int blk = blockIdx.x, g = blockIdx.y;  // g: four stages, 16 K blocks
+  const int row = blk * 128 + t;
+  const int k0 = 16 * g;
+  uint4 v = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  if (row < rows) {
+    const uint8_t* q = src + static_cast<int64_t>(row) * ld + k0;
+    if (k0 + 16 <= nkb && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
+      v = __ldg(reinterpret_cast<const uint4*>(q));
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int k = k0 + 4 * i + b;
+          x |= (k < nkb ? static_cast<uint32_t>(__ldg(q + 4 * i + b)) : 0x7Fu) << (8 * b);
+        }
+        w[i] = x;
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  *reinterpret_cast<uint4*>(sm + t * 16) = v;
+  __syncthreads();
+  const int c = t >> 5, r = t & 31;  // stage within the four, block row
+  const int kb = 4 * g + c;
+  if (kb >= KB) return;
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) o[j] = *reinterpret_cast<const uint32_t*>(sm + (32 * j + r) * 16 + 4 * c);
+  const int64_t blk_off = cols256 ? ((static_cast<int64_t>(blk / 2) * KB + kb) * 2 + (blk & 1)) * 512
+                                  : (static_cast<int64_t>(blk) * KB + kb) * 512;
+  *reinterpret_cast<uint4*>(dst + blk_off + r * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ------------------------------------------------------------------ one-CTA kernel
+
 template <uint32_t AB_FMT>
 __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                   const __grid_constant__ CUtensorMap tmXA, const __grid_constant__ CUtensorMap tmXB,
                    const GemmParams p) {
   using Cfg = MxCfg;
   constexpr int S = Cfg::STAGES;
@@ -87,8 +140,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sf_base = smem + S * Cfg::STAGE_BYTES;
-  uint8_t* sg_base = sf_base + S * Cfg::SF_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sg_base + Cfg::SG_BUFS * Cfg::SG_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_base + S * Cfg::SF_STAGE_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
   uint32_t* abort_flag = tmem_slot + 1;
 
@@ -100,17 +152,15 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   const uint32_t tfull_bar = smem_addr(bars + 2 * S);
   const uint32_t tempty_bar = smem_addr(bars + 2 * S + 1);
   const uint32_t drain_bar = smem_addr(bars + 2 * S + 2);
-  auto sgfull_bar = [&](int b) { return smem_addr(bars + 2 * S + 3 + b); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 2);  // the operand copies (with their bytes) and the scale blocks
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, Cfg::EPI_THREADS);
     mbar_init(drain_bar, 1);
-    for (int b = 0; b < Cfg::SG_BUFS; ++b) mbar_init(sgfull_bar(b), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -128,10 +178,9 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   const int num_n = (p.N + Cfg::BN - 1) / Cfg::BN;
   const int num_tiles = num_m * num_n;
   const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;  // stages per tile
-  const int NG = (KB + 3) / 4;                   // scale groups per tile (16 K blocks each)
 
   // programmatic dependent launch: L2 prefetch of the first ring of operand tiles, then
-  // the wait for the previous kernel of the stream (scales, C and D come after it)
+  // the wait for the previous kernel of the stream (scale blocks, C and D come after it)
   if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < num_tiles) {
     int mb, nb;
     tile_coords(blockIdx.x, num_m, num_n, p.group_m, mb, nb);
@@ -144,10 +193,12 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- operand producer
+    // ---------------------------------------------------------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmXA);
+      tma_prefetch_desc(&tmXB);
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -161,12 +212,15 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           }
           uint8_t* a_s = smem + s * Cfg::STAGE_BYTES;
           uint8_t* b_s = a_s + Cfg::A_BYTES;
-          mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
+          uint8_t* sf = sf_base + s * Cfg::SF_STAGE_BYTES;
+          mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES + Cfg::SF_STAGE_BYTES);
           tma_load_2d(smem_addr(a_s), &tmA, full_bar(s), kb * Cfg::BK, mb * Cfg::BM);
 #pragma unroll
           for (int j = 0; j < Cfg::B_BOXES; ++j)
             tma_load_2d(smem_addr(b_s + j * Cfg::B_BOX_BYTES), &tmB, full_bar(s), nb * Cfg::BN + j * Cfg::B_BOX_N,
                         kb * Cfg::BK);
+          tma_load_2d(smem_addr(sf), &tmXA, full_bar(s), 0, (mb * KB + kb) * 32);
+          tma_load_2d(smem_addr(sf + Cfg::SF_BLOCK), &tmXB, full_bar(s), 0, (nb * KB + kb) * 64);
           ++it;
         }
       }
@@ -174,83 +228,6 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0u); j < it; ++j)
           wait_drain(full_bar(j % S), (j / S) & 1u, p.timeout_ns);
       }
-    }
-  } else if (warp == 2) {
-    // ---------------------------------------------------------------- scale blocks
-    // This CTA's stages in order: stage i is K block i % KB of its (i / KB)-th tile.  Scale
-    // group g (this CTA's g-th run of four stages of one tile) lands in buffer g % 3 and is
-    // requested two groups ahead, so it is in place when its first stage comes.
-    if (lane == 0) {
-      tma_prefetch_desc(&tmSA);
-      tma_prefetch_desc(&tmSB);
-    }
-    const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
-                             ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                                   static_cast<int>(gridDim.x)
-                             : 0;
-    const uint32_t total = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(KB);
-    const uint32_t groups = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(NG);
-    uint32_t g_requested = 0, g_waited = 0;  // scale groups requested / seen complete
-    auto request_group = [&](uint32_t g) {  // lane 0
-      if (g >= groups) return;
-      g_requested = g + 1;
-      int mb, nb;
-      tile_coords(blockIdx.x + static_cast<int>(g / NG) * gridDim.x, num_m, num_n, p.group_m, mb, nb);
-      const int x = static_cast<int>(g % NG) * Cfg::SG_KB;  // first K block (a multiple of 16 bytes)
-      uint8_t* buf = sg_base + (g % Cfg::SG_BUFS) * Cfg::SG_BYTES;
-      const uint32_t bar = sgfull_bar(g % Cfg::SG_BUFS);
-      mbar_arrive_expect_tx(bar, Cfg::SG_BYTES);
-      tma_load_2d(smem_addr(buf), &tmSA, bar, x, mb * Cfg::BM);
-      tma_load_2d(smem_addr(buf + Cfg::SG_A), &tmSB, bar, x, nb * Cfg::BN);
-    };
-    if (lane == 0) {
-      request_group(0);
-      request_group(1);
-    }
-    bool ok = true;
-    for (uint32_t i = 0; i < total && ok; ++i) {
-      const int kb = static_cast<int>(i % KB);
-      const uint32_t g = (i / KB) * NG + kb / 4;
-      const int c = kb & 3;  // stage within the group
-      const uint8_t* grp = sg_base + (g % Cfg::SG_BUFS) * Cfg::SG_BYTES;
-      if (c == 0) {
-        bool ok_g = wait_bounded(sgfull_bar(g % Cfg::SG_BUFS), (g / Cfg::SG_BUFS) & 1u, wctx, kRoleProducer);
-        ok_g = __all_sync(0xffffffffu, ok_g);
-        if (!ok_g) {
-          ok = false;
-          break;
-        }
-        g_waited = g + 1;
-        fence_proxy_async_smem();  // every lane's reads of buffer (g + 2) % 3 (group g - 1) ...
-        __syncwarp();
-        if (lane == 0) request_group(g + 2);  // ... come before its refill
-      }
-      // this stage's words: K blocks 4c .. 4c + 3 of the group for row 32 j + lane of A and
-      // column 32 j + lane of B (group rows are 16 bytes: K blocks 0-15 of the group)
-      uint32_t w[12];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[j] = *reinterpret_cast<const uint32_t*>(grp + (32 * j + lane) * 16 + 4 * c);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        w[4 + j] = *reinterpret_cast<const uint32_t*>(grp + Cfg::SG_A + (32 * j + lane) * 16 + 4 * c);
-      const int s = i % S;
-      bool ok_w = wait_bounded(empty_bar(s), ((i / S) & 1u) ^ 1u, wctx, kRoleProducer);
-      ok_w = __all_sync(0xffffffffu, ok_w);
-      if (!ok_w) {
-        ok = false;
-        break;
-      }
-      uint8_t* sf = sf_base + s * Cfg::SF_STAGE_BYTES;
-      *reinterpret_cast<uint4*>(sf + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(sf + Cfg::SF_BLOCK + lane * 16) = make_uint4(w[4], w[5], w[6], w[7]);
-      *reinterpret_cast<uint4*>(sf + 2 * Cfg::SF_BLOCK + lane * 16) = make_uint4(w[8], w[9], w[10], w[11]);
-      fence_proxy_async_smem();  // the generic-proxy writes, for tcgen05.cp's reads
-      __syncwarp();
-      if (lane == 0) mbar_arrive(full_bar(s));
-    }
-    if (!ok && lane == 0) {  // scale groups still in flight land before the CTA may exit
-      for (uint32_t g = g_waited; g < g_requested; ++g)
-        wait_drain(sgfull_bar(g % Cfg::SG_BUFS), (g / Cfg::SG_BUFS) & 1u, p.timeout_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- scale copies + MMA issuer
@@ -332,6 +309,246 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// Large problems run on CTA pairs (2-CTA clusters): a pair owns a 256 x 256 output tile;
+// CTA r loads rows 128 r .. 128 r + 127 of the tile's A and columns 128 r .. 128 r + 127
+// of its B (one 128-byte-swizzled box per stage), and the even CTA's MMA thread issues
+// tcgen05.mma.cta_group::2 (M = 256).  Per SM that halves the B bytes TMA writes into
+// shared memory and the tensor cores read back (the one-CTA tile moves 96 KB through
+// shared memory per 128-K stage, which bounds it).  Each CTA's TMEM must hold the scales of
+// its own 128 rows of A and of all 256 columns of B (in the one-CTA layout), so each CTA's
+// producer fetches exactly those blocks into its own shared memory, completing on the even
+// CTA's stage barrier with the operands, and one tcgen05.cp.cta_group::2 from the even CTA
+// copies both CTAs' blocks into their own TMEM.
+//   full[s]   (even CTA)  count 1: the even CTA's producer arms it with both CTAs' bytes
+//   empty[s], tfull       (each CTA) count 1: the MMA commits, multicast to both CTAs
+//   tempty    (even CTA)  one relaxed arrival per epilogue warp of each CTA (16)
+struct Mx2Cfg {
+  static constexpr int BM = 128;                 // rows per CTA (the pair tile has 256)
+  static constexpr int BN = 256;                 // columns of the pair tile
+  static constexpr int BK = 128;
+  static constexpr int UMMA_K = 32, KSTEPS = 4;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_HALF = BN / 2;          // columns of B in each CTA
+  static constexpr int B_BYTES = BK * 128;       // one 128-column box
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+  static constexpr int SF_BLOCK = 512;
+  static constexpr int SF_STAGE_BYTES = 3 * SF_BLOCK;
+  static constexpr int STAGES = 6;
+  static constexpr int EPI_WARP0 = 2, EPI_WARPS = 8;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SF_COL0 = BN, SF_COLS = 16;
+  static constexpr int NBARS = 2 * STAGES + 3;
+  static constexpr int SMEM = STAGES * (STAGE_BYTES + SF_STAGE_BYTES) + NBARS * 8 + 16 + 1024;
+  static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+template <uint32_t AB_FMT>
+__global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
+    gemm_mx2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmXA, const __grid_constant__ CUtensorMap tmXB,
+                    const GemmParams p) {
+  using Cfg = Mx2Cfg;
+  constexpr int S = Cfg::STAGES;
+  constexpr uint32_t IDESC = make_idesc_mx(AB_FMT, Cfg::BN, 2 * Cfg::BM);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sf_base = smem + S * Cfg::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf_base + S * Cfg::SF_STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NBARS);
+  uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t rank = cluster_ctarank();
+  const int rank_i = static_cast<int>(rank);
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  auto full_bar = [&](int s) { return smem_addr(bars + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + S + s); };
+  const uint32_t tfull_bar = smem_addr(bars + 2 * S);
+  const uint32_t tempty_bar = smem_addr(bars + 2 * S + 1);
+  const uint32_t drain_bar = smem_addr(bars + 2 * S + 2);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 2 * Cfg::EPI_WARPS);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  WaitCtx wctx{p.status, p.timeout_ns, abort_flag};
+  const int num_m2 = (p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM);
+  const int num_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+  const int num_tiles = num_m2 * num_n;
+  const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;
+
+  if (warp == 0 && lane == 0 && pair < num_tiles) {
+    int mb, nb;
+    tile_coords(pair, num_m2, num_n, p.group_m, mb, nb);
+    const int pre = KB < S ? KB : S;
+    for (int kb = 0; kb < pre; ++kb) {
+      tma_prefetch_l2(&tmA, kb * Cfg::BK, mb * 2 * Cfg::BM + Cfg::BM * rank_i);
+      tma_prefetch_l2(&tmB, nb * Cfg::BN + Cfg::B_HALF * rank_i, kb * Cfg::BK);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer (each CTA)
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmXA);
+      tma_prefetch_desc(&tmXB);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = pair; u < num_tiles && ok; u += num_pairs) {
+        int mb, nb;
+        tile_coords(u, num_m2, num_n, p.group_m, mb, nb);
+        const int ablk = 2 * mb + rank_i;  // this CTA's 128-row block of A
+        for (int kb = 0; kb < KB; ++kb) {
+          const int s = it % S;
+          if (!wait_bounded(empty_bar(s), ((it / S) & 1u) ^ 1u, wctx, kRoleProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t cfull = mapa_cluster(full_bar(s), 0);
+          uint8_t* a_s = smem + s * Cfg::STAGE_BYTES;
+          uint8_t* sf = sf_base + s * Cfg::SF_STAGE_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * (Cfg::STAGE_BYTES + Cfg::SF_STAGE_BYTES));
+          tma_load_2d_pair(smem_addr(a_s), &tmA, cfull, kb * Cfg::BK, ablk * Cfg::BM);
+          tma_load_2d_pair(smem_addr(a_s + Cfg::A_BYTES), &tmB, cfull, nb * Cfg::BN + Cfg::B_HALF * rank_i,
+                           kb * Cfg::BK);
+          tma_load_2d_pair(smem_addr(sf), &tmXA, cfull, 0, (ablk * KB + kb) * 32);
+          tma_load_2d_pair(smem_addr(sf + Cfg::SF_BLOCK), &tmXB, cfull, 0, (nb * KB + kb) * 64);
+          ++it;
+        }
+      }
+      if (!ok && rank == 0) {  // the even CTA's full barriers see both CTAs' copies
+        for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0u); j < it; ++j)
+          wait_drain(full_bar(j % S), (j / S) & 1u, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- scale copies + MMA (even CTA)
+    if (lane == 0 && rank == 0) {
+      uint32_t it = 0, tiles = 0;
+      bool ok = true;
+      for (int u = pair; u < num_tiles && ok; u += num_pairs) {
+        if (!wait_bounded(tempty_bar, (tiles & 1u) ^ 1u, wctx, kRoleMma)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          const int s = it % S;
+          if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_COLS;
+          const uint32_t sf_s = smem_addr(sf_base + s * Cfg::SF_STAGE_BYTES);
+          tmem_cp_32x128b_x4_pair(sf_t, smem_desc_plain16(sf_s));
+          tmem_cp_32x128b_x4_pair(sf_t + 4, smem_desc_plain16(sf_s + Cfg::SF_BLOCK));
+          tmem_cp_32x128b_x4_pair(sf_t + 8, smem_desc_plain16(sf_s + 2 * Cfg::SF_BLOCK));
+          const uint32_t a_base = smem_addr(smem + s * Cfg::STAGE_BYTES);
+          const uint32_t b_base = a_base + Cfg::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BYTES, 1024);
+            mma_mxf8_pair(tmem_base, adesc, bdesc, IDESC | sf_ids(kk), sf_t, sf_t + 4,
+                          (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_pair_mc(empty_bar(s), 0x3);
+          ++it;
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(tfull_bar, 0x3);
+        ++tiles;
+      }
+      mma_commit_pair(drain_bar);
+      wait_drain(drain_bar, 0u, p.timeout_ns);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (each CTA)
+    const int ew = warp - Cfg::EPI_WARP0;
+    const int q = warp & 3;
+    const int h = ew >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t tiles = 0;
+    for (int u = pair; u < num_tiles; u += num_pairs) {
+      int mb, nb;
+      tile_coords(u, num_m2, num_n, p.group_m, mb, nb);
+      const int m = mb * 2 * Cfg::BM + Cfg::BM * rank_i + q * 32 + lane;
+      const int ncol0 = nb * Cfg::BN + h * (Cfg::BN / 2);
+      bool w = wait_bounded(tfull_bar, tiles & 1u, wctx, kRoleEpilogue);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(tmem_base + lane_base + h * (Cfg::BN / 2) + c * 32, v[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(v[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar, 0));
+      float acc[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[c][j] = __uint_as_float(v[c][j]);
+      epilogue_rows<4>(p, m, ncol0, acc);
+      ++tiles;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+// Tensor maps of the operands and of the two scale-block arrays (16-byte rows).
+template <class Cfg>
+bool mx_maps(const GemmArgs& a, int a_box_rows, int b_box_cols, CUtensorMap* tmA, CUtensorMap* tmB,
+             CUtensorMap* tmXA, CUtensorMap* tmXB) {
+  const int64_t KB = (a.K + 127) / 128;
+  const int64_t xa_rows = ((a.M + 127) / 128) * KB * 32;
+  const int64_t xb_rows = ((a.N + 255) / 256) * KB * 64;
+  return make_tensor_map_2d(tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.M, a.K, a.lda, Cfg::BK, a_box_rows) &&
+         make_tensor_map_2d(tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.K, a.N, a.ldb, b_box_cols, Cfg::BK) &&
+         make_tensor_map_2d(tmXA, a.mx_sat, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xa_rows, 16, 16, 16, 32,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         make_tensor_map_2d(tmXB, a.mx_sbt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xb_rows, 16, 16, 16, 64,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 template <uint32_t F>
 ll_status run_mx(const GemmArgs& a, const LaunchCtx& ctx) {
   using Cfg = MxCfg;
@@ -340,20 +557,8 @@ ll_status run_mx(const GemmArgs& a, const LaunchCtx& ctx) {
     cudaGetLastError();
     return LL_ERR_CUDA;
   }
-  CUtensorMap tmA, tmB;
-  if (!make_tensor_map_2d(&tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.M, a.K, a.lda, Cfg::BK, Cfg::BM))
-    return LL_ERR_CUDA;
-  if (!make_tensor_map_2d(&tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.K, a.N, a.ldb, Cfg::B_BOX_N, Cfg::BK))
-    return LL_ERR_CUDA;
-  // scale codes: K-block-contiguous rows with 16-byte-multiple pitches (repacked otherwise)
-  const int64_t nkb = (a.K + 31) / 32;
-  CUtensorMap tmSA, tmSB;
-  if (!make_tensor_map_2d(&tmSA, a.mx_sa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.M, nkb, a.ld_mx_sa, Cfg::SG_KB, Cfg::BM,
-                          CU_TENSOR_MAP_SWIZZLE_NONE))
-    return LL_ERR_CUDA;
-  if (!make_tensor_map_2d(&tmSB, a.mx_sb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.N, nkb, a.ld_mx_sb, Cfg::SG_KB, Cfg::BN,
-                          CU_TENSOR_MAP_SWIZZLE_NONE))
-    return LL_ERR_CUDA;
+  CUtensorMap tmA, tmB, tmXA, tmXB;
+  if (!mx_maps<Cfg>(a, Cfg::BM, Cfg::B_BOX_N, &tmA, &tmB, &tmXA, &tmXB)) return LL_ERR_CUDA;
   const GemmParams p = make_gemm_params(a, ctx);
   const int num_tiles = ((a.M + Cfg::BM - 1) / Cfg::BM) * ((a.N + Cfg::BN - 1) / Cfg::BN);
   cudaLaunchConfig_t cfg = {};
@@ -366,7 +571,52 @@ ll_status run_mx(const GemmArgs& a, const LaunchCtx& ctx) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSA, tmSB, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmXA, tmXB, p) != cudaSuccess) {
+    cudaGetLastError();
+    return LL_ERR_CUDA;
+  }
+  return LL_OK;
+}
+
+template <uint32_t F>
+ll_status run_mx2(const GemmArgs& a, const LaunchCtx& ctx) {
+  using Cfg = Mx2Cfg;
+  auto kern = gemm_mx2_kernel<F>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess) {
+    cudaGetLastError();
+    return LL_ERR_CUDA;
+  }
+  CUtensorMap tmA, tmB, tmXA, tmXB;
+  if (!mx_maps<Cfg>(a, Cfg::BM, Cfg::B_HALF, &tmA, &tmB, &tmXA, &tmXB)) return LL_ERR_CUDA;
+  const GemmParams p = make_gemm_params(a, ctx);
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  // co-resident CTA pairs (one CTA per SM): the persistent grid
+  static int max_pairs[64] = {};
+  if (ctx.device < 0 || ctx.device >= 64) return LL_ERR_NO_DEVICE;
+  if (max_pairs[ctx.device] == 0) {
+    cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = ctx.num_sms / 2;
+    }
+    max_pairs[ctx.device] = n;
+  }
+  const int tiles = ((a.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((a.N + Cfg::BN - 1) / Cfg::BN);
+  cfg.gridDim = dim3(2 * (tiles < max_pairs[ctx.device] ? tiles : max_pairs[ctx.device]));
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmXA, tmXB, p) != cudaSuccess) {
     cudaGetLastError();
     return LL_ERR_CUDA;
   }
@@ -375,8 +625,37 @@ ll_status run_mx(const GemmArgs& a, const LaunchCtx& ctx) {
 
 }  // namespace
 
+size_t mx_scale_block_bytes(int M, int N, int K, size_t* a_bytes) {
+  const size_t KB = static_cast<size_t>((K + 127) / 128);
+  const size_t xa = static_cast<size_t>((M + 127) / 128) * KB * 512;
+  const size_t xb = static_cast<size_t>((N + 255) / 256) * KB * 1024;
+  if (a_bytes) *a_bytes = xa;
+  return xa + xb;
+}
+
+ll_status launch_mx_scale_tiles(const GemmArgs& a, uint8_t* xa, uint8_t* xb, const LaunchCtx& ctx) {
+  const int KB = (a.K + 127) / 128;
+  const int nkb = (a.K + 31) / 32;
+  const int G = (KB + 3) / 4;
+  mx_scale_tile_kernel<<<dim3((a.M + 127) / 128, G), 128, 0, ctx.stream>>>(a.mx_sa, a.ld_mx_sa, a.M, nkb, KB, 0, xa);
+  if (cudaGetLastError() != cudaSuccess) return LL_ERR_CUDA;
+  // B: every 128-column block of each 256-column tile (a block past N gets neutral codes)
+  mx_scale_tile_kernel<<<dim3(2 * ((a.N + 255) / 256), G), 128, 0, ctx.stream>>>(a.mx_sb, a.ld_mx_sb, a.N, nkb, KB, 1,
+                                                                                 xb);
+  return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
 ll_status launch_gemm_mx(const GemmArgs& a, const LaunchCtx& ctx) {
   const bool a5 = a.in_type == LL_IN_E5M2, b5 = a.b_type == LL_IN_E5M2;
+  // CTA pairs once there are enough 256 x 256 tiles to occupy a quarter of the SM pairs;
+  // the one-CTA kernel below that
+  const int pair_tiles = ((a.M + 255) / 256) * ((a.N + 255) / 256);
+  if (pair_tiles >= ctx.num_sms / 4) {
+    if (!a5 && !b5) return run_mx2<fmt_pair(0, 0)>(a, ctx);
+    if (a5 && b5) return run_mx2<fmt_pair(1, 1)>(a, ctx);
+    if (!a5) return run_mx2<fmt_pair(0, 1)>(a, ctx);
+    return run_mx2<fmt_pair(1, 0)>(a, ctx);
+  }
   if (!a5 && !b5) return run_mx<fmt_pair(0, 0)>(a, ctx);
   if (a5 && b5) return run_mx<fmt_pair(1, 1)>(a, ctx);
   if (!a5) return run_mx<fmt_pair(0, 1)>(a, ctx);

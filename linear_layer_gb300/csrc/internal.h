@@ -41,6 +41,8 @@ struct GemmArgs {
   int64_t ld_mx_sa;
   const uint8_t* mx_sb;   // MX: N x ld_mx_sb scale codes of B, one per column and K block
   int64_t ld_mx_sb;
+  const uint8_t* mx_sat;  // MX: the scale codes rearranged into tcgen05.cp blocks (workspace)
+  const uint8_t* mx_sbt;
 };
 
 // Launch context of the current device (status word, SM count, wait limit) for `stream`;
@@ -72,17 +74,16 @@ ll_status validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes);
 
 // Where the operand repack of a GEMM puts A and B: A (when repacked) at the 256-byte-
 // aligned start of the scratch, B after it.  a_bytes = roundup(M * lda_p * esize, 256)
-// and b_bytes = K * ldb_p * esize with the pitches rounded up to 16 bytes; MX scale
-// codes follow B (each region rounded up to 256 bytes).
+// and b_bytes = K * ldb_p * esize with the pitches rounded up to 16 bytes; the MX scale
+// blocks follow B (at a 256-byte boundary).
 struct RepackPlan {
   bool a, b;
   int64_t lda_p, ldb_p;  // elements
   size_t a_bytes, b_bytes;
-  // MX scale codes (bytes, K-block-contiguous rows): repacked to 16-byte pitches after B,
-  // each at a 256-byte boundary, when their base or pitch is not 16-byte aligned
-  bool sa, sb;
-  int64_t ld_sa_p, ld_sb_p;
-  size_t sa_bytes, sb_bytes;
+  // MX: the scale codes rearranged into the blocks tcgen05.cp copies (always), after B at a
+  // 256-byte boundary: A's blocks (xa_bytes), then B's (xb_bytes)
+  bool mx;
+  size_t xa_bytes, xb_bytes;
 };
 RepackPlan plan_repack(const GemmArgs& a);
 
@@ -94,8 +95,13 @@ ll_status launch_gemm_planned(GemmArgs a, const RepackPlan& plan, void* scratch,
 ll_status launch_gemm_tc(const GemmArgs& a, const LaunchCtx& ctx);
 
 // MX block-scaled 8-bit GEMM on tcgen05 with hardware block scaling (gemm_mx.cu); the same
-// operand requirements.
+// operand requirements, and a.mx_sat / a.mx_sbt holding the scale blocks.
 ll_status launch_gemm_mx(const GemmArgs& a, const LaunchCtx& ctx);
+
+// Bytes of the MX scale blocks of an M x N x K problem (A's in *a_bytes when not NULL), and
+// the kernel that writes them from a.mx_sa / a.mx_sb into xa / xb (gemm_mx.cu).
+size_t mx_scale_block_bytes(int M, int N, int K, size_t* a_bytes);
+ll_status launch_mx_scale_tiles(const GemmArgs& a, uint8_t* xa, uint8_t* xb, const LaunchCtx& ctx);
 
 // D = beta * C (or 0) for K == 0 (aux.cu).
 ll_status launch_scale_c(const GemmArgs& a, const LaunchCtx& ctx);

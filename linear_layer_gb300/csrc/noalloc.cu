@@ -85,6 +85,8 @@ extern "C" ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const
   a.ld_mx_sa = 0;
   a.mx_sb = nullptr;
   a.ld_mx_sb = 0;
+  a.mx_sat = nullptr;
+  a.mx_sbt = nullptr;
 
   // the same argument rules as ll_gemm_f16 (the scratch cannot alias caller memory)
   ll_status st = ll::validate_gemm(a, nullptr, 0);

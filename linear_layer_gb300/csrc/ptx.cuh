@@ -63,6 +63,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// As mbar_try_wait, with acquire semantics at cluster scope: writes that other CTAs of the
+// cluster ordered before their release arrivals on this barrier are visible afterwards.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Shared context of the bounded waits of one CTA.
 struct WaitCtx {
   uint32_t* status;          // device status word (global)
@@ -82,6 +96,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*ctx.abort) return false;
+      if (global_timer_ns() - t0 > ctx.timeout_ns) {
+        atomicCAS(ctx.status, 0u, kStatusTimeout | (role << 8));
+        *ctx.abort = 1u;
+        __threadfence_block();
+        return false;
+      }
+    }
+  }
+}
+
+// wait_bounded with cluster-scope acquire (see mbar_try_wait_cluster).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, const WaitCtx& ctx,
+                                                     uint32_t role) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (*ctx.abort) return false;
       if (global_timer_ns() - t0 > ctx.timeout_ns) {
@@ -129,6 +162,12 @@ __device__ __forceinline__ void cluster_sync() {
 // would first wait for all of the thread's outstanding memory operations.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cbar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
+// Release arrival at cluster scope on a barrier that may be another CTA's: the calling
+// thread's earlier memory writes (and proxy fences) are ordered before it.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA / bulk copies
@@ -307,6 +346,25 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint6
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
+}
+
+// CTA-pair form of mma_mxf8 (M = 256 over the pair; each CTA's TMEM holds its 128 rows of
+// D, the scales of its own 128 rows of A and those of all N columns of B).
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// CTA-pair form of tmem_cp_32x128b_x4: issued by one thread of the even CTA, it copies each
+// CTA's own block (same shared-memory offset) into its own TMEM (same columns).
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Copy a 32-row x 16-byte shared-memory block into TMEM columns taddr .. taddr + 3 of all

@@ -244,6 +244,32 @@ def check_layer_output_overlap(ll):
     assert q(4, 64, P, 64, P + 0x100000, 64, P + 0x100000 + 8, None) == E   # scale over q
 
 
+@check
+def check_mx_gemm(ll):
+    """ll_gemm_mxf8: element types, scale pointers and pitches, and the workspace it always
+    needs for the rearranged scale codes."""
+    E = ll.LL_ERR_INVALID_ARG
+    f = ll.lib.ll_gemm_mxf8
+    Q, SA, SB, WS = P + 0x100000, P + 0x200000, P + 0x300000, P + 0x400000
+    need = ll.lib.ll_gemm_mxf8_workspace_size(64, 64, 100, 100, 64)
+    assert need >= 64 * 4 * 512 // 64  # scale blocks of one 128-row block of A and 256 columns of B
+
+    def call(at=2, bt=2, K=100, ld_sa=4, ld_sb=4, sa=SA, sb=SB, ws=WS, wsb=None, D=Q):
+        return f(at, bt, 64, 64, K, 1.0, P, K, sa, ld_sa, P, 64, sb, ld_sb, 0.0, None, 64, D, 64, ll.OUT_BF16, ws,
+                 need if wsb is None else wsb, None)
+    assert call(at=0) == E                  # FP16 is not an MX element type here
+    assert call(bt=7) == E
+    assert call(sa=None) == E
+    assert call(ld_sb=3) == E               # ceil(100 / 32) = 4 K blocks per row of scales
+    # a missing or short workspace is reported after the device check (as for a repack)
+    assert _no_device(ll, call(ws=None, wsb=0))
+    assert _no_device(ll, call(wsb=need - 1))
+    assert call(D=SA + 2) == E              # D over scale_a
+    assert call(ws=P + 0x10) == E           # workspace over A
+    assert _no_device(ll, call())
+    assert _no_device(ll, call(K=0, ws=None, wsb=0))  # K == 0: D = beta * C, no workspace
+
+
 @pytest.mark.parametrize("name", CHECKS)
 def test_host_check_in_device_less_child(child_results, name):
     line = child_results.get(name)

@@ -2,7 +2,9 @@
 tensor cores) against the CPU oracle, every element, at the FP8 tolerance bar: tails in M, N
 and K (K not a multiple of 32 or 128), padded operand and scale pitches, TMA-illegal pitches
 (repacked), scale matrices whose rows do not start on 4-byte boundaries, alpha / beta and
-every output type, E4M3 and E5M2 elements, and the full-size 8192^3 workload."""
+every output type, E4M3 and E5M2 elements, both kernels (one CTA per 128 x 256 tile for
+small problems, CTA pairs per 256 x 256 tile for large ones), and the full-size 8192^3
+workload."""
 import numpy as np
 import pytest
 import torch
@@ -32,9 +34,7 @@ def run_mx(orc, M, N, K, alpha=1.0, beta=0.0, out="bf16", pad=0, spad=0, soff=0,
     tSA[soff:soff + SAp.size] = up(SAp.ravel())
     tSB = torch.empty(SBp.size + 16, dtype=torch.uint8, device="cuda")
     tSB[soff:soff + SBp.size] = up(SBp.ravel())
-    # scale rows off a 16-byte boundary are repacked: query with pitch 1 for that worst case
-    ld_q = ld_s if soff == 0 else 1
-    need = ll.gemm_mxf8_workspace_size(M, N, K, lda, ldb, ld_q, ld_q)
+    need = ll.gemm_mxf8_workspace_size(M, N, K, lda, ldb)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
     code = {"e4m3": ll.IN_E4M3, "e5m2": ll.IN_E5M2}
     ll.gemm_mxf8(code[a_fmt], code[b_fmt], M, N, K, alpha, up(A), lda, tSA.data_ptr() + soff, ld_s, up(B), ldb,
@@ -73,8 +73,8 @@ def test_mx_padded_and_repacked_pitches(orc):
 
 
 def test_mx_unaligned_scale_rows(orc):
-    # scale matrices 1 and 3 bytes past an aligned start, or with pitches that are not a
-    # multiple of 16 bytes, are repacked into the workspace; 16-byte pitches are read in place
+    # scale matrices 1 and 3 bytes past an aligned start, pitches that are not a multiple of
+    # 16 bytes, and 16-byte pitches (read with 16-byte loads when rearranged)
     run_mx(orc, 130, 260, 384, spad=1, soff=1)
     run_mx(orc, 130, 260, 384, spad=0, soff=3)
     run_mx(orc, 130, 260, 384, spad=5)
@@ -84,6 +84,34 @@ def test_mx_unaligned_scale_rows(orc):
 def test_mx_many_tiles(orc):
     # more tiles than SMs (several per CTA) with M and N tails
     run_mx(orc, 2000, 3000, 512, beta=1.0, out="f32", seed=5)
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,out,a_fmt,b_fmt,spad", [
+    (2100, 2600, 777, 0.5, -1.25, "f32", "e4m3", "e4m3", 0),
+    (4096, 2048, 1024, 1.0, 0.0, "bf16", "e5m2", "e4m3", 0),
+    (1999, 4100, 256, 1.0, 1.0, "f16", "e4m3", "e5m2", 3),
+    (2304, 2304, 4096, 1.0, 0.0, "bf16", "e4m3", "e4m3", 0)])
+def test_mx_pair_kernel(orc, M, N, K, alpha, beta, out, a_fmt, b_fmt, spad):
+    """Sizes with at least a quarter of the SM pairs' worth of 256 x 256 tiles run on CTA
+    pairs: M tails inside the odd CTA's rows, N tails inside a column half, K tails, mixed
+    element formats, alpha / beta, every output type, repacked scale matrices."""
+    run_mx(orc, M, N, K, alpha, beta, out, spad=spad, a_fmt=a_fmt, b_fmt=b_fmt, seed=11)
+
+
+def test_mx_needs_workspace():
+    """The rearranged scale codes always need workspace: a call without it, or with too
+    little, is rejected before anything runs."""
+    import linear_layer_gb300 as ll
+    M = N = K = 256
+    t = torch.zeros(M * K, dtype=torch.uint8, device="cuda")
+    s = torch.full((M * 8,), 127, dtype=torch.uint8, device="cuda")
+    D = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    need = ll.gemm_mxf8_workspace_size(M, N, K, K, N)
+    for ws in (None, torch.empty(need - 1, dtype=torch.uint8, device="cuda")):
+        with pytest.raises(ll.LLError) as e:
+            ll.gemm_mxf8(ll.IN_E4M3, ll.IN_E4M3, M, N, K, 1.0, t, K, s, 8, t, N, s, 8, 0.0, None, N, D, N,
+                         ll.OUT_BF16, workspace=ws)
+        assert e.value.status == ll.LL_ERR_WORKSPACE
 
 
 def test_mx_deterministic(orc):
