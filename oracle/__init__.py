@@ -22,6 +22,8 @@ Functions and the passages they follow:
   one E8M0 scale 2^(e-127) shared by 32 consecutive K elements of a row of A or a
   column of B, scales stored K-block-contiguous per row of A / column of B (the pages
   name the formats only).
+* ``decode_e2m1`` / ``decode_ue4m3`` / ``gemm_nvf4`` -- the same table: FP4 E2M1 elements
+  in blocks of 16 along K sharing one UE4M3 scale (NVFP4), B given K-major.
 * ``gemv_w8a8`` -- "NVIDIA A100: chip to SIMT", sections 5.1-5.2: int8 x int8
   summed exactly, then y = fp16(float(z) * s_x * s_W[o]).
 * ``quantize_per_token_f16`` -- same page, 5.1: the activation is quantised per token
@@ -52,6 +54,10 @@ def lib():
         L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
         L.orc_decode_e5m2.restype = ctypes.c_double
         L.orc_decode_e5m2.argtypes = [ctypes.c_uint8]
+        L.orc_decode_e2m1.restype = ctypes.c_double
+        L.orc_decode_e2m1.argtypes = [ctypes.c_uint8]
+        L.orc_decode_ue4m3.restype = ctypes.c_double
+        L.orc_decode_ue4m3.argtypes = [ctypes.c_uint8]
         L.orc_decode_ue8m0.restype = ctypes.c_double
         L.orc_decode_ue8m0.argtypes = [ctypes.c_uint8]
         L.orc_encode_f16_rn.restype = ctypes.c_uint16
@@ -74,6 +80,9 @@ def lib():
         L.orc_gemm_mx_f8.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_double, vp, i64, vp, i64, vp, i64, vp, i64, ctypes.c_double, vp,
                                      i64, vp, ctypes.c_int, vp, vp]
+        L.orc_gemm_nvf4.restype = ctypes.c_int
+        L.orc_gemm_nvf4.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, vp, i64, vp, i64,
+                                    vp, i64, vp, i64, ctypes.c_double, vp, i64, vp, ctypes.c_int, vp, vp]
         L.orc_quantize_per_token_f16.restype = ctypes.c_int
         L.orc_quantize_per_token_f16.argtypes = [ctypes.c_int, ctypes.c_int, vp, i64, vp, i64, vp]
         L.orc_gemv_w8a8_ex.restype = ctypes.c_int
@@ -111,6 +120,14 @@ def decode_e4m3(bits: int) -> float:
 
 def decode_e5m2(bits: int) -> float:
     return lib().orc_decode_e5m2(int(bits) & 0xFF)
+
+
+def decode_e2m1(bits: int) -> float:
+    return lib().orc_decode_e2m1(int(bits) & 0xF)
+
+
+def decode_ue4m3(bits: int) -> float:
+    return lib().orc_decode_ue4m3(int(bits) & 0xFF)
 
 
 def decode_ue8m0(bits: int) -> float:
@@ -207,6 +224,26 @@ def gemm_mx_f8(a_fmt, b_fmt, M, N, K, alpha, A, lda, SA, ld_sa, B, ldb, SB, ld_s
                               _ptr(D), _ptr(S))
     if rc != 0:
         raise ValueError("orc_gemm_mx_f8 failed with code %d" % rc)
+    return D, S
+
+
+def gemm_nvf4(M, N, K, alpha, A, lda, SA, ld_sa, Bt, ldbt, SB, ld_sb, beta=0.0, C=None, ldc=0, rows=None,
+              want_absab=True):
+    """NVFP4 GEMM: E2M1 codes packed two per byte (A M x lda elements, Bt N x ldbt elements,
+    Bt row j = column j of B), UE4M3 scale codes per 16 K elements (SA M x ld_sa, SB N x
+    ld_sb).  Returns (D double [len(rows), N], absab)."""
+    rows = _rows(M, rows)
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    Bt = np.ascontiguousarray(Bt, dtype=np.uint8)
+    SA = np.ascontiguousarray(SA, dtype=np.uint8)
+    SB = np.ascontiguousarray(SB, dtype=np.uint8)
+    C = None if C is None else np.ascontiguousarray(C, dtype=np.float32)
+    D = np.zeros((len(rows), N), dtype=np.float64)
+    S = np.zeros((len(rows), N), dtype=np.float64) if want_absab else None
+    rc = lib().orc_gemm_nvf4(M, N, K, float(alpha), _ptr(A), lda, _ptr(SA), ld_sa, _ptr(Bt), ldbt, _ptr(SB), ld_sb,
+                             float(beta), _ptr(C), ldc, _ptr(rows), len(rows), _ptr(D), _ptr(S))
+    if rc != 0:
+        raise ValueError("orc_gemm_nvf4 failed with code %d" % rc)
     return D, S
 
 

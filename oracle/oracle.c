@@ -322,6 +322,77 @@ int orc_gemm_mx_f8(int a_fmt, int b_fmt, int M, int N, int K, double alpha, cons
   return 0;
 }
 
+/*
+ * FP4 E2M1 (one sign bit, 2 exponent bits with bias 1, 1 mantissa bit; no infinities or
+ * NaN): exponent 0 is subnormal, m * 0.5; otherwise (1 + m / 2) * 2^(e - 1).  The values are
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives.  ("Tensor Core" chapter: Blackwell adds
+ * FP4, including block-scaled NVFP4 / MXFP4.)
+ */
+double orc_decode_e2m1(uint8_t c) {
+  const int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -v : v;
+}
+
+/* NVFP4 block scale UE4M3: the E4M3 bit layout without a sign (codes 0..126; 127 is NaN). */
+double orc_decode_ue4m3(uint8_t c) {
+  if (c >= 128) return NAN;
+  return orc_decode_e4m3(c);
+}
+
+/*
+ * NVFP4 GEMM: FP4 E2M1 elements packed two per byte (element k of a row in byte k / 2, the
+ * low nibble for even k), one UE4M3 scale per 16 consecutive K elements of a row of A and of
+ * a column of B:
+ *   D_ref[i][j] = alpha * sum_k (SA[i][k/16] * e2m1(A[i][k])) * (SB[j][k/16] * e2m1(Bt[j][k]))
+ *                 + beta * C[i][j]
+ * A is M x K with row pitch lda ELEMENTS (lda even); B is given transposed, Bt N x K (row j =
+ * column j of B) with pitch ldbt elements; SA M x ceil(K/16) (ld_sa), SB N x ceil(K/16)
+ * (ld_sb).  Scaled elements are exact in double; sums are plain double loops.
+ */
+int orc_gemm_nvf4(int M, int N, int K, double alpha, const uint8_t* A, int64_t lda, const uint8_t* SA,
+                  int64_t ld_sa, const uint8_t* Bt, int64_t ldbt, const uint8_t* SB, int64_t ld_sb, double beta,
+                  const float* C, int64_t ldc, const int32_t* rows, int nrows, double* D_ref, double* absab) {
+  if (M < 0 || N < 0 || K < 0 || nrows < 0 || (lda & 1) || (ldbt & 1)) return 1;
+  for (int r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= M) return 2;
+  if (beta != 0.0 && C == NULL) return 3;
+  double* Bs = (double*)malloc(sizeof(double) * ((size_t)K * (size_t)N + 1));  /* Bs[j][k] */
+  if (!Bs) return 4;
+  for (int64_t j = 0; j < N; ++j)
+    for (int64_t k = 0; k < K; ++k) {
+      const uint8_t byte = Bt[(j * ldbt + k) / 2];
+      const uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+      Bs[j * K + k] = orc_decode_ue4m3(SB[j * ld_sb + k / 16]) * orc_decode_e2m1(code);
+    }
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    const int64_t i = rows[r];
+    double* a = (double*)malloc(sizeof(double) * ((size_t)K + 1));
+    for (int64_t k = 0; k < K; ++k) {
+      const uint8_t byte = A[(i * lda + k) / 2];
+      const uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+      a[k] = orc_decode_ue4m3(SA[i * ld_sa + k / 16]) * orc_decode_e2m1(code);
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      double acc = 0.0, aab = 0.0;
+      const double* b = Bs + j * K;
+      for (int64_t k = 0; k < K; ++k) {
+        acc += a[k] * b[k];
+        aab += fabs(a[k]) * fabs(b[k]);
+      }
+      double d = alpha * acc;
+      if (beta != 0.0) d += beta * (double)C[i * ldc + j];
+      if (D_ref) D_ref[(int64_t)r * N + j] = d;
+      if (absab) absab[(int64_t)r * N + j] = aab;
+    }
+    free(a);
+  }
+  free(Bs);
+  return 0;
+}
+
 /* ------------------------------------------------------------------ W8A8 GEMV */
 
 /*

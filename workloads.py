@@ -240,3 +240,41 @@ def mx_quant(rows, cols, seed, block_axis, ld=None, fmt="e4m3", spread=4):
     if block_axis == 0:
         codes_s = np.ascontiguousarray(codes_s.T)
     return _pad(codes, ld, NAN_BITS["e4m3"], np.uint8), codes_s
+
+
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def nvf4_quant(rows, cols, seed, ld=None, spread=3):
+    """NVFP4 quantisation of seeded N(0, 1) draws along rows (K contiguous), each 16-element
+    block first multiplied by 2^u (u uniform in [-spread, spread]): the block's UE4M3 scale is
+    amax / 6 rounded to E4M3 (1 for an all-zero block; never below the smallest normal), each
+    element v / scale rounded to the nearest E2M1 magnitude (ties to the smaller one).
+
+    Returns (codes uint8 rows x ld/2 -- two per byte, element k in byte k / 2, low nibble for
+    even k -- and scale codes uint8 rows x ceil(cols / 16))."""
+    import torch
+    ld = cols if ld is None else ld
+    if ld % 2:
+        raise ValueError("FP4 pitch must be even")
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal(size=(rows, cols), dtype=np.float32).astype(np.float64)
+    nb = -(-cols // 16)
+    u = rng.integers(-spread, spread + 1, size=(rows, nb))
+    v = v * np.ldexp(1.0, u[:, np.arange(cols) // 16])
+    amax = np.zeros((rows, nb))
+    for b in range(nb):
+        amax[:, b] = np.max(np.abs(v[:, 16 * b:16 * b + 16]), axis=1) if cols else 0
+    target = np.where(amax > 0, np.maximum(amax / 6.0, 2.0 ** -6), 1.0).astype(np.float32)
+    sc = torch.from_numpy(target).to(torch.float8_e4m3fn)
+    scodes = sc.view(torch.uint8).numpy().copy()
+    svals = sc.to(torch.float64).numpy()
+    q = v / svals[:, np.arange(cols) // 16]
+    mag = np.abs(q)
+    vals = np.array(E2M1_VALUES)
+    best = np.argmin(np.abs(mag[..., None] - vals), axis=-1)  # nearest; ties to the smaller magnitude
+    codes = (best | (np.signbit(q).astype(np.int64) << 3)).astype(np.uint8)
+    full = np.zeros((rows, ld), dtype=np.uint8)
+    full[:, :cols] = codes
+    packed = (full[:, 0::2] | (full[:, 1::2] << 4)).astype(np.uint8)
+    return packed, scodes
