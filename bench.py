@@ -33,6 +33,7 @@ METRIC = "GEMM TFLOPS & % of GB300 dense tensor peak; W8A8 GEMV HBM GB/s & % of 
 HEADLINE = "bf16_gemm_4096"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor throughput (4.5 : 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0  # nominal dense FP4 : BF16 tensor throughput (13.5 : 2.25 PFLOP/s)
 L2_BYTES = 129 * 1000 * 1000
 HEADLINE_GROUPS = 5  # the headline is the median of this many groups of `steps` steps
 
@@ -52,6 +53,8 @@ def gemv_bytes(N, K):
 KERNEL_SOURCES = {
     "gemm_mx_kernel": ["linear_layer_gb300/csrc/gemm_mx.cu", "linear_layer_gb300/csrc/gemm_common.cuh",
                        "linear_layer_gb300/csrc/ptx.cuh"],
+    "gemm_mx2_kernel": ["linear_layer_gb300/csrc/gemm_mx.cu", "linear_layer_gb300/csrc/gemm_common.cuh",
+                        "linear_layer_gb300/csrc/ptx.cuh"],
     "gemm_tc2_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/gemm_common.cuh",
                         "linear_layer_gb300/csrc/ptx.cuh"],
     "gemm_tc_kernel": ["linear_layer_gb300/csrc/gemm_tc.cu", "linear_layer_gb300/csrc/gemm_common.cuh",
@@ -704,12 +707,67 @@ def bench_mx(args, dev, stream, peaks, peak_src):
             "ms_per_launch_min_max": [round(min(group_ms), 4), round(max(group_ms), 4)],
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
-                         "traffic": measured_traffic("mxf8_gemm_8192", "gemm_mx_kernel"),
-                         "kernel": "gemm_mx_kernel<0> (one CTA per 128 x 256 tile, hardware block scaling)",
+                         "traffic": measured_traffic("mxf8_gemm_8192", "gemm_mx2_kernel"),
+                         "kernel": "gemm_mx2_kernel<E4M3, MX> (CTA pairs per 256 x 256 tile, hardware block "
+                                   "scaling)",
                          "peak_source": "%s bf16_tflops x %g (nominal FP8:BF16)" % (peak_src, FP8_OVER_BF16),
                          "algorithmic_bytes_per_launch": M * K + K * N + M * KB + N * KB + M * N * 2},
             "timing": "median of 5 groups of %d back-to-back calls alternating 2 input sets "
                       "(A+B 128 MB each); each call rearranges the scale codes, then runs the GEMM" % steps,
+            "status": ll.status_string(st)}
+
+
+def bench_nvf4(args, dev, stream, peaks, peak_src):
+    """NVFP4 block-scaled GEMM 8192^3 (E2M1, UE4M3 scale per 16 K elements, BF16 out)."""
+    import torch
+
+    import linear_layer_gb300 as ll
+    import workloads as wl
+    cfg = wl.WORKLOADS["nvf4_gemm_8192"]
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    A, SA = wl.nvf4_quant(M, K, wl.SEED_A)
+    Bt, SB = wl.nvf4_quant(N, K, wl.SEED_B)
+    KB = SA.shape[1]
+    tA, tSA, tB, tSB = _up(A, dev), _up(SA, dev), _up(Bt, dev), _up(SB, dev)
+    # three input sets (A + Bt 64 MB each) and outputs (128 MB each): a set is read again
+    # only after two other calls have moved 384 MB, three times L2
+    sets = [(tA, tSA, tB, tSB, torch.empty((M, N), dtype=torch.bfloat16, device=dev))]
+    for _ in range(2):
+        sets.append((tA.clone(), tSA.clone(), tB.clone(), tSB.clone(),
+                     torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+    ws = torch.empty(ll.gemm_nvf4_workspace_size(M, N, K, K, K), dtype=torch.uint8, device=dev)
+
+    def call(i):
+        a, sa, b, sb, d = sets[i % 3]
+        ll.gemm_nvf4(M, N, K, 1.0, a, K, sa, KB, b, K, sb, KB, 0.0, None, N, d, N, ll.OUT_BF16, workspace=ws,
+                     stream=stream)
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize(dev)
+    steps = max(12, min(3 * (args.steps // 30), 120))
+    group_ms = []
+    for _ in range(5):  # median of 5 groups of back-to-back launches
+        total_ms, _ = time_events(call, steps, stream, per_call=False)
+        group_ms.append(total_ms / steps)
+    ms = statistics.median(group_ms)
+    st, _ = ll.get_device_status(stream)
+    flops = gemm_flops(M, N, K)
+    tflops = flops / (ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    return {"metric": "NVFP4 block-scaled GEMM TFLOPS", "value": round(tflops, 1), "unit": "TFLOPS",
+            "ms_per_launch": round(ms, 4),
+            "ms_per_launch_min_max": [round(min(group_ms), 4), round(max(group_ms), 4)],
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": round(peak, 1),
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "traffic": measured_traffic("nvf4_gemm_8192", "gemm_mx2_kernel"),
+                         "kernel": "gemm_mx2_kernel<E2M1, NVFP4> (CTA pairs per 256 x 256 tile, hardware "
+                                   "block scaling)",
+                         "peak_source": "%s bf16_tflops x %g (nominal FP4:BF16)" % (peak_src, FP4_OVER_BF16),
+                         "algorithmic_bytes_per_launch": M * K // 2 + N * K // 2 + M * KB + N * KB + M * N * 2},
+            "timing": "median of 5 groups of %d back-to-back calls rotating 3 input sets "
+                      "(A+Bt 64 MB each, D 128 MB each); each call rearranges the scale codes, then runs the "
+                      "GEMM" % steps,
             "status": ll.status_string(st)}
 
 
@@ -909,8 +967,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the GEMV / FP8 / ragged lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "mx", "ragged", "tokens", "w8a16",
-                                           "small"],
+    ap.add_argument("--workload", choices=["all", "gemv", "gemv_fused", "fp8", "mx", "nvf4", "ragged", "tokens",
+                                           "w8a16", "small"],
                     default="all",
                     help="all = the contract line; otherwise time one other kernel and print its object")
     args = ap.parse_args(argv)
@@ -929,7 +987,7 @@ def main(argv=None):
     stream = torch.cuda.Stream(device=dev)
 
     single = {"gemv": bench_gemv, "gemv_fused": bench_gemv_fused, "fp8": bench_fp8, "mx": bench_mx,
-              "ragged": bench_ragged, "tokens": bench_w8a8_tokens, "w8a16": bench_w8a16,
+              "nvf4": bench_nvf4, "ragged": bench_ragged, "tokens": bench_w8a8_tokens, "w8a16": bench_w8a16,
               "small": bench_small}.get(args.workload)
     if single is not None:
         res = single(args, dev, stream, peaks, peak_src)

@@ -235,6 +235,43 @@ ll_status ll_gemm_mxf8(int a_type, int b_type, int M, int N, int K, float alpha,
                        int64_t ld_sb, float beta, const float* C, int64_t ldc, void* D, int64_t ldd, int d_type,
                        void* workspace, size_t ws_bytes, ll_stream_t stream);
 
+/*
+ * NVFP4 block-scaled GEMM: FP4 E2M1 elements (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their
+ * negatives), every 16 consecutive K elements of a row of A, and of a column of B, sharing
+ * one UE4M3 scale (the E4M3 bit pattern with the sign bit clear):
+ *
+ *   D[i][j] = alpha * sum_k (ue4m3(scale_a[i][k/16]) e2m1(A[i][k]))
+ *                         * (ue4m3(scale_b[j][k/16]) e2m1(B[k][j]))  + beta * C[i][j]
+ *
+ * Defined by: "Tensor Core" chapter, the table of tensor-core formats per generation
+ * (Blackwell adds block-scaled 4-bit formats, NVFP4 among them).  The tensor cores apply
+ * the scales.
+ *
+ *   A      : M x K elements packed two per byte (element k of a row in byte k/2 of it, the
+ *            low nibble for even k); lda = row pitch in ELEMENTS, even, >= K
+ *   Bt     : B given transposed, N x K (row j holds column j of B), packed like A; ldbt =
+ *            row pitch in elements, even, >= K
+ *   K      : even (a row ends on a byte boundary); the last block may be shorter than 16
+ *   scale_a: M x ld_sa UE4M3 codes, ld_sa >= ceil(K/16), row i for row i of A
+ *   scale_b: N x ld_sb UE4M3 codes, ld_sb >= ceil(K/16), row j for column j of B
+ *            scale codes 0..126 (127 is NaN and codes >= 128 carry a sign: not supported)
+ *   C, D, stream: as for ll_gemm_f16.
+ *   workspace : required, sized by ll_gemm_nvf4_workspace_size: the scale codes are first
+ *            rearranged there (16 ceil(K/256) bytes for each of ceil(M/128) 128 rows and
+ *            ceil(N/256) 256 columns: 8 MiB at 8192^3), plus a 16-byte-pitch copy of A or
+ *            Bt when its byte pitch (lda/2, ldbt/2) is not a multiple of 16.
+ * Accumulation is FP32 over the whole K; alpha / beta and the output cast as ll_gemm_f16.
+ * Errors: LL_ERR_INVALID_ARG for odd K, lda or ldbt, pitches below K, scale pitches below
+ * ceil(K/16), overlapping output; others as ll_gemm_f16.
+ */
+/* Workspace bytes an ll_gemm_nvf4 call needs (assuming 16-byte-aligned A and Bt). */
+size_t ll_gemm_nvf4_workspace_size(int M, int N, int K, int64_t lda, int64_t ldbt);
+
+ll_status ll_gemm_nvf4(int M, int N, int K, float alpha, const uint8_t* A, int64_t lda, const uint8_t* scale_a,
+                       int64_t ld_sa, const uint8_t* Bt, int64_t ldbt, const uint8_t* scale_b, int64_t ld_sb,
+                       float beta, const float* C, int64_t ldc, void* D, int64_t ldd, int d_type, void* workspace,
+                       size_t ws_bytes, ll_stream_t stream);
+
 /* ------------------------------------------------------------------ W8A8 GEMV */
 
 /*
@@ -380,7 +417,8 @@ ll_status ll_linear_f16_w8a8_gemv(int N, int K, const void* x, int8_t* x_q, floa
  * Returns LL_OK, LL_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out since the
  * last call, or LL_ERR_CUDA if the synchronisation itself failed.
  * `detail` (host, may be NULL) receives the raw word: bits 0-7 the status code,
- * bits 8-15 the kernel role that gave up (1 producer, 2 MMA, 3 epilogue, 4 test wait).
+ * bits 8-15 the kernel role that gave up (1 producer, 2 MMA, 3 epilogue, 4 test wait,
+ * 5 block-scale staging).
  */
 ll_status ll_get_device_status(ll_stream_t stream, uint32_t* detail);
 

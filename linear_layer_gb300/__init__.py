@@ -14,6 +14,8 @@ gemm_fp8_blockscaled ll_gemm_fp8_blockscaled
 gemm_f8_blockscaled_mixed ll_gemm_f8_blockscaled_mixed
 gemm_mxf8            ll_gemm_mxf8
 gemm_mxf8_workspace_size ll_gemm_mxf8_workspace_size
+gemm_nvf4            ll_gemm_nvf4
+gemm_nvf4_workspace_size ll_gemm_nvf4_workspace_size
 linear_w8a8_gemv     ll_linear_w8a8_gemv
 linear_w8a8_gemv_ex  ll_linear_w8a8_gemv_ex
 linear_w8a8          ll_linear_w8a8
@@ -41,7 +43,7 @@ OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
 # every symbol the header declares
 EXPORTS = ["ll_gemm_workspace_size", "ll_gemm_f16", "ll_gemm_bf16", "ll_gemm_fp8_blockscaled",
            "ll_gemm_f16_noalloc", "ll_gemm_f8_blockscaled_mixed", "ll_gemm_mxf8",
-           "ll_gemm_mxf8_workspace_size",
+           "ll_gemm_mxf8_workspace_size", "ll_gemm_nvf4", "ll_gemm_nvf4_workspace_size",
            "ll_linear_w8a8_gemv", "ll_linear_w8a8_gemv_ex", "ll_linear_f16_w8a8_gemv",
            "ll_linear_w8a8", "ll_linear_w8a16",
            "ll_quantize_per_token_f16", "ll_get_device_status", "ll_set_wait_timeout_ns",
@@ -77,6 +79,10 @@ def _load():
     L.ll_gemm_mxf8_workspace_size.argtypes = [i32, i32, i32, i64, i64]
     L.ll_gemm_mxf8.restype = i32
     L.ll_gemm_mxf8.argtypes = [i32, i32] + L.ll_gemm_fp8_blockscaled.argtypes
+    L.ll_gemm_nvf4_workspace_size.restype = ctypes.c_size_t
+    L.ll_gemm_nvf4_workspace_size.argtypes = [i32, i32, i32, i64, i64]
+    L.ll_gemm_nvf4.restype = i32
+    L.ll_gemm_nvf4.argtypes = L.ll_gemm_fp8_blockscaled.argtypes
     L.ll_linear_w8a8_gemv.restype = i32
     L.ll_linear_w8a8_gemv.argtypes = [i32, i32, vp, vp, vp, i64, vp, vp, vp, vp]
     L.ll_linear_w8a8_gemv_ex.restype = i32
@@ -213,6 +219,20 @@ def gemm_mxf8(a_type, b_type, M, N, K, alpha, A, lda, scale_a, ld_sa, B, ldb, sc
     return _check(lib.ll_gemm_mxf8(a_type, b_type, M, N, K, alpha, _p(A), lda, _p(scale_a), ld_sa, _p(B), ldb,
                                    _p(scale_b), ld_sb, beta, _p(C), ldc, _p(D), ldd, d_type, w, wb,
                                    _stream(stream)), "ll_gemm_mxf8")
+
+
+def gemm_nvf4_workspace_size(M, N, K, lda, ldbt):
+    return lib.ll_gemm_nvf4_workspace_size(M, N, K, lda, ldbt)
+
+
+def gemm_nvf4(M, N, K, alpha, A, lda, scale_a, ld_sa, Bt, ldbt, scale_b, ld_sb, beta, C, ldc, D, ldd, d_type,
+              workspace=None, stream=None):
+    """NVFP4 GEMM: A (M x K) and Bt (N x K, B transposed) hold E2M1 codes two per byte,
+    pitches in elements; scale_a / scale_b hold UE4M3 codes, one per 16-wide K block."""
+    w, wb = _ws(workspace)
+    return _check(lib.ll_gemm_nvf4(M, N, K, alpha, _p(A), lda, _p(scale_a), ld_sa, _p(Bt), ldbt, _p(scale_b),
+                                   ld_sb, beta, _p(C), ldc, _p(D), ldd, d_type, w, wb, _stream(stream)),
+                  "ll_gemm_nvf4")
 
 
 def linear_w8a8_gemv(N, K, x, x_scale, W, ldw, w_scale, y, z_out=None, stream=None):

@@ -185,9 +185,12 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
     return LL_ERR_MISALIGNED;
   const bool f8 = (a.in_type == LL_IN_E4M3 || a.in_type == LL_IN_E5M2) && !a.mx;  // FP32 128-blocks
   const int64_t kb = (a.K + 127) / 128, nb = (a.N + 127) / 128;
-  const int64_t kb32 = (a.K + 31) / 32;  // MX: E8M0 blocks of 32 along K
+  const int64_t kb32 = a.nvf4 ? (a.K + 15) / 16 : (a.K + 31) / 32;  // scale codes per row (MX / NVFP4)
+  const int64_t kbytes = a.K / 2;                                     // NVFP4 row bytes
   if (a.K > 0) {
-    if (a.A == nullptr || a.B == nullptr || a.lda < a.K || a.ldb < a.N) return LL_ERR_INVALID_ARG;
+    if (a.A == nullptr || a.B == nullptr) return LL_ERR_INVALID_ARG;
+    if (a.nvf4 ? (a.K % 2 != 0 || a.lda < kbytes || a.ldb < kbytes) : (a.lda < a.K || a.ldb < a.N))
+      return LL_ERR_INVALID_ARG;
     if (f8 && (a.scale_a == nullptr || a.scale_b == nullptr || a.ld_sa < kb || a.ld_sb < nb))
       return LL_ERR_INVALID_ARG;
     if (a.mx && (a.mx_sa == nullptr || a.mx_sb == nullptr || a.ld_mx_sa < kb32 || a.ld_mx_sb < kb32))
@@ -210,6 +213,10 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
     ins[3] = Extent{a.K > 0 ? a.mx_sa : nullptr, a.M, kb32, a.ld_mx_sa};
     ins[4] = Extent{a.K > 0 ? a.mx_sb : nullptr, a.N, kb32, a.ld_mx_sb};
   }
+  if (a.nvf4) {  // A: M x K/2 bytes; B^T: N x K/2 bytes
+    ins[0] = Extent{a.K > 0 ? a.A : nullptr, a.M, kbytes, a.lda};
+    ins[1] = Extent{a.K > 0 ? a.B : nullptr, a.N, kbytes, a.ldb};
+  }
   if (outputs_overlap(&D, 1, ins, 5)) return LL_ERR_INVALID_ARG;
   if (a.K > 0 && ws != nullptr && ws_bytes > 0) {
     const RepackPlan plan = plan_repack(a);
@@ -228,13 +235,19 @@ ll::RepackPlan ll::plan_repack(const GemmArgs& a) {
   RepackPlan pl;
   pl.a = !pitch_ok(a.A, a.lda, es);
   pl.b = !pitch_ok(a.B, a.ldb, es);
-  pl.lda_p = round_up(a.K, 16 / es);
-  pl.ldb_p = round_up(a.N, 16 / es);
-  pl.a_bytes = pl.a ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.lda_p * es, 256)) : 0;
-  pl.b_bytes = pl.b ? static_cast<size_t>(static_cast<int64_t>(a.K) * pl.ldb_p * es) : 0;
+  if (a.nvf4) {  // byte rows: A M x K/2, B^T N x K/2
+    pl.lda_p = pl.ldb_p = round_up(a.K / 2, 16);
+    pl.a_bytes = pl.a ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.lda_p, 256)) : 0;
+    pl.b_bytes = pl.b ? static_cast<size_t>(static_cast<int64_t>(a.N) * pl.ldb_p) : 0;
+  } else {
+    pl.lda_p = round_up(a.K, 16 / es);
+    pl.ldb_p = round_up(a.N, 16 / es);
+    pl.a_bytes = pl.a ? static_cast<size_t>(round_up(static_cast<int64_t>(a.M) * pl.lda_p * es, 256)) : 0;
+    pl.b_bytes = pl.b ? static_cast<size_t>(static_cast<int64_t>(a.K) * pl.ldb_p * es) : 0;
+  }
   pl.mx = a.mx != 0;
   pl.xa_bytes = pl.xb_bytes = 0;
-  if (pl.mx) pl.xb_bytes = mx_scale_block_bytes(a.M, a.N, a.K, &pl.xa_bytes) - pl.xa_bytes;
+  if (pl.mx) pl.xb_bytes = mx_scale_block_bytes(a.M, a.N, a.K, a.nvf4 != 0, &pl.xa_bytes) - pl.xa_bytes;
   return pl;
 }
 
@@ -243,14 +256,16 @@ ll_status ll::launch_gemm_planned(GemmArgs a, const RepackPlan& plan, void* scra
   unsigned char* w = static_cast<unsigned char*>(scratch);
   // every byte the GEMM reads from the scratch is written here first (pad columns are
   // zeroed), so nothing an earlier call left there reaches this one
+  const int arow = a.nvf4 ? a.K / 2 : a.K;    // row widths: elements (bytes for NVFP4)
+  const int brows = a.nvf4 ? a.N : a.K, brow = a.nvf4 ? a.K / 2 : a.N;
   if (plan.a) {
-    const ll_status st = launch_repack(a.A, a.lda, w, plan.lda_p, a.M, a.K, es, ctx);
+    const ll_status st = launch_repack(a.A, a.lda, w, plan.lda_p, a.M, arow, es, ctx);
     if (st != LL_OK) return st;
     a.A = w;
     a.lda = plan.lda_p;
   }
   if (plan.b) {
-    const ll_status st = launch_repack(a.B, a.ldb, w + plan.a_bytes, plan.ldb_p, a.K, a.N, es, ctx);
+    const ll_status st = launch_repack(a.B, a.ldb, w + plan.a_bytes, plan.ldb_p, brows, brow, es, ctx);
     if (st != LL_OK) return st;
     a.B = w + plan.a_bytes;
     a.ldb = plan.ldb_p;
@@ -279,8 +294,8 @@ ll_status gemm_common(const ll::GemmArgs& a, void* workspace, size_t ws_bytes, l
   if (plan.a || plan.b || plan.mx) {
     const int es = in_esize(a.in_type);
     size_t need = 0;
-    if (plan.a) need += repack_bytes(a.M, a.K, es);
-    if (plan.b) need += repack_bytes(a.K, a.N, es);
+    if (plan.a) need += repack_bytes(a.M, a.nvf4 ? a.K / 2 : a.K, es);
+    if (plan.b) need += a.nvf4 ? repack_bytes(a.N, a.K / 2, es) : repack_bytes(a.K, a.N, es);
     if (plan.mx) need += plan.xa_bytes + plan.xb_bytes + 512;
     if (workspace == nullptr || ws_bytes < need) return LL_ERR_WORKSPACE;
     base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
@@ -330,7 +345,16 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
 
 size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  return ll_gemm_workspace_size(M, N, K, lda, ldb, LL_IN_E4M3) + ll::mx_scale_block_bytes(M, N, K, nullptr) + 512;
+  return ll_gemm_workspace_size(M, N, K, lda, ldb, LL_IN_E4M3) + ll::mx_scale_block_bytes(M, N, K, false, nullptr) +
+         512;
+}
+
+size_t ll_gemm_nvf4_workspace_size(int M, int N, int K, int64_t lda, int64_t ldbt) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  size_t need = ll::mx_scale_block_bytes(M, N, K, true, nullptr) + 512;
+  if ((lda / 2) % 16 != 0) need += repack_bytes(M, K / 2, 1);
+  if ((ldbt / 2) % 16 != 0) need += repack_bytes(N, K / 2, 1);
+  return need;
 }
 
 static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, const void* A,
@@ -358,6 +382,7 @@ static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, co
   a.scale_b = nullptr;
   a.ld_sb = 0;
   a.mx = 0;
+  a.nvf4 = 0;
   a.mx_sa = nullptr;
   a.ld_mx_sa = 0;
   a.mx_sb = nullptr;
@@ -424,6 +449,21 @@ ll_status ll_gemm_mxf8(int a_type, int b_type, int M, int N, int K, float alpha,
   ll::GemmArgs a = dense_args(a_type, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type);
   a.b_type = b_type;
   a.mx = 1;
+  a.mx_sa = scale_a;
+  a.ld_mx_sa = ld_sa;
+  a.mx_sb = scale_b;
+  a.ld_mx_sb = ld_sb;
+  return gemm_common(a, workspace, ws_bytes, stream);
+}
+
+ll_status ll_gemm_nvf4(int M, int N, int K, float alpha, const uint8_t* A, int64_t lda, const uint8_t* scale_a,
+                       int64_t ld_sa, const uint8_t* Bt, int64_t ldbt, const uint8_t* scale_b, int64_t ld_sb,
+                       float beta, const float* C, int64_t ldc, void* D, int64_t ldd, int d_type, void* workspace,
+                       size_t ws_bytes, ll_stream_t stream) {
+  if ((lda & 1) || (ldbt & 1)) return LL_ERR_INVALID_ARG;  // rows start on byte boundaries
+  ll::GemmArgs a = dense_args(LL_IN_E4M3, M, N, K, alpha, A, lda / 2, Bt, ldbt / 2, beta, C, ldc, D, ldd, d_type);
+  a.mx = 1;
+  a.nvf4 = 1;
   a.mx_sa = scale_a;
   a.ld_mx_sa = ld_sa;
   a.mx_sb = scale_b;

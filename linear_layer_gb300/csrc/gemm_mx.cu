@@ -40,21 +40,31 @@ namespace ll {
 
 namespace {
 
+// NV = false: MXFP8 (8-bit elements, B N-major as K x N, one E8M0 scale per 32 K elements:
+// one 4-byte scale word per row / column covers a 128-byte stage, its bytes picked by the
+// scale-factor IDs).  NV = true: NVFP4 (E2M1 elements two per byte, B given K-major as N x K,
+// one UE4M3 scale per 16 K elements: each K = 64 MMA reads a whole word, so a 128-byte stage
+// of 256 elements carries four words per row / column).
+template <bool NV>
 struct MxCfg {
   static constexpr int BM = 128, BN = 256;
-  static constexpr int BK = 128;                 // K elements (bytes) per stage
-  static constexpr int UMMA_K = 32, KSTEPS = 4;  // one E8M0 K block per MMA
+  static constexpr int BK = 128;                 // bytes of K per stage
+  static constexpr int BK_ELEMS = NV ? 256 : 128;
+  static constexpr int KSTEPS = 4;               // MMAs per stage (K = 64 FP4 or 32 FP8: 32 bytes)
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BOX_N = 128, B_BOXES = BN / B_BOX_N, B_BOX_BYTES = BK * 128;
+  static constexpr int B_BOX_N = NV ? BN : 128;  // B rows (NV: N rows of B^T) or columns per box
+  static constexpr int B_BOXES = BN / B_BOX_N;
+  static constexpr int B_BOX_BYTES = NV ? BN * 128 : BK * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BOXES * B_BOX_BYTES;  // 48 KB
-  static constexpr int SF_BLOCK = 512;                                 // 32 rows x 16 bytes
-  static constexpr int SF_STAGE_BYTES = 3 * SF_BLOCK;                  // A, B columns 0-127, 128-255
+  static constexpr int SETS = NV ? 4 : 1;                                // scale words per row and stage
+  static constexpr int SF_BLOCK = 512;                                   // 32 rows x 16 bytes
+  static constexpr int SF_STAGE_BYTES = 3 * SETS * SF_BLOCK;             // A's blocks, then B's
   static constexpr int STAGES = 4;
   static constexpr int EPI_WARP0 = 2, EPI_WARPS = 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SF_COL0 = BN, SF_COLS = 16;
+  static constexpr int SF_COL0 = BN, SF_COLS = 12 * SETS;  // A: 4 per set, B: 8 per set
   static constexpr int NBARS = 2 * STAGES + 3;  // full, empty, tfull, tempty, drain
   static constexpr int SMEM = STAGES * (STAGE_BYTES + SF_STAGE_BYTES) + NBARS * 8 + 16 + 1024;
   static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
@@ -71,20 +81,46 @@ __host__ __device__ constexpr uint32_t make_idesc_mx(uint32_t fmts, int n, int m
 
 __host__ __device__ constexpr uint32_t sf_ids(uint32_t kk) { return (kk << 4) | (kk << 29); }
 
+// kind::mxf4nvf4 (NVFP4): A / B format E2M1 (1), both K-major, N >> 3, scale type UE4M3
+// (bit 23 = 0), M >> 4; scale-factor IDs 0 (each K = 64 MMA reads all four bytes of a word).
+__host__ __device__ constexpr uint32_t make_idesc_nv(int n, int m) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+template <bool NV>
+__host__ __device__ constexpr uint32_t mx_idesc(uint32_t fmts, int n, int m) {
+  return NV ? make_idesc_nv(n, m) : make_idesc_mx(fmts, n, m);
+}
+
+// MMA kk of a stage: its instruction descriptor and the TMEM columns (from the stage's base)
+// of its A and B scale words
+template <bool NV>
+__device__ __forceinline__ uint32_t mma_idesc(uint32_t base, int kk) {
+  return NV ? base : base | sf_ids(kk);
+}
+template <bool NV, int SETS>
+__device__ __forceinline__ uint32_t sfa_col(int kk) { return NV ? 4 * kk : 0; }
+template <bool NV, int SETS>
+__device__ __forceinline__ uint32_t sfb_col(int kk) { return 4 * SETS + (NV ? 8 * kk : 0); }
+
+// 4-code scale words per row of the rearranged scale blocks: one per 128-K stage (MX), four
+// per 256-element stage (NVFP4; whole stages, the words past K holding neutral codes)
+__host__ __device__ constexpr int mx_words(int K, bool nv) { return nv ? 4 * ((K + 255) / 256) : (K + 127) / 128; }
+
 // ------------------------------------------------------------------ scale blocks
 //
 // Block (blk, kb) of a code matrix (rows of K-block-contiguous codes, `ld` bytes apart)
 // holds rows 128 blk .. 128 blk + 127 and K blocks 4 kb .. 4 kb + 3: 512 bytes, 16-byte row r
 // holding at byte 4j + b the code of row 128 blk + 32j + r for K block 4 kb + b.  Codes of
-// rows past `rows` or K blocks past `nkb` are written as 127 (2^0; their operand elements
-// are zero).  Blocks are stored in the order the kernels fetch them:
+// rows past `rows` or K blocks past `nkb` are written as `neutral` (a finite scale: their
+// operand elements are zero).  Blocks are stored in the order the kernels fetch them:
 //   A (cols256 = 0): block (blk, kb) at ((blk * KB) + kb) * 512
 //   B (cols256 = 1): block (blk, kb) at (((blk / 2) * KB + kb) * 2 + blk % 2) * 512
 // so that the two blocks of a 256-column tile's stage are adjacent.  One CTA of 128
 // threads per (blk, four stages): each thread loads one row's 16 codes, the block is
 // transposed through shared memory, and each warp writes one 512-byte block.
 __global__ void __launch_bounds__(128) mx_scale_tile_kernel(const uint8_t* __restrict__ src, int64_t ld, int rows,
-                                                            int nkb, int KB, int cols256,
+                                                            int nkb, int KB, int cols256, uint32_t neutral,
                                                             uint8_t* __restrict__ dst) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ __align__(16) uint8_t sm[128 * 16];
@@ -92,7 +128,8 @@ __global__ void __launch_bounds__(128) mx_scale_tile_kernel(const uint8_t* __res
   const int blk = blockIdx.x, g = blockIdx.y;  // g: four stages, 16 K blocks
   const int row = blk * 128 + t;
   const int k0 = 16 * g;
-  uint4 v = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const uint32_t n4 = neutral * 0x01010101u;
+  uint4 v = make_uint4(n4, n4, n4, n4);
   if (row < rows) {
     const uint8_t* q = src + static_cast<int64_t>(row) * ld + k0;
     if (k0 + 16 <= nkb && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
@@ -105,7 +142,7 @@ __global__ void __launch_bounds__(128) mx_scale_tile_kernel(const uint8_t* __res
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const int k = k0 + 4 * i + b;
-          x |= (k < nkb ? static_cast<uint32_t>(__ldg(q + 4 * i + b)) : 0x7Fu) << (8 * b);
+          x |= (k < nkb ? static_cast<uint32_t>(__ldg(q + 4 * i + b)) : neutral) << (8 * b);
         }
         w[i] = x;
       }
@@ -127,14 +164,14 @@ __global__ void __launch_bounds__(128) mx_scale_tile_kernel(const uint8_t* __res
 
 // ------------------------------------------------------------------ one-CTA kernel
 
-template <uint32_t AB_FMT>
-__global__ void __launch_bounds__(MxCfg::THREADS, 1)
+template <uint32_t AB_FMT, bool NV>
+__global__ void __launch_bounds__(MxCfg<NV>::THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmXA, const __grid_constant__ CUtensorMap tmXB,
                    const GemmParams p) {
-  using Cfg = MxCfg;
+  using Cfg = MxCfg<NV>;
   constexpr int S = Cfg::STAGES;
-  constexpr uint32_t IDESC = make_idesc_mx(AB_FMT, Cfg::BN, Cfg::BM);
+  constexpr uint32_t IDESC = mx_idesc<NV>(AB_FMT, Cfg::BN, Cfg::BM);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -177,7 +214,8 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
   const int num_m = (p.M + Cfg::BM - 1) / Cfg::BM;
   const int num_n = (p.N + Cfg::BN - 1) / Cfg::BN;
   const int num_tiles = num_m * num_n;
-  const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;  // stages per tile
+  const int KB = (p.K + Cfg::BK_ELEMS - 1) / Cfg::BK_ELEMS;  // stages per tile
+  const int KBw = mx_words(p.K, NV);                            // scale words per row
 
   // programmatic dependent launch: L2 prefetch of the first ring of operand tiles, then
   // the wait for the previous kernel of the stream (scale blocks, C and D come after it)
@@ -187,7 +225,10 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     const int pre = KB < S ? KB : S;
     for (int kb = 0; kb < pre; ++kb) {
       tma_prefetch_l2(&tmA, kb * Cfg::BK, mb * Cfg::BM);
-      for (int j = 0; j < Cfg::B_BOXES; ++j) tma_prefetch_l2(&tmB, nb * Cfg::BN + j * Cfg::B_BOX_N, kb * Cfg::BK);
+      if (NV)
+        tma_prefetch_l2(&tmB, kb * Cfg::BK, nb * Cfg::BN);
+      else
+        for (int j = 0; j < Cfg::B_BOXES; ++j) tma_prefetch_l2(&tmB, nb * Cfg::BN + j * Cfg::B_BOX_N, kb * Cfg::BK);
     }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -215,12 +256,17 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           uint8_t* sf = sf_base + s * Cfg::SF_STAGE_BYTES;
           mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES + Cfg::SF_STAGE_BYTES);
           tma_load_2d(smem_addr(a_s), &tmA, full_bar(s), kb * Cfg::BK, mb * Cfg::BM);
+          if (NV) {  // B^T: 256 rows x 128 bytes, K-major
+            tma_load_2d(smem_addr(b_s), &tmB, full_bar(s), kb * Cfg::BK, nb * Cfg::BN);
+          } else {
 #pragma unroll
-          for (int j = 0; j < Cfg::B_BOXES; ++j)
-            tma_load_2d(smem_addr(b_s + j * Cfg::B_BOX_BYTES), &tmB, full_bar(s), nb * Cfg::BN + j * Cfg::B_BOX_N,
-                        kb * Cfg::BK);
-          tma_load_2d(smem_addr(sf), &tmXA, full_bar(s), 0, (mb * KB + kb) * 32);
-          tma_load_2d(smem_addr(sf + Cfg::SF_BLOCK), &tmXB, full_bar(s), 0, (nb * KB + kb) * 64);
+            for (int j = 0; j < Cfg::B_BOXES; ++j)
+              tma_load_2d(smem_addr(b_s + j * Cfg::B_BOX_BYTES), &tmB, full_bar(s), nb * Cfg::BN + j * Cfg::B_BOX_N,
+                          kb * Cfg::BK);
+          }
+          tma_load_2d(smem_addr(sf), &tmXA, full_bar(s), 0, (mb * KBw + Cfg::SETS * kb) * 2);
+          tma_load_2d(smem_addr(sf + Cfg::SETS * Cfg::SF_BLOCK), &tmXB, full_bar(s), 0,
+                      (nb * KBw + Cfg::SETS * kb) * 4);
           ++it;
         }
       }
@@ -246,16 +292,23 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
           tc_fence_after();
           const uint32_t sf_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_COLS;
           const uint32_t sf_s = smem_addr(sf_base + s * Cfg::SF_STAGE_BYTES);
-          tmem_cp_32x128b_x4(sf_t, smem_desc_plain16(sf_s));
-          tmem_cp_32x128b_x4(sf_t + 4, smem_desc_plain16(sf_s + Cfg::SF_BLOCK));
-          tmem_cp_32x128b_x4(sf_t + 8, smem_desc_plain16(sf_s + 2 * Cfg::SF_BLOCK));
+#pragma unroll
+          for (int j = 0; j < 3 * Cfg::SETS; ++j)  // A's blocks, then B's (two per set)
+            tmem_cp_32x128b_x4(sf_t + 4 * j, smem_desc_plain16(sf_s + j * Cfg::SF_BLOCK));
           const uint32_t a_base = smem_addr(smem + s * Cfg::STAGE_BYTES);
           const uint32_t b_base = a_base + Cfg::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BOX_BYTES, 1024);
-            mma_mxf8(tmem_base, adesc, bdesc, IDESC | sf_ids(kk), sf_t, sf_t + 4, (kb > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bdesc = NV ? smem_desc_sw128(b_base + kk * 32, 16, 1024)
+                                      : smem_desc_sw128(b_base + kk * 32 * 128, Cfg::B_BOX_BYTES, 1024);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            if (NV)
+              mma_nvf4(tmem_base, adesc, bdesc, IDESC, sf_t + sfa_col<NV, Cfg::SETS>(kk),
+                       sf_t + sfb_col<NV, Cfg::SETS>(kk), acc);
+            else
+              mma_mxf8(tmem_base, adesc, bdesc, mma_idesc<NV>(IDESC, kk), sf_t + sfa_col<NV, Cfg::SETS>(kk),
+                       sf_t + sfb_col<NV, Cfg::SETS>(kk), acc);
           }
           mma_commit(empty_bar(s));  // the stage (operands and scale blocks) may be refilled
           ++it;
@@ -316,45 +369,71 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
 // of its B (one 128-byte-swizzled box per stage), and the even CTA's MMA thread issues
 // tcgen05.mma.cta_group::2 (M = 256).  Per SM that halves the B bytes TMA writes into
 // shared memory and the tensor cores read back (the one-CTA tile moves 96 KB through
-// shared memory per 128-K stage, which bounds it).  Each CTA's TMEM must hold the scales of
-// its own 128 rows of A and of all 256 columns of B (in the one-CTA layout), so each CTA's
-// producer fetches exactly those blocks into its own shared memory, completing on the even
-// CTA's stage barrier with the operands, and one tcgen05.cp.cta_group::2 from the even CTA
-// copies both CTAs' blocks into their own TMEM.
-//   full[s]   (even CTA)  count 1: the even CTA's producer arms it with both CTAs' bytes
+// shared memory per 128-K stage, which bounds it).
+//
+// Scales.  Each CTA's TMEM must hold the scales of its own 128 rows of A and of all 256
+// columns of B.  Copying them with tcgen05.cp (as the one-CTA kernel does) puts three
+// copies per stage for MX, twelve for NVFP4, into the tensor pipe in front of the MMAs,
+// which measured as the larger part of the NVFP4 kernel's time.  Here four scale warps per
+// CTA, one per TMEM lane quarter, write the same TMEM contents with tcgen05.st instead:
+// warp q reads row `lane` of each of the stage's scale blocks (fetched by TMA into its own
+// CTA's shared memory) and stores it into lane 32 q + lane, so that every lane quarter
+// holds what the replicating copy would have put there:
+//   SFA: block kk (4 words: rows lane, 32 + lane, 64 + lane, 96 + lane) at column SFA + 4 kk,
+//   SFB: block (kk, h) (columns 128 h + 32 j + lane, j < 4) at column SFB + 8 kk + 4 h.
+// (The scale-factor TMEM addresses given to the MMA stay multiples of 4 columns, as the
+// copy layout has them.)  Each warp then arrives on the even CTA's sf_ready[s] (8 arrivals:
+// 4 warps x 2 CTAs).  The odd CTA's arrivals are relaxed: tcgen05.wait::st has completed the
+// warp's TMEM writes before it, so the arrival publishes no outstanding memory writes (a
+// release arrival at cluster scope waits on the whole memory system and measured 2x slower
+// overall); tcgen05.fence::before_thread_sync orders the writes before it, and the MMA
+// thread's acquire wait and tcgen05.fence::after_thread_sync order its MMAs after.
+//
+// Warps: 0 producer, 1 TMEM allocator and (even CTA) MMA issuer, 2-3 idle, 4-7 scale
+// warps, 8-15 epilogue.  setmaxnreg gives the epilogue warpgroups 192 registers a thread
+// and the others 48 / 72, within the 512 x 128 the block is launched with.
+//   full[s]     (even CTA) count 1: the even producer arms it with both CTAs' operand bytes
+//   sf_full[s]  (each CTA) count 1: its own producer arms it with its scale-block bytes
+//   sf_ready[s] (even CTA) count 8: the scale warps of both CTAs
 //   empty[s], tfull       (each CTA) count 1: the MMA commits, multicast to both CTAs
 //   tempty    (even CTA)  one relaxed arrival per epilogue warp of each CTA (16)
+template <bool NV>
 struct Mx2Cfg {
   static constexpr int BM = 128;                 // rows per CTA (the pair tile has 256)
   static constexpr int BN = 256;                 // columns of the pair tile
-  static constexpr int BK = 128;
-  static constexpr int UMMA_K = 32, KSTEPS = 4;
+  static constexpr int BK = 128;                 // bytes of K per stage
+  static constexpr int BK_ELEMS = NV ? 256 : 128;
+  static constexpr int KSTEPS = 4;
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_HALF = BN / 2;          // columns of B in each CTA
-  static constexpr int B_BYTES = BK * 128;       // one 128-column box
+  static constexpr int B_HALF = BN / 2;          // columns of B (NV: rows of B^T) in each CTA
+  static constexpr int B_BYTES = 128 * 128;      // one box: 128 K x 128 columns, or 128 rows x 128 K bytes
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+  static constexpr int SETS = NV ? 4 : 1;
   static constexpr int SF_BLOCK = 512;
-  static constexpr int SF_STAGE_BYTES = 3 * SF_BLOCK;
-  static constexpr int STAGES = 6;
-  static constexpr int EPI_WARP0 = 2, EPI_WARPS = 8;
-  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-  static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+  static constexpr int SF_STAGE_BYTES = 3 * SETS * SF_BLOCK;
+  static constexpr int STAGES = NV ? 5 : 6;
+  static constexpr int SF_WARP0 = 4, EPI_WARP0 = 8, EPI_WARPS = 8;
+  static constexpr int THREADS = 512;
+  static constexpr int LAUNCH_REGS = 65536 / THREADS;  // 128
+  static constexpr int REGS_CTRL = 48, REGS_SF = 72, REGS_EPI = 192;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int SF_COL0 = BN, SF_COLS = 16;
-  static constexpr int NBARS = 2 * STAGES + 3;
+  static constexpr int SFA_COLS = 4 * SETS;
+  static constexpr int SF_COL0 = BN, SF_COLS = SFA_COLS + 8 * SETS;
+  static constexpr int NBARS = 4 * STAGES + 3;   // full, empty, sf_full, sf_ready, tfull, tempty, drain
   static constexpr int SMEM = STAGES * (STAGE_BYTES + SF_STAGE_BYTES) + NBARS * 8 + 16 + 1024;
   static_assert(SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(128 * REGS_CTRL + 128 * REGS_SF + 256 * REGS_EPI <= THREADS * LAUNCH_REGS, "register split");
 };
 
-template <uint32_t AB_FMT>
-__global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
+template <uint32_t AB_FMT, bool NV>
+__global__ void __launch_bounds__(Mx2Cfg<NV>::THREADS, 1)
     gemm_mx2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmXA, const __grid_constant__ CUtensorMap tmXB,
                     const GemmParams p) {
-  using Cfg = Mx2Cfg;
+  using Cfg = Mx2Cfg<NV>;
   constexpr int S = Cfg::STAGES;
-  constexpr uint32_t IDESC = make_idesc_mx(AB_FMT, Cfg::BN, 2 * Cfg::BM);
+  constexpr uint32_t IDESC = mx_idesc<NV>(AB_FMT, Cfg::BN, 2 * Cfg::BM);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -373,14 +452,18 @@ __global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
   const int num_pairs = gridDim.x >> 1;
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + S + s); };
-  const uint32_t tfull_bar = smem_addr(bars + 2 * S);
-  const uint32_t tempty_bar = smem_addr(bars + 2 * S + 1);
-  const uint32_t drain_bar = smem_addr(bars + 2 * S + 2);
+  auto sf_full_bar = [&](int s) { return smem_addr(bars + 2 * S + s); };
+  auto sf_ready_bar = [&](int s) { return smem_addr(bars + 3 * S + s); };
+  const uint32_t tfull_bar = smem_addr(bars + 4 * S);
+  const uint32_t tempty_bar = smem_addr(bars + 4 * S + 1);
+  const uint32_t drain_bar = smem_addr(bars + 4 * S + 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sf_full_bar(s), 1);
+      mbar_init(sf_ready_bar(s), 8);
     }
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, 2 * Cfg::EPI_WARPS);
@@ -401,7 +484,8 @@ __global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
   const int num_m2 = (p.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM);
   const int num_n = (p.N + Cfg::BN - 1) / Cfg::BN;
   const int num_tiles = num_m2 * num_n;
-  const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;
+  const int KB = (p.K + Cfg::BK_ELEMS - 1) / Cfg::BK_ELEMS;
+  const int KBw = mx_words(p.K, NV);  // scale words per row
 
   if (warp == 0 && lane == 0 && pair < num_tiles) {
     int mb, nb;
@@ -409,11 +493,23 @@ __global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
     const int pre = KB < S ? KB : S;
     for (int kb = 0; kb < pre; ++kb) {
       tma_prefetch_l2(&tmA, kb * Cfg::BK, mb * 2 * Cfg::BM + Cfg::BM * rank_i);
-      tma_prefetch_l2(&tmB, nb * Cfg::BN + Cfg::B_HALF * rank_i, kb * Cfg::BK);
+      if (NV)
+        tma_prefetch_l2(&tmB, kb * Cfg::BK, nb * Cfg::BN + Cfg::B_HALF * rank_i);
+      else
+        tma_prefetch_l2(&tmB, nb * Cfg::BN + Cfg::B_HALF * rank_i, kb * Cfg::BK);
     }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  if (warp < Cfg::SF_WARP0) {
+    regs_dec<Cfg::REGS_CTRL>();  // warpgroup 0: producer, MMA issuer, two idle warps
+  } else if (warp < Cfg::EPI_WARP0) {
+    regs_dec<Cfg::REGS_SF>();
+  } else {
+    regs_inc<Cfg::REGS_EPI>();
+  }
+
+  if (warp < Cfg::SF_WARP0) {
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (each CTA)
     if (lane == 0) {
@@ -436,22 +532,30 @@ __global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
           const uint32_t cfull = mapa_cluster(full_bar(s), 0);
           uint8_t* a_s = smem + s * Cfg::STAGE_BYTES;
           uint8_t* sf = sf_base + s * Cfg::SF_STAGE_BYTES;
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * (Cfg::STAGE_BYTES + Cfg::SF_STAGE_BYTES));
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::STAGE_BYTES);
+          mbar_arrive_expect_tx(sf_full_bar(s), Cfg::SF_STAGE_BYTES);
           tma_load_2d_pair(smem_addr(a_s), &tmA, cfull, kb * Cfg::BK, ablk * Cfg::BM);
-          tma_load_2d_pair(smem_addr(a_s + Cfg::A_BYTES), &tmB, cfull, nb * Cfg::BN + Cfg::B_HALF * rank_i,
-                           kb * Cfg::BK);
-          tma_load_2d_pair(smem_addr(sf), &tmXA, cfull, 0, (ablk * KB + kb) * 32);
-          tma_load_2d_pair(smem_addr(sf + Cfg::SF_BLOCK), &tmXB, cfull, 0, (nb * KB + kb) * 64);
+          if (NV)  // this CTA's 128 rows of B^T (K-major)
+            tma_load_2d_pair(smem_addr(a_s + Cfg::A_BYTES), &tmB, cfull, kb * Cfg::BK,
+                             nb * Cfg::BN + Cfg::B_HALF * rank_i);
+          else
+            tma_load_2d_pair(smem_addr(a_s + Cfg::A_BYTES), &tmB, cfull, nb * Cfg::BN + Cfg::B_HALF * rank_i,
+                             kb * Cfg::BK);
+          tma_load_2d(smem_addr(sf), &tmXA, sf_full_bar(s), 0, (ablk * KBw + Cfg::SETS * kb) * 2);
+          tma_load_2d(smem_addr(sf + Cfg::SETS * Cfg::SF_BLOCK), &tmXB, sf_full_bar(s), 0,
+                      (nb * KBw + Cfg::SETS * kb) * 4);
           ++it;
         }
       }
-      if (!ok && rank == 0) {  // the even CTA's full barriers see both CTAs' copies
-        for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0u); j < it; ++j)
-          wait_drain(full_bar(j % S), (j / S) & 1u, p.timeout_ns);
+      if (!ok) {  // copies still in flight: the even CTA's full barriers see both CTAs' operands
+        for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0u); j < it; ++j) {
+          if (rank == 0) wait_drain(full_bar(j % S), (j / S) & 1u, p.timeout_ns);
+          wait_drain(sf_full_bar(j % S), (j / S) & 1u, p.timeout_ns);
+        }
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- scale copies + MMA (even CTA)
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
       uint32_t it = 0, tiles = 0;
       bool ok = true;
@@ -460,24 +564,25 @@ __global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
           const int s = it % S;
-          if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
+          if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma) ||
+              !wait_bounded_cluster(sf_ready_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sf_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_COLS;
-          const uint32_t sf_s = smem_addr(sf_base + s * Cfg::SF_STAGE_BYTES);
-          tmem_cp_32x128b_x4_pair(sf_t, smem_desc_plain16(sf_s));
-          tmem_cp_32x128b_x4_pair(sf_t + 4, smem_desc_plain16(sf_s + Cfg::SF_BLOCK));
-          tmem_cp_32x128b_x4_pair(sf_t + 8, smem_desc_plain16(sf_s + 2 * Cfg::SF_BLOCK));
           const uint32_t a_base = smem_addr(smem + s * Cfg::STAGE_BYTES);
           const uint32_t b_base = a_base + Cfg::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BYTES, 1024);
-            mma_mxf8_pair(tmem_base, adesc, bdesc, IDESC | sf_ids(kk), sf_t, sf_t + 4,
-                          (kb > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bdesc = NV ? smem_desc_sw128(b_base + kk * 32, 16, 1024)
+                                      : smem_desc_sw128(b_base + kk * 32 * 128, Cfg::B_BYTES, 1024);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            if (NV)
+              mma_nvf4_pair(tmem_base, adesc, bdesc, IDESC, sf_t + 4 * kk, sf_t + Cfg::SFA_COLS + 8 * kk, acc);
+            else
+              mma_mxf8_pair(tmem_base, adesc, bdesc, mma_idesc<NV>(IDESC, kk), sf_t, sf_t + Cfg::SFA_COLS, acc);
           }
           mma_commit_pair_mc(empty_bar(s), 0x3);
           ++it;
@@ -488,6 +593,55 @@ __global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
       }
       mma_commit_pair(drain_bar);
       wait_drain(drain_bar, 0u, p.timeout_ns);
+    }
+  }
+  } else if (warp < Cfg::EPI_WARP0) {
+    // ---------------------------------------------------------------- scale warps (each CTA)
+    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t ready0 = rank == 0 ? 0u : mapa_cluster(sf_ready_bar(0), 0);
+    uint32_t it = 0;
+    for (int u = pair; u < num_tiles; u += num_pairs) {
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = it % S;
+        bool w = wait_bounded(sf_full_bar(s), (it / S) & 1u, wctx, kRoleScales);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sf = sf_base + s * Cfg::SF_STAGE_BYTES;
+        const uint32_t col = tmem_base + lane_base + Cfg::SF_COL0 + s * Cfg::SF_COLS;
+        // row `lane` of A's blocks (one per MMA set), then of B's (two per set)
+        uint32_t a[4 * Cfg::SETS], b[8 * Cfg::SETS];
+#pragma unroll
+        for (int g = 0; g < 3 * Cfg::SETS; ++g) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sf + g * Cfg::SF_BLOCK + lane * 16);
+          uint32_t* d = g < Cfg::SETS ? a + 4 * g : b + 4 * (g - Cfg::SETS);
+          d[0] = v.x;
+          d[1] = v.y;
+          d[2] = v.z;
+          d[3] = v.w;
+        }
+        if constexpr (NV) {
+          tmem_st_x16(col, a);
+          tmem_st_x32(col + Cfg::SFA_COLS, b);
+        } else {
+          tmem_st_x4(col, a);
+          tmem_st_x8(col + Cfg::SFA_COLS, b);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(sf_ready_bar(s));
+          else
+            mbar_arrive_cluster_relaxed(ready0 + 8u * static_cast<uint32_t>(s));
+        }
+        ++it;
+      }
+      if (!ok) break;
     }
   } else {
     // ---------------------------------------------------------------- epilogue (each CTA)
@@ -534,31 +688,37 @@ __global__ void __launch_bounds__(Mx2Cfg::THREADS, 1)
 
 // ------------------------------------------------------------------ host side
 
-// Tensor maps of the operands and of the two scale-block arrays (16-byte rows).
-template <class Cfg>
-bool mx_maps(const GemmArgs& a, int a_box_rows, int b_box_cols, CUtensorMap* tmA, CUtensorMap* tmB,
-             CUtensorMap* tmXA, CUtensorMap* tmXB) {
-  const int64_t KB = (a.K + 127) / 128;
-  const int64_t xa_rows = ((a.M + 127) / 128) * KB * 32;
-  const int64_t xb_rows = ((a.N + 255) / 256) * KB * 64;
-  return make_tensor_map_2d(tmA, a.A, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.M, a.K, a.lda, Cfg::BK, a_box_rows) &&
-         make_tensor_map_2d(tmB, a.B, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.K, a.N, a.ldb, b_box_cols, Cfg::BK) &&
-         make_tensor_map_2d(tmXA, a.mx_sat, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xa_rows, 16, 16, 16, 32,
-                            CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         make_tensor_map_2d(tmXB, a.mx_sbt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xb_rows, 16, 16, 16, 64,
-                            CU_TENSOR_MAP_SWIZZLE_NONE);
+// Tensor maps of the operands and of the two scale-block arrays (16-byte rows).  MX: A M x K
+// bytes, B K x N (N-major boxes of 128 columns).  NVFP4: A M x K/2 bytes, B given as B^T,
+// N x K/2 bytes (K-major boxes of b_rows rows); pitches in bytes.
+template <bool NV>
+bool mx_maps(const GemmArgs& a, int b_box, CUtensorMap* tmA, CUtensorMap* tmB, CUtensorMap* tmXA,
+             CUtensorMap* tmXB) {
+  const int64_t kbytes = NV ? a.K / 2 : a.K;
+  const int64_t KBw = mx_words(a.K, NV);
+  const int sets = NV ? 4 : 1;
+  // the blocks of a stage are contiguous: fetched as rows of 256 bytes (2 per 128-row block
+  // of A, 4 per 256-column block of B), which keeps the number of TMA rows per stage small
+  const int64_t xa_rows = ((a.M + 127) / 128) * KBw * 2;
+  const int64_t xb_rows = ((a.N + 255) / 256) * KBw * 4;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const bool b_ok = NV ? make_tensor_map_2d(tmB, a.B, u8, 1, a.N, kbytes, a.ldb, 128, b_box)
+                       : make_tensor_map_2d(tmB, a.B, u8, 1, a.K, a.N, a.ldb, b_box, 128);
+  return b_ok && make_tensor_map_2d(tmA, a.A, u8, 1, a.M, kbytes, a.lda, 128, 128) &&
+         make_tensor_map_2d(tmXA, a.mx_sat, u8, 1, xa_rows, 256, 256, 256, 2 * sets, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         make_tensor_map_2d(tmXB, a.mx_sbt, u8, 1, xb_rows, 256, 256, 256, 4 * sets, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <uint32_t F>
+template <uint32_t F, bool NV>
 ll_status run_mx(const GemmArgs& a, const LaunchCtx& ctx) {
-  using Cfg = MxCfg;
-  auto kern = gemm_mx_kernel<F>;
+  using Cfg = MxCfg<NV>;
+  auto kern = gemm_mx_kernel<F, NV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess) {
     cudaGetLastError();
     return LL_ERR_CUDA;
   }
   CUtensorMap tmA, tmB, tmXA, tmXB;
-  if (!mx_maps<Cfg>(a, Cfg::BM, Cfg::B_BOX_N, &tmA, &tmB, &tmXA, &tmXB)) return LL_ERR_CUDA;
+  if (!mx_maps<NV>(a, Cfg::B_BOX_N, &tmA, &tmB, &tmXA, &tmXB)) return LL_ERR_CUDA;
   const GemmParams p = make_gemm_params(a, ctx);
   const int num_tiles = ((a.M + Cfg::BM - 1) / Cfg::BM) * ((a.N + Cfg::BN - 1) / Cfg::BN);
   cudaLaunchConfig_t cfg = {};
@@ -578,16 +738,29 @@ ll_status run_mx(const GemmArgs& a, const LaunchCtx& ctx) {
   return LL_OK;
 }
 
-template <uint32_t F>
+template <uint32_t F, bool NV>
 ll_status run_mx2(const GemmArgs& a, const LaunchCtx& ctx) {
-  using Cfg = Mx2Cfg;
-  auto kern = gemm_mx2_kernel<F>;
+  using Cfg = Mx2Cfg<NV>;
+  auto kern = gemm_mx2_kernel<F, NV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess) {
     cudaGetLastError();
     return LL_ERR_CUDA;
   }
+  // the kernel's setmaxnreg split needs the block launched with LAUNCH_REGS registers a
+  // thread (an increase beyond what the block holds would never be granted)
+  static int launch_regs = 0;
+  if (launch_regs == 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
+      cudaGetLastError();
+      return LL_ERR_CUDA;
+    }
+    launch_regs = fa.numRegs;
+  }
+  if (launch_regs * Cfg::THREADS < 128 * Cfg::REGS_CTRL + 128 * Cfg::REGS_SF + 256 * Cfg::REGS_EPI)
+    return LL_ERR_UNSUPPORTED;
   CUtensorMap tmA, tmB, tmXA, tmXB;
-  if (!mx_maps<Cfg>(a, Cfg::BM, Cfg::B_HALF, &tmA, &tmB, &tmXA, &tmXB)) return LL_ERR_CUDA;
+  if (!mx_maps<NV>(a, Cfg::B_HALF, &tmA, &tmB, &tmXA, &tmXB)) return LL_ERR_CUDA;
   const GemmParams p = make_gemm_params(a, ctx);
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(Cfg::THREADS);
@@ -603,19 +776,20 @@ ll_status run_mx2(const GemmArgs& a, const LaunchCtx& ctx) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   // co-resident CTA pairs (one CTA per SM): the persistent grid
-  static int max_pairs[64] = {};
+  static int max_pairs[2][64] = {};
   if (ctx.device < 0 || ctx.device >= 64) return LL_ERR_NO_DEVICE;
-  if (max_pairs[ctx.device] == 0) {
+  int& mp = max_pairs[NV ? 1 : 0][ctx.device];
+  if (mp == 0) {
     cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = ctx.num_sms / 2;
     }
-    max_pairs[ctx.device] = n;
+    mp = n;
   }
   const int tiles = ((a.M + 2 * Cfg::BM - 1) / (2 * Cfg::BM)) * ((a.N + Cfg::BN - 1) / Cfg::BN);
-  cfg.gridDim = dim3(2 * (tiles < max_pairs[ctx.device] ? tiles : max_pairs[ctx.device]));
+  cfg.gridDim = dim3(2 * (tiles < mp ? tiles : mp));
   if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmXA, tmXB, p) != cudaSuccess) {
     cudaGetLastError();
     return LL_ERR_CUDA;
@@ -625,41 +799,46 @@ ll_status run_mx2(const GemmArgs& a, const LaunchCtx& ctx) {
 
 }  // namespace
 
-size_t mx_scale_block_bytes(int M, int N, int K, size_t* a_bytes) {
-  const size_t KB = static_cast<size_t>((K + 127) / 128);
-  const size_t xa = static_cast<size_t>((M + 127) / 128) * KB * 512;
-  const size_t xb = static_cast<size_t>((N + 255) / 256) * KB * 1024;
+size_t mx_scale_block_bytes(int M, int N, int K, bool nv, size_t* a_bytes) {
+  const size_t KBw = static_cast<size_t>(mx_words(K, nv));
+  const size_t xa = static_cast<size_t>((M + 127) / 128) * KBw * 512;
+  const size_t xb = static_cast<size_t>((N + 255) / 256) * KBw * 1024;
   if (a_bytes) *a_bytes = xa;
   return xa + xb;
 }
 
 ll_status launch_mx_scale_tiles(const GemmArgs& a, uint8_t* xa, uint8_t* xb, const LaunchCtx& ctx) {
-  const int KB = (a.K + 127) / 128;
-  const int nkb = (a.K + 31) / 32;
-  const int G = (KB + 3) / 4;
-  mx_scale_tile_kernel<<<dim3((a.M + 127) / 128, G), 128, 0, ctx.stream>>>(a.mx_sa, a.ld_mx_sa, a.M, nkb, KB, 0, xa);
+  const bool nv = a.nvf4 != 0;
+  const int KBw = mx_words(a.K, nv);                         // 4-code words per row
+  const int nkb = nv ? (a.K + 15) / 16 : (a.K + 31) / 32;    // codes per row
+  const uint32_t neutral = nv ? 0x38u : 0x7Fu;               // 1.0 as UE4M3 / E8M0
+  const int G = (KBw + 3) / 4;
+  mx_scale_tile_kernel<<<dim3((a.M + 127) / 128, G), 128, 0, ctx.stream>>>(a.mx_sa, a.ld_mx_sa, a.M, nkb, KBw, 0,
+                                                                          neutral, xa);
   if (cudaGetLastError() != cudaSuccess) return LL_ERR_CUDA;
   // B: every 128-column block of each 256-column tile (a block past N gets neutral codes)
-  mx_scale_tile_kernel<<<dim3(2 * ((a.N + 255) / 256), G), 128, 0, ctx.stream>>>(a.mx_sb, a.ld_mx_sb, a.N, nkb, KB, 1,
-                                                                                 xb);
+  mx_scale_tile_kernel<<<dim3(2 * ((a.N + 255) / 256), G), 128, 0, ctx.stream>>>(a.mx_sb, a.ld_mx_sb, a.N, nkb, KBw,
+                                                                                 1, neutral, xb);
   return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
 ll_status launch_gemm_mx(const GemmArgs& a, const LaunchCtx& ctx) {
-  const bool a5 = a.in_type == LL_IN_E5M2, b5 = a.b_type == LL_IN_E5M2;
   // CTA pairs once there are enough 256 x 256 tiles to occupy a quarter of the SM pairs;
   // the one-CTA kernel below that
   const int pair_tiles = ((a.M + 255) / 256) * ((a.N + 255) / 256);
-  if (pair_tiles >= ctx.num_sms / 4) {
-    if (!a5 && !b5) return run_mx2<fmt_pair(0, 0)>(a, ctx);
-    if (a5 && b5) return run_mx2<fmt_pair(1, 1)>(a, ctx);
-    if (!a5) return run_mx2<fmt_pair(0, 1)>(a, ctx);
-    return run_mx2<fmt_pair(1, 0)>(a, ctx);
+  const bool pair = pair_tiles >= ctx.num_sms / 4;
+  if (a.nvf4) return pair ? run_mx2<fmt_pair(1, 1), true>(a, ctx) : run_mx<fmt_pair(1, 1), true>(a, ctx);
+  const bool a5 = a.in_type == LL_IN_E5M2, b5 = a.b_type == LL_IN_E5M2;
+  if (pair) {
+    if (!a5 && !b5) return run_mx2<fmt_pair(0, 0), false>(a, ctx);
+    if (a5 && b5) return run_mx2<fmt_pair(1, 1), false>(a, ctx);
+    if (!a5) return run_mx2<fmt_pair(0, 1), false>(a, ctx);
+    return run_mx2<fmt_pair(1, 0), false>(a, ctx);
   }
-  if (!a5 && !b5) return run_mx<fmt_pair(0, 0)>(a, ctx);
-  if (a5 && b5) return run_mx<fmt_pair(1, 1)>(a, ctx);
-  if (!a5) return run_mx<fmt_pair(0, 1)>(a, ctx);
-  return run_mx<fmt_pair(1, 0)>(a, ctx);
+  if (!a5 && !b5) return run_mx<fmt_pair(0, 0), false>(a, ctx);
+  if (a5 && b5) return run_mx<fmt_pair(1, 1), false>(a, ctx);
+  if (!a5) return run_mx<fmt_pair(0, 1), false>(a, ctx);
+  return run_mx<fmt_pair(1, 0), false>(a, ctx);
 }
 
 }  // namespace ll

@@ -36,7 +36,9 @@ struct GemmArgs {
   int64_t ld_sa;
   const float* scale_b;
   int64_t ld_sb;
-  int mx;                 // MX block scaling (E8M0 per 32 K elements) instead of FP32 128-blocks
+  int mx;                 // hardware block scaling (MX or NVFP4) instead of FP32 128-blocks
+  int nvf4;               // NVFP4: A is M x K/2 bytes and B holds B^T, N x K/2 bytes (pitches
+                          // lda / ldb in bytes), scales UE4M3 per 16 K elements
   const uint8_t* mx_sa;   // MX: M x ld_mx_sa scale codes of A, one per row and 32-wide K block
   int64_t ld_mx_sa;
   const uint8_t* mx_sb;   // MX: N x ld_mx_sb scale codes of B, one per column and K block
@@ -100,7 +102,7 @@ ll_status launch_gemm_mx(const GemmArgs& a, const LaunchCtx& ctx);
 
 // Bytes of the MX scale blocks of an M x N x K problem (A's in *a_bytes when not NULL), and
 // the kernel that writes them from a.mx_sa / a.mx_sb into xa / xb (gemm_mx.cu).
-size_t mx_scale_block_bytes(int M, int N, int K, size_t* a_bytes);
+size_t mx_scale_block_bytes(int M, int N, int K, bool nv, size_t* a_bytes);
 ll_status launch_mx_scale_tiles(const GemmArgs& a, uint8_t* xa, uint8_t* xb, const LaunchCtx& ctx);
 
 // D = beta * C (or 0) for K == 0 (aux.cu).

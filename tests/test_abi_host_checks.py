@@ -270,6 +270,36 @@ def check_mx_gemm(ll):
     assert _no_device(ll, call(K=0, ws=None, wsb=0))  # K == 0: D = beta * C, no workspace
 
 
+@check
+def check_nvf4_gemm(ll):
+    """ll_gemm_nvf4: even K and pitches (rows start on bytes), pitches in elements, scale
+    pitches of ceil(K/16), and the workspace for the rearranged scale codes."""
+    E = ll.LL_ERR_INVALID_ARG
+    f = ll.lib.ll_gemm_nvf4
+    Q, SA, SB, WS = P + 0x100000, P + 0x200000, P + 0x300000, P + 0x400000
+    need = ll.lib.ll_gemm_nvf4_workspace_size(64, 64, 96, 96, 96)
+    # pitch 48 bytes: no repack; scale blocks of one 128-row block of A (16 codes per row)
+    # and one 256-column block of B
+    assert need == 128 * 16 + 256 * 16 + 512
+    assert ll.lib.ll_gemm_nvf4_workspace_size(64, 64, 96, 100, 96) > need  # 50-byte rows of A
+
+    def call(K=96, lda=96, ldbt=96, ld_sa=6, ld_sb=6, sa=SA, ws=WS, wsb=None, D=Q):
+        return f(64, 64, K, 1.0, P, lda, sa, ld_sa, P + 0x80000, ldbt, SB, ld_sb, 0.0, None, 64, D, 64,
+                 ll.OUT_F32, ws, need if wsb is None else wsb, None)
+    assert call(K=95) == E                  # odd K: a row would end inside a byte
+    assert call(lda=97) == E                # odd pitch
+    assert call(ldbt=95) == E
+    assert call(lda=94) == E                # pitch below K
+    assert call(ld_sa=5) == E               # ceil(96 / 16) = 6 scale codes per row
+    assert call(ld_sb=5) == E
+    assert call(sa=None) == E
+    assert call(D=SB + 4) == E              # D over scale_b
+    assert call(ws=P + 0x10) == E           # workspace over A (64 rows x 48 bytes)
+    assert _no_device(ll, call(ws=None, wsb=0))
+    assert _no_device(ll, call())
+    assert _no_device(ll, call(ws=P + 64 * 48))  # just past A
+
+
 @pytest.mark.parametrize("name", CHECKS)
 def test_host_check_in_device_less_child(child_results, name):
     line = child_results.get(name)

@@ -44,6 +44,8 @@ WORKLOADS = {
                            out="bf16"),
     "mxf8_gemm_8192": dict(op="gemm_mx", kind="e4m3", M=8192, N=8192, K=8192, alpha=1.0, beta=0.0,
                            out="bf16"),
+    "nvf4_gemm_8192": dict(op="gemm_nvf4", kind="e2m1", M=8192, N=8192, K=8192, alpha=1.0, beta=0.0,
+                           out="bf16"),
 }
 
 
