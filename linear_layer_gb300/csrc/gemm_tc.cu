@@ -190,6 +190,44 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, float* st, int 
   __syncwarp();
 }
 
+// Row-contiguous variants for rows of C or D that need not start on 16-byte boundaries
+// (the CTA-pair kernel's transposing epilogue): lane l handles column n0 + l of each of
+// the chunk's 32 rows, so that every warp-wide access is 32 consecutive elements of one
+// row (one contiguous 128-byte or 64-byte span whatever the row's alignment).  C goes to
+// a 32 x 32 FP32 buffer in shared memory (row r at r * 32) by cp.async, each lane copying
+// the elements it later reads itself.
+__device__ __forceinline__ void issue_c_rows(const GemmParams& p, uint32_t cbuf, int m_base, int n0, int lane) {
+  const int n = n0 + lane;
+  if (p.beta == 0.0f || n >= p.N) return;
+  const float* cp = p.C + static_cast<int64_t>(m_base) * p.ldc + n;
+#pragma unroll 8
+  for (int r = 0; r < 32; ++r)
+    if (m_base + r < p.M) cp_async_4(cbuf + (r * 32 + lane) * 4, cp + static_cast<int64_t>(r) * p.ldc);
+}
+
+// st: the chunk's accumulator, row r (TMEM lane) holding its 32 columns as 8 float4 slots,
+// slot j at position j ^ (r & 7).
+__device__ __forceinline__ void store_rows(const GemmParams& p, const float* st, int m_base, int n0,
+                                           const float* cbuf, int lane) {
+  const int n = n0 + lane;
+  if (n >= p.N) return;
+  const bool use_c = p.beta != 0.0f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const int m = m_base + r;
+    if (m >= p.M) break;
+    float o = p.alpha * st[(r * 8 + ((lane >> 2) ^ (r & 7))) * 4 + (lane & 3)];
+    if (use_c) o = fmaf(p.beta, cbuf[r * 32 + lane], o);
+    const int64_t off = static_cast<int64_t>(m) * p.ldd + n;
+    if (p.d_type == LL_OUT_F32)
+      static_cast<float*>(p.D)[off] = o;
+    else if (p.d_type == LL_OUT_BF16)
+      static_cast<__nv_bfloat16*>(p.D)[off] = __float2bfloat16_rn(o);
+    else
+      static_cast<__half*>(p.D)[off] = __float2half_rn(o);
+  }
+}
+
 template <class Cfg, uint32_t AB_FMT>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -820,18 +858,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       __syncwarp();
     } else {
-      // unaligned rows of C or D: each chunk is transposed through shared memory into
-      // coalesced row segments.  C is loaded into registers one chunk ahead: chunk c + 1
-      // while chunk c is stored, and the first chunk of a unit before its accumulator is
-      // ready.  Units have 8 or 4 chunks, so chunks go in (even, odd) pairs.
+      // unaligned rows of C or D: each chunk is transposed through shared memory, and
+      // every warp-wide load of C and store of D covers 32 consecutive elements of one
+      // row.  C arrives by cp.async two chunks ahead, across unit boundaries, in a ring of
+      // three 4 KB buffers (this warp's epilogue buffers 1-3; buffer 0 holds the
+      // transposed accumulator), so that several chunks' loads are in flight while one is
+      // stored.
       float* st = reinterpret_cast<float*>(ebuf);
-      float c_even[32], c_odd[32];
-      uint32_t acc_it = 0;
-      if (pair < sc.num_units) {
-        int m0, n0, ncols;
-        unit(pair, m0, n0, ncols);
-        load_c_chunk(p, m0 + row_off, n0, lane, c_even);
-      }
+      float4* st4 = reinterpret_cast<float4*>(ebuf);
+      const uint32_t cring = smem_addr(ebuf + Cfg::EPI_BUF_BYTES);
+      int lu = pair, lc = 0;  // the chunk whose C is requested next
+      uint32_t k_req = 0;     // chunks requested (one cp.async group each)
+      auto request_next = [&]() {
+        if (lu < sc.num_units) {
+          int m1, n1, nc1;
+          unit(lu, m1, n1, nc1);
+          issue_c_rows(p, cring + (k_req % 3) * Cfg::EPI_BUF_BYTES, m1 + row_off, n1 + 32 * lc, lane);
+          if (++lc == nc1 / 32) {
+            lc = 0;
+            lu += num_pairs;
+          }
+        }
+        cp_async_commit();
+        ++k_req;
+      };
+      request_next();
+      request_next();
+      uint32_t acc_it = 0, k = 0;
       for (int u = pair; u < sc.num_units; u += num_pairs) {
         int m0, n0, ncols;
         unit(u, m0, n0, ncols);
@@ -843,35 +896,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int m_base = m0 + row_off;
         const int chunks = ncols / 32;
 #pragma unroll 1
-        for (int c = 0; c < chunks; c += 2) {
+        for (int c = 0; c < chunks; ++c, ++k) {
+          request_next();       // chunk k + 2
+          cp_async_wait<2>();   // chunk k's C has landed (this lane's elements)
           uint32_t r[32];
-          float v[32];
-          load_c_chunk(p, m_base, n0 + (c + 1) * 32, lane, c_odd);
           tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
           tmem_ld_wait(r);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_chunk(p, st, m_base, n0 + c * 32, v, c_even, lane);
-          if (c + 2 < chunks) {
-            load_c_chunk(p, m_base, n0 + (c + 2) * 32, lane, c_even);
-          } else if (u + num_pairs < sc.num_units) {  // the next unit's first chunk
-            int m1, n1, nc1;
-            unit(u + num_pairs, m1, n1, nc1);
-            load_c_chunk(p, m1 + row_off, n1, lane, c_even);
-          }
-          tmem_ld_x32(tmem_base + lane_base + ab * BN + (c + 1) * 32, r);
-          tmem_ld_wait(r);
-          if (c + 2 == chunks) {  // accumulator in registers: release it to the MMA
+          if (c == chunks - 1) {  // accumulator in registers: release it to the MMA
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_chunk(p, st, m_base, n0 + (c + 1) * 32, v, c_odd, lane);
+          for (int j = 0; j < 8; ++j)
+            st4[lane * 8 + (j ^ (lane & 7))] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          __syncwarp();
+          store_rows(p, st, m_base, n0 + c * 32, st + (1 + k % 3) * (Cfg::EPI_BUF_BYTES / 4), lane);
+          __syncwarp();
         }
         ++acc_it;
       }
+      cp_async_wait<0>();  // no copy into shared memory outlives the loop
     }
   }
 
