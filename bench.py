@@ -5,8 +5,10 @@ beta = 1 (FP32 C), BF16 output, FP32 accumulation -- TFLOPS and its fraction of
 the measured dense BF16 tensor peak.  A "step" is one call of the GEMM over one
 batch of synthetic inputs already resident in HBM.  The same line carries the
 other kernels of the path ("extra"): the batch-1 W8A8 GEMV 1 x 4096 . 4096 x 11008
-(GB/s of HBM), the FP8 E4M3 block-scaled GEMM 8192^3 and the ragged FP16 GEMM
-4093 x 5003 x 2056.
+(GB/s of HBM) and its fused FP16-activation form, the W8A8 and weight-only layers for a
+few tokens, the FP8 E4M3 block-scaled GEMM 8192^3, the MXFP8 and NVFP4 GEMMs 8192^3
+(hardware block scaling), the ragged FP16 GEMM 4093 x 5003 x 2056 and the launch-bound
+FP16 256^3.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -1005,6 +1007,7 @@ def main(argv=None):
         extra["w8a16_linear_tokens_4096x11008"] = bench_w8a16(args, dev, stream, peaks, peak_src)
         extra["e4m3_gemm_8192"] = bench_fp8(args, dev, stream, peaks, peak_src)
         extra["mxf8_gemm_8192"] = bench_mx(args, dev, stream, peaks, peak_src)
+        extra["nvf4_gemm_8192"] = bench_nvf4(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_4093x5003x2056"] = bench_ragged(args, dev, stream, peaks, peak_src)
         extra["f16_gemm_256"] = bench_small(args, dev, stream, peaks, peak_src)
     barrier(dev)
