@@ -21,6 +21,7 @@ struct GemmParams {
   int c_vec, d_vec;  // rows of C / D may be accessed with 4-element vectors
   int d_row16;       // rows of D start on 16-byte boundaries
   int epi_tma;       // CTA-pair 16-bit epilogue through TMA (C and D rows 16-byte aligned)
+  int epi_res;       // CTA-pair epilogue through TMA by row classes (FP32 D rows not 16-byte aligned)
   const float* sA;
   int64_t ld_sa;
   const float* sB;
@@ -163,6 +164,7 @@ inline GemmParams make_gemm_params(const GemmArgs& a, const LaunchCtx& ctx) {
   p.d_vec = (reinterpret_cast<uintptr_t>(a.D) % (4 * dsize) == 0) && ((a.ldd * dsize) % (4 * dsize) == 0);
   p.d_row16 = (reinterpret_cast<uintptr_t>(a.D) % 16 == 0) && ((a.ldd * dsize) % 16 == 0);
   p.epi_tma = 0;
+  p.epi_res = 0;
   p.sA = a.scale_a;
   p.ld_sa = a.ld_sa;
   p.sB = a.scale_b;

@@ -556,11 +556,23 @@ struct PairSched {
   int num_units;      // full_units + 2 * split tiles
 };
 
+// FP32 C and D whose rows do not start on 16-byte boundaries, as four row classes: class k
+// holds rows k, k + 4, k + 8, ..., 16 * ld bytes apart (a pitch a tensor map can describe),
+// its map starting at the first 16-byte boundary of row k, off_k = 0..3 elements in; all rows
+// of a class then have the same offset.  Column c of a row of class k is element c - off_k of
+// that map's row.  Boxes: C 36 x 8 (loaded from x = n - 4, which covers columns n .. n + 31
+// whatever off_k is), D 32 x 8 when off_k = 0 and 28 x 8 otherwise (stored at x = n: columns
+// n + off_k .. n + off_k + 27, the other 4 columns of the chunk by the lanes).
+struct EpiResMaps {
+  CUtensorMap c[4];
+  CUtensorMap d[4];
+};
+
 template <class Cfg, uint32_t AB_FMT>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
-                    const GemmParams p, const PairSched sc) {
+                    const GemmParams p, const PairSched sc, const __grid_constant__ EpiResMaps rm) {
   constexpr int S = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
   extern __shared__ uint8_t smem_raw[];
@@ -857,6 +869,166 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         bulk_wait_all();
       }
       __syncwarp();
+    } else if (p.epi_res) {
+      // FP32 D rows (and C rows) that do not start on 16-byte boundaries, through TMA by
+      // row classes (EpiResMaps).  Each lane keeps its own accumulator row (no transpose):
+      // lane l is row m_w + l, of class l & 3, row l >> 2 of that class's 8-row box.  C
+      // arrives two chunks ahead in a ring of two slots of four 36 x 8 boxes; the lane reads
+      // its row's 32 values at box column 4 - off + t (columns left of the map's first
+      // element, only in the chunk at column 0, are read by the lane itself).  D goes to
+      // four staging boxes (the lane's values shifted by its class's offset) and out with
+      // four TMA stores; the at most 4 columns of the chunk outside its class's box are
+      // stored by the lane.  Every value is fma(beta, C, alpha * acc) in FP32, as on the
+      // other paths.
+      constexpr int CBOX = 8 * 36 * 4;
+      constexpr int CSLOT = 4 * CBOX;
+      uint8_t* dstage = ebuf + 2 * CSLOT;  // four D boxes of up to 8 x 32 FP32, 1 KB apart
+      const bool use_c = p.beta != 0.0f;
+      const uint64_t pol_once = l2_evict_first_policy();  // C read once, D written once
+      const int rc = lane & 3, jr = lane >> 2;
+      int pu = pair, pc = 0, pchunks = 0, pm = 0, pn = 0;
+      auto cursor_unit = [&](int u) {
+        pu = u;
+        pc = 0;
+        if (u < sc.num_units) {
+          int m1, n1, nc1;
+          unit(u, m1, n1, nc1);
+          pm = m1 + row_off;
+          pn = n1;
+          pchunks = nc1 / 32;
+        }
+      };
+      uint32_t issued = 0;
+      auto issue_c = [&]() {  // lane 0; the ring slot is free
+        if (pu >= sc.num_units) return;
+        const int b = static_cast<int>(issued & 1u);
+        const int n = pn + 32 * pc;
+        if (n < p.N && pm < p.M) {
+          mbar_arrive_expect_tx(cfull_bar(ew, b), CSLOT);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tma_load_2d_hint(smem_addr(ebuf + b * CSLOT + k * CBOX), &rm.c[k], cfull_bar(ew, b), n - 4, pm / 4,
+                             pol_once);
+        } else {
+          mbar_arrive(cfull_bar(ew, b));
+        }
+        ++issued;
+        if (++pc == pchunks) cursor_unit(pu + num_pairs);
+      };
+      if (use_c) {
+        cursor_unit(pair);
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tma_prefetch_desc(&rm.c[k]);
+          issue_c();
+          issue_c();
+        }
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tma_prefetch_desc(&rm.d[k]);
+      }
+      uint32_t acc_it = 0, g = 0;
+      bool ok = true;
+      for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
+        int m0, n0, ncols;
+        unit(u, m0, n0, ncols);
+        const uint32_t ab = acc_it & 1u;
+        ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int m_w = m0 + row_off;
+        const int m = m_w + lane;
+        // this lane's row: its class's offset to the first 16-byte boundary (the address is
+        // only formed, never read, for rows past M)
+        const float* crow = p.C + static_cast<int64_t>(m) * p.ldc;
+        float* drow = static_cast<float*>(p.D) + static_cast<int64_t>(m) * p.ldd;
+        const int off_c = use_c ? static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(crow) >> 2) & 3u)) & 3u) : 0;
+        const int off_d = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(drow) >> 2) & 3u)) & 3u);
+        const int wd = off_d ? 28 : 32;
+        const int chunks = ncols / 32;
+#pragma unroll 1
+        for (int c = 0; c < chunks; ++c, ++g) {
+          const int b = static_cast<int>(g & 1u);
+          const int n = n0 + 32 * c;
+          uint32_t r[32];
+          tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
+          tmem_ld_wait(r);
+          if (c == chunks - 1) {  // accumulator in registers: release it to the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
+          }
+          float o[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = p.alpha * __uint_as_float(r[j]);
+          if (use_c) {
+            bool w = wait_bounded(cfull_bar(ew, b), (g >> 1) & 1u, wctx, kRoleEpilogue);
+            w = __all_sync(0xffffffffu, w);
+            if (!w) {
+              ok = false;
+              break;
+            }
+            const float* cb = reinterpret_cast<const float*>(ebuf + b * CSLOT + rc * CBOX) + jr * 36 + 4 - off_c;
+            const bool lead = n == 0 && m < p.M;  // columns left of the class map's first element
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const float cv = (t < 3 && lead && t < off_c) ? crow[t] : cb[t];
+              o[t] = fmaf(p.beta, cv, o[t]);
+            }
+            fence_proxy_async_smem();  // this lane's reads of the slot, before the TMA refills it
+            __syncwarp();
+            if (lane == 0 && static_cast<int>(issued - g) < 3) issue_c();  // chunk g + 2 into this slot
+          }
+          if (n < p.N && n + 32 > p.N) {
+            // the chunk that crosses column N: a TMA store writes the whole 16-byte unit that
+            // holds column N - 1, which with tight rows reaches into the next row, so each
+            // lane stores its row's valid columns itself
+            if (m < p.M) {
+#pragma unroll
+              for (int t = 0; t < 32; ++t)
+                if (n + t < p.N) drow[n + t] = o[t];
+            }
+          } else if (n < p.N) {
+            // s[k] = o[k + off_d] through two fixed-index selections
+            float s1[32], s2[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) s1[k] = (off_d & 1) ? (k + 1 < 32 ? o[k + 1] : 0.0f) : o[k];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) s2[k] = (off_d & 2) ? (k + 2 < 32 ? s1[k + 2] : 0.0f) : s1[k];
+            if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the staging
+            __syncwarp();
+            float4* ds = reinterpret_cast<float4*>(dstage + rc * 1024 + jr * wd * 4);
+#pragma unroll
+            for (int i = 0; i < 7; ++i) ds[i] = make_float4(s2[4 * i], s2[4 * i + 1], s2[4 * i + 2], s2[4 * i + 3]);
+            if (wd == 32) ds[7] = make_float4(s2[28], s2[29], s2[30], s2[31]);
+            if (m < p.M) {  // the chunk's columns outside this class's box
+#pragma unroll
+              for (int t = 0; t < 3; ++t)
+                if (t < off_d && n + t < p.N) drow[n + t] = o[t];
+#pragma unroll
+              for (int t = 29; t < 32; ++t)
+                if (off_d > 0 && t >= off_d + 28 && n + t < p.N) drow[n + t] = o[t];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && m_w < p.M) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) tma_store_2d_hint(&rm.d[k], smem_addr(dstage + k * 1024), n, m_w / 4, pol_once);
+              bulk_commit_group();
+            }
+          }
+        }
+        ++acc_it;
+      }
+      if (lane == 0) {
+        if (!ok && use_c) {  // C loads still in flight land before the CTA may exit
+          for (uint32_t j = g; j < issued; ++j) wait_drain(cfull_bar(ew, static_cast<int>(j & 1u)), (j >> 1) & 1u, p.timeout_ns);
+        }
+        bulk_wait_all();
+      }
+      __syncwarp();
     } else {
       // unaligned rows of C or D: each chunk is transposed through shared memory, and
       // every warp-wide load of C and store of D covers 32 consecutive elements of one
@@ -1024,6 +1196,26 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   memset(&tmD, 0, sizeof(tmD));
   const bool o32 = a.d_type == LL_OUT_F32;
   p.epi_tma = p.d_row16 && (a.beta == 0.0f || p.c_vec);
+  // FP32 D rows not on 16-byte boundaries: TMA by row classes (EpiResMaps)
+  EpiResMaps rm;
+  memset(&rm, 0, sizeof(rm));
+  p.epi_res = !p.epi_tma && o32 && a.M >= 4 && a.N >= 4;
+  if (p.epi_res) {
+    for (int k = 0; k < 4; ++k) {
+      const float* drow = static_cast<const float*>(a.D) + static_cast<int64_t>(k) * a.ldd;
+      const int off_d = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(drow) >> 2) & 3u)) & 3u);
+      if (!make_tensor_map_2d(&rm.d[k], drow + off_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (a.M - k + 3) / 4,
+                              a.N - off_d, 4 * a.ldd, off_d ? 28 : 32, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return LL_ERR_CUDA;
+      if (a.beta != 0.0f) {
+        const float* crow = a.C + static_cast<int64_t>(k) * a.ldc;
+        const int off_c = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(crow) >> 2) & 3u)) & 3u);
+        if (!make_tensor_map_2d(&rm.c[k], crow + off_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (a.M - k + 3) / 4,
+                                a.N - off_c, 4 * a.ldc, 36, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+          return LL_ERR_CUDA;
+      }
+    }
+  }
   if (p.epi_tma) {
     if (!make_tensor_map_2d(&tmD, a.D, o32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
                             o32 ? 4 : 2, a.M, a.N, a.ldd, 32, 32,
@@ -1081,7 +1273,7 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
     sc.num_units = T;
   }
   cfg.gridDim = dim3(2 * P);
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p, sc) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p, sc, rm) != cudaSuccess) {
     cudaGetLastError();
     return LL_ERR_CUDA;
   }
