@@ -861,7 +861,8 @@ def bench_ragged(args, dev, stream, peaks, peak_src):
             "ms_per_call_min_max": [round(min(group_ms), 4), round(max(group_ms), 4)],
             "timing": "median of 5 groups of %d back-to-back calls" % steps,
             "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                         "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                         "traffic": measured_traffic("f16_gemm_4093x5003x2056", "gemm_tc2_kernel"),
                          "peak_source": peak_src + " bf16_tflops (FP16 = BF16 rate)"},
             "status": ll.status_string(st)}
 
