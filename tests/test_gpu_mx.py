@@ -124,3 +124,17 @@ def test_mx_8192_full_size(orc):
     """The MX FP8 workload at full size (8192^3, E4M3, BF16 out), every element."""
     cfg = wl.WORKLOADS["mxf8_gemm_8192"]
     run_mx(orc, cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"], cfg["out"])
+
+
+def test_mx_k_zero_is_beta_c():
+    """K = 0: an empty contraction, D = beta * C exactly (no scale codes or workspace read)."""
+    import linear_layer_gb300 as ll
+    M, N = 300, 260
+    C = wl.f32_normal(M, N, 78)
+    tD = out_tensor(M, N, "f32")
+    ll.gemm_mxf8(ll.IN_E4M3, ll.IN_E4M3, M, N, 0, 1.0, None, 0, None, 0, None, N, None, 0, 2.5, up(C), N, tD, N,
+                 ll.OUT_F32)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK
+    want = torch.from_numpy((np.float32(2.5) * C).astype(np.float32))
+    assert torch.equal(tD.cpu(), want)

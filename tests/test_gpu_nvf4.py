@@ -147,3 +147,16 @@ def test_nvf4_8192_full_size(orc):
     """The NVFP4 workload at full size (8192^3, BF16 out), every element."""
     cfg = wl.WORKLOADS["nvf4_gemm_8192"]
     run_nvf4(orc, cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"], cfg["out"])
+
+
+def test_nvf4_k_zero_is_beta_c():
+    """K = 0: an empty contraction, D = beta * C exactly (no scale codes or workspace read)."""
+    import linear_layer_gb300 as ll
+    M, N = 300, 260
+    C = wl.f32_normal(M, N, 77)
+    tD = out_tensor(M, N, "f32")
+    ll.gemm_nvf4(M, N, 0, 1.0, None, 0, None, 0, None, 0, None, 0, -0.75, up(C), N, tD, N, ll.OUT_F32)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK
+    want = torch.from_numpy((np.float32(-0.75) * C).astype(np.float32))
+    assert torch.equal(tD.cpu(), want)
