@@ -256,10 +256,14 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
         sets.append((_up(A, dev), _up(B, dev), _up(C, dev),
                      torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
 
+    # the workspace the library asks for (here: the partial tiles of its stream-K tail)
+    ws_bytes = ll.gemm_workspace_size(M, N, K, K, N, ll.IN_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+
     def step(i):
         a, b, c, d = sets[i % nsets]
         ll.gemm_bf16(M, N, K, cfg["alpha"], a, K, b, N, cfg["beta"], c, N, d, N, ll.OUT_BF16,
-                     stream=stream)
+                     workspace=ws, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -335,7 +339,7 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
             if i >= 2:
                 stream.wait_event(ev_out[b])  # D of step i-2 has left buffer b
             ll.gemm_bf16(M, N, K, cfg["alpha"], a, K, bb, N, cfg["beta"], c, N, d, N, ll.OUT_BF16,
-                         stream=stream)
+                         workspace=ws, stream=stream)
             ev_mm[b].record(stream)
             s_out.wait_event(ev_mm[b])
             with torch.cuda.stream(s_out):
@@ -371,6 +375,7 @@ def bench_headline(args, dev, stream, rank, world, peaks, peak_src):
                       "beta": cfg["beta"], "out": "bf16", "accumulate": "fp32",
                       "l2": "inputs rotate over %d resident sets (%.0f MB > L2)" % (
                           nsets, nsets * set_bytes / 1e6),
+                      "workspace_bytes": ws_bytes,
                       "parallelism": "replicas" if world > 1 else "single"}}
     del sets
     return out

@@ -291,16 +291,26 @@ ll_status gemm_common(const ll::GemmArgs& a, void* workspace, size_t ws_bytes, l
   if (a.K == 0) return ll::launch_scale_c(a, ctx);
   const ll::RepackPlan plan = ll::plan_repack(a);
   void* base = nullptr;
+  size_t need = 0;
   if (plan.a || plan.b || plan.mx) {
     const int es = in_esize(a.in_type);
-    size_t need = 0;
     if (plan.a) need += repack_bytes(a.M, a.nvf4 ? a.K / 2 : a.K, es);
     if (plan.b) need += a.nvf4 ? repack_bytes(a.N, a.K / 2, es) : repack_bytes(a.K, a.N, es);
     if (plan.mx) need += plan.xa_bytes + plan.xb_bytes + 512;
     if (workspace == nullptr || ws_bytes < need) return LL_ERR_WORKSPACE;
-    base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
   }
-  return ll::launch_gemm_planned(a, plan, base, ctx);
+  if (workspace != nullptr)
+    base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
+  ll::GemmArgs b = a;
+  if (base != nullptr && !a.mx) {  // what the repacks leave: the stream-K partial tiles
+    const size_t skip = static_cast<size_t>(round_up(static_cast<int64_t>(need), 256)) +
+                        (reinterpret_cast<uintptr_t>(base) - reinterpret_cast<uintptr_t>(workspace));
+    if (ws_bytes > skip) {
+      b.sk_ws = static_cast<unsigned char*>(workspace) + skip;
+      b.sk_bytes = ws_bytes - skip;
+    }
+  }
+  return ll::launch_gemm_planned(b, plan, base, ctx);
 }
 
 }  // namespace
@@ -340,6 +350,16 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
   size_t need = 0;
   if ((lda * es) % 16 != 0) need += repack_bytes(M, K, es);
   if ((ldb * es) % 16 != 0) need += repack_bytes(K, N, es);
+  if (in_type == LL_IN_F16 || in_type == LL_IN_BF16) {  // the optional stream-K tail
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+      const size_t sk = ll::pair_sk_workspace(M, N, K, sms);
+      if (sk) need = static_cast<size_t>(round_up(static_cast<int64_t>(need), 256)) + 256 + sk;
+    } else {
+      cudaGetLastError();
+    }
+  }
   return need;
 }
 
@@ -383,6 +403,8 @@ static ll::GemmArgs dense_args(int in_type, int M, int N, int K, float alpha, co
   a.ld_sb = 0;
   a.mx = 0;
   a.nvf4 = 0;
+  a.sk_ws = nullptr;
+  a.sk_bytes = 0;
   a.mx_sa = nullptr;
   a.ld_mx_sa = 0;
   a.mx_sb = nullptr;

@@ -33,6 +33,9 @@
 #include <cstring>
 #include <mutex>
 
+#include <atomic>
+#include <chrono>
+
 #include "gemm_common.cuh"
 
 namespace ll {
@@ -554,6 +557,16 @@ struct PairSched {
   int num_m2, num_n;  // pair tiles in M (256 rows) and N (BN columns)
   int full_units;     // units that are whole tiles
   int num_units;      // full_units + 2 * split tiles
+  // stream-K tail: the sk_tiles tiles after the num_units whole ones are done by K ranges,
+  // one contiguous range of their K blocks per pair (0: none).  A pair whose range ends
+  // inside a tile writes that piece's FP32 partial to its slot of sk_part (two CTAs x 128
+  // rows x 256 columns) and sets its flags (sk_flag[(pair * 2 + rank) * 4 + warp quarter])
+  // to `epoch`; the pair whose range ends at a tile's end adds the partials of the pairs
+  // before it to its own, in pair order, and stores the tile.
+  int sk_tiles;
+  float* sk_part;
+  unsigned long long* sk_flag;
+  unsigned long long epoch;
 };
 
 // FP32 C and D whose rows do not start on 16-byte boundaries, as four row classes: class k
@@ -637,20 +650,75 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     n0 = nb * BN + (half > 0 ? BN / 2 : 0);
     ncols = half < 0 ? BN : BN / 2;
   };
+  // This pair's work items, in order: its stream-K pieces first — the piece that ends
+  // inside a tile (kind kSkPart: its partial goes to the workspace), then the pieces that
+  // end at a tile's end (kSkOwner when pairs before this one hold the tile's first K
+  // blocks, whose partials it adds; otherwise kWhole) — then its units (u = pair,
+  // pair + num_pairs, ...).  With the pieces first, every partial is written early, each
+  // owner adds them while its next tile's MMAs run, and the grid ends on whole tiles.
+  enum { kWhole = 0, kSkPart = 1, kSkOwner = 2 };
+  struct Item {
+    int m0, n0, ncols, kb0, kb1, kind, pfirst;
+  };
+  const int n_units = pair < sc.num_units ? (sc.num_units - 1 - pair) / num_pairs + 1 : 0;
+  const int64_t sk_total = static_cast<int64_t>(sc.sk_tiles) * KB;
+  auto sk_begin = [&](int q2) { return static_cast<int64_t>(q2) * sk_total / num_pairs; };
+  const int64_t sk_a = sk_begin(pair), sk_b = sk_begin(pair + 1);
+  const bool sk_has_part = sk_b > sk_a && sk_b % KB != 0;
+  const int sk_t0 = static_cast<int>(sk_a / KB);
+  const int sk_tend = sk_b > sk_a ? static_cast<int>((sk_b - 1) / KB) + (sk_has_part ? 0 : 1) : sk_t0;
+  const int n_sk = (sk_has_part ? 1 : 0) + (sk_tend > sk_t0 ? sk_tend - sk_t0 : 0);
+  const int n_items = n_sk + n_units;
+  auto item = [&](int i) {
+    Item it;
+    it.pfirst = pair;
+    if (i >= n_sk) {
+      unit(pair + (i - n_sk) * num_pairs, it.m0, it.n0, it.ncols);
+      it.kb0 = 0;
+      it.kb1 = KB;
+      it.kind = kWhole;
+      return it;
+    }
+    const int j = i;
+    int t;
+    if (sk_has_part && j == 0) {
+      t = static_cast<int>((sk_b - 1) / KB);
+      it.kind = kSkPart;
+      it.kb1 = static_cast<int>(sk_b - static_cast<int64_t>(t) * KB);
+    } else {
+      t = sk_t0 + j - (sk_has_part ? 1 : 0);
+      it.kb1 = KB;
+    }
+    const int64_t t0 = static_cast<int64_t>(t) * KB;
+    it.kb0 = static_cast<int>((sk_a > t0 ? sk_a : t0) - t0);
+    if (!(sk_has_part && j == 0)) {
+      it.kind = it.kb0 > 0 ? kSkOwner : kWhole;
+      if (it.kind == kSkOwner) {  // the pairs whose ranges end inside this tile
+        int pf = pair;
+        while (pf > 0 && sk_begin(pf) > t0) --pf;
+        it.pfirst = pf;
+      }
+    }
+    int mb, nb;
+    tile_coords(sc.num_units + t, sc.num_m2, sc.num_n, p.group_m, mb, nb);
+    it.m0 = mb * 256;
+    it.n0 = nb * BN;
+    it.ncols = BN;
+    return it;
+  };
 
   // Programmatic dependent launch: everything above overlaps the previous kernel of
   // the stream; the producer also pulls its first ring of operand tiles into L2 (L2 is
   // coherent, so a prefetch may run ahead of the previous kernel's writes).  Operand
   // copies into shared memory, scale and C reads and D writes come after the wait.
-  if (warp == 0 && lane == 0 && pair < sc.num_units) {
-    int m0, n0, ncols;
-    unit(pair, m0, n0, ncols);
-    const int boxes = ncols / 2 / Cfg::B_BOX_N;
-    const int pre = KB < S ? KB : S;
-    for (int kb = 0; kb < pre; ++kb) {
-      tma_prefetch_l2(&tmA, kb * Cfg::BK, m0 + 128 * static_cast<int>(rank));
+  if (warp == 0 && lane == 0 && n_items > 0) {
+    const Item it0 = item(0);
+    const int boxes = it0.ncols / 2 / Cfg::B_BOX_N;
+    const int pre = it0.kb1 - it0.kb0 < S ? it0.kb1 - it0.kb0 : S;
+    for (int kb = it0.kb0; kb < it0.kb0 + pre; ++kb) {
+      tma_prefetch_l2(&tmA, kb * Cfg::BK, it0.m0 + 128 * static_cast<int>(rank));
       for (int j = 0; j < boxes; ++j)
-        tma_prefetch_l2(&tmB, n0 + static_cast<int>(rank) * (ncols / 2) + j * Cfg::B_BOX_N, kb * Cfg::BK);
+        tma_prefetch_l2(&tmB, it0.n0 + static_cast<int>(rank) * (it0.ncols / 2) + j * Cfg::B_BOX_N, kb * Cfg::BK);
     }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -662,12 +730,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       tma_prefetch_desc(&tmB);
       uint32_t it = 0;
       bool ok = true;
-      for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
-        int m0, n0, ncols;
-        unit(u, m0, n0, ncols);
+      for (int i = 0; i < n_items && ok; ++i) {
+        const Item w = item(i);
+        const int m0 = w.m0, n0 = w.n0, ncols = w.ncols;
         const int boxes = ncols / 2 / Cfg::B_BOX_N;
         const uint32_t bytes = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           const int s = it % S;
           if (!wait_bounded(empty_bar(s), ((it / S) & 1u) ^ 1u, wctx, kRoleProducer)) {
             ok = false;
@@ -694,15 +762,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (lane == 0 && rank == 0) {
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
-        int m0, n0, ncols;
-        unit(u, m0, n0, ncols);
-        const uint32_t idesc = make_idesc(AB_FMT, ncols, 256);
-        const uint32_t ab = acc_it & 1u;  // one accumulator per tile
+      for (int i = 0; i < n_items && ok; ++i) {
+        const Item w = item(i);
+        const uint32_t idesc = make_idesc(AB_FMT, w.ncols, 256);
+        const uint32_t ab = acc_it & 1u;  // one accumulator per item
         if (!wait_bounded(tempty_bar(ab), ((acc_it >> 1) & 1u) ^ 1u, wctx, kRoleMma)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * BN;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           const int s = it % S;
           if (!wait_bounded(full_bar(s), (it / S) & 1u, wctx, kRoleMma)) {
             ok = false;
@@ -716,7 +783,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc =
                 smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BOX_BYTES, 1024);
-            mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair_mc(empty_bar(s), 0x3);
           ++it;
@@ -750,22 +817,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const uint64_t pol_once = l2_evict_first_policy();
       const bool out32 = p.d_type == LL_OUT_F32;
       const bool bf = p.d_type == LL_OUT_BF16;
-      // prefetch cursor: the chunk whose C load is issued next
-      int pu = pair, pc = 0, pchunks = 0, pm = 0, pn = 0;
-      auto cursor_unit = [&](int u) {
-        pu = u;
+      // prefetch cursor: the chunk whose C load is issued next (items that end in a
+      // stream-K partial store no D and read no C)
+      int pu = 0, pc = 0, pchunks = 0, pm = 0, pn = 0;
+      auto cursor_item = [&](int i) {
+        while (i < n_items && item(i).kind == kSkPart) ++i;
+        pu = i;
         pc = 0;
-        if (u < sc.num_units) {
-          int m0, n0, ncols;
-          unit(u, m0, n0, ncols);
-          pm = m0 + row_off;
-          pn = n0;
-          pchunks = ncols / 32;
+        if (i < n_items) {
+          const Item w = item(i);
+          pm = w.m0 + row_off;
+          pn = w.n0;
+          pchunks = w.ncols / 32;
         }
       };
       uint32_t issued = 0;  // C loads issued by this warp
       auto issue_c = [&]() {  // lane 0; call with the ring slot free
-        if (pu >= sc.num_units) return;
+        if (pu >= n_items) return;
         const int b = static_cast<int>(issued % R);
         const int n = pn + 32 * pc;
         if (n < p.N && pm < p.M) {
@@ -775,28 +843,70 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           mbar_arrive(cfull_bar(ew, b));
         }
         ++issued;
-        if (++pc == pchunks) cursor_unit(pu + num_pairs);
+        if (++pc == pchunks) cursor_item(pu + 1);
       };
       if (use_c) {
-        cursor_unit(pair);
+        cursor_item(0);
         if (lane == 0) {
           tma_prefetch_desc(&tmC);
           for (int i = 0; i < PF; ++i) issue_c();
         }
       }
       if (lane == 0) tma_prefetch_desc(&tmD);
+      // a stream-K slot holds the CTA's 128 rows x 256 columns as [chunk c][4-column group
+      // j][row][4]: the 32 lanes (rows) of a warp access 512 contiguous bytes at a time
+      auto sk_vec = [&](int slot, int c, int j) {
+        return reinterpret_cast<float4*>(sc.sk_part + (static_cast<size_t>(slot) * 2 + rank) * (128 * 256)) +
+               ((c * 8 + j) * 128 + q * 32 + lane);
+      };
+      auto sk_flag = [&](int slot) { return sc.sk_flag + (static_cast<size_t>(slot) * 2 + rank) * 4 + q; };
       uint32_t acc_it = 0, g = 0;
       bool ok = true;
-      for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
-        int m0, n0, ncols;
-        unit(u, m0, n0, ncols);
+      for (int i = 0; i < n_items && ok; ++i) {
+        const Item w = item(i);
+        const int m0 = w.m0, n0 = w.n0, ncols = w.ncols;
         const uint32_t ab = acc_it & 1u;
+        const int chunks = ncols / 32;
+        if (w.kind == kSkOwner) {  // a tile this pair completes: the pairs before it are done
+          bool fw = true;
+          if (lane == 0)
+            for (int pc2 = w.pfirst; pc2 < pair && fw; ++pc2) fw = flag_wait_bounded(sk_flag(pc2), sc.epoch, wctx, kRoleEpilogue);
+          fw = __shfl_sync(0xffffffffu, fw ? 1 : 0, 0) != 0;
+          __syncwarp();  // lane 0's acquire, before every lane's reads of the partials
+          if (!fw) {
+            ok = false;
+            break;
+          }
+        }
         ok = wait_bounded(tfull_bar(ab), (acc_it >> 1) & 1u, wctx, kRoleEpilogue);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        if (w.kind == kSkPart) {
+          // a stream-K piece that ends inside its tile: its FP32 partial goes to this pair's
+          // slot, then the flag tells the pair that completes the tile
+#pragma unroll 1
+          for (int c = 0; c < chunks; ++c) {
+            uint32_t r[32];
+            tmem_ld_x32(tmem_base + lane_base + ab * BN + c * 32, r);
+            tmem_ld_wait(r);
+            if (c == chunks - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *sk_vec(pair, c, j) = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) flag_release(sk_flag(pair), sc.epoch);
+          ++acc_it;
+          continue;
+        }
         const int m_w = m0 + row_off;
-        const int chunks = ncols / 32;
 #pragma unroll 1
         for (int c = 0; c < chunks; ++c, ++g) {
           const int b = static_cast<int>(g % R);
@@ -819,13 +929,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (lane == 0) mbar_arrive_cluster_relaxed(mapa_cluster(tempty_bar(ab), 0));
           }
           float o[32];
+          if (w.kind == kSkOwner) {  // own partial, then the others' in pair order, then alpha
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = p.alpha * __uint_as_float(r[j]);
+            for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(r[j]);
+            for (int pc2 = w.pfirst; pc2 < pair; ++pc2) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 v = __ldcg(sk_vec(pc2, c, j));
+                o[4 * j] += v.x;
+                o[4 * j + 1] += v.y;
+                o[4 * j + 2] += v.z;
+                o[4 * j + 3] += v.w;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] *= p.alpha;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = p.alpha * __uint_as_float(r[j]);
+          }
           const float4* row = reinterpret_cast<const float4*>(ebuf + b * Cfg::EPI_BUF_BYTES + lane * 128);
           if (use_c) {
-            bool w = wait_bounded(cfull_bar(ew, b), (g / R) & 1u, wctx, kRoleEpilogue);
-            w = __all_sync(0xffffffffu, w);
-            if (!w) {
+            bool cw = wait_bounded(cfull_bar(ew, b), (g / R) & 1u, wctx, kRoleEpilogue);
+            cw = __all_sync(0xffffffffu, cw);
+            if (!cw) {
               ok = false;
               break;
             }
@@ -1177,6 +1304,44 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
 }
 
 
+// stream-K tail: one 256 x 256 FP32 partial slot (two CTAs x 128 rows) and 8 flags per pair
+size_t pair_sk_bytes(int pairs) {
+  return static_cast<size_t>(pairs) * (2 * 128 * 256 * sizeof(float) + 8 * sizeof(unsigned long long));
+}
+
+// The schedule's tail: W whole waves of P pairs and R more tiles.  The R tiles are split by
+// K ranges across all P pairs when there are at least P / 4 of them and at least 8 K blocks
+// a tile (so that no tile has more than ~4 pieces); fewer run as 256 x 128 halves.
+static bool pair_sk_tail(int T, int P, int KB, int& W, int& R) {
+  W = T / P;
+  R = T - W * P;
+  return W >= 1 && R > 0 && 4 * R >= P && KB >= 8;
+}
+
+size_t pair_sk_workspace(int M, int N, int K, int num_sms) {
+  const int P = num_sms / 2;
+  if (P <= 0) return 0;
+  const int T = ((M + 255) / 256) * ((N + 255) / 256);
+  const int KB = (K + PairCfg<256>::BK - 1) / PairCfg<256>::BK;
+  int W, R;
+  return pair_sk_tail(T, P, KB, W, R) ? pair_sk_bytes(P) : 0;
+}
+
+// A value no flag of an earlier call holds: a per-process random high word over a call count.
+static unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> seq{0};
+  static const unsigned long long salt = [] {
+    unsigned long long x = static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                           static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(&seq));
+    x += 0x9E3779B97F4A7C15ull;  // splitmix64 finaliser
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    x ^= x >> 31;
+    return (x | 1ull) << 32;
+  }();
+  return salt | ((seq.fetch_add(1) + 1) & 0xFFFFFFFFull);
+}
+
 template <uint32_t AB_FMT>
 static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   using Cfg = PairCfg<256>;
@@ -1271,6 +1436,25 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   } else {
     sc.full_units = T;
     sc.num_units = T;
+  }
+  sc.sk_tiles = 0;
+  sc.sk_part = nullptr;
+  sc.sk_flag = nullptr;
+  sc.epoch = 0;
+  {  // stream-K tail (TMA epilogue only), when the caller's workspace has room for it
+    const int KB = (a.K + Cfg::BK - 1) / Cfg::BK;
+    int W, R;
+    if (p.epi_tma && T > max_pairs[dev] && pair_sk_tail(T, max_pairs[dev], KB, W, R) && a.sk_ws != nullptr &&
+        a.sk_bytes >= pair_sk_bytes(max_pairs[dev])) {
+      P = max_pairs[dev];
+      sc.full_units = W * P;
+      sc.num_units = W * P;
+      sc.sk_tiles = R;
+      sc.sk_part = static_cast<float*>(a.sk_ws);
+      sc.sk_flag = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(a.sk_ws) +
+                                                         static_cast<size_t>(P) * 2 * 128 * 256 * sizeof(float));
+      sc.epoch = next_epoch();
+    }
   }
   cfg.gridDim = dim3(2 * P);
   if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, tmD, p, sc, rm) != cudaSuccess) {

@@ -45,7 +45,16 @@ struct GemmArgs {
   int64_t ld_mx_sb;
   const uint8_t* mx_sat;  // MX: the scale codes rearranged into tcgen05.cp blocks (workspace)
   const uint8_t* mx_sbt;
+  void* sk_ws;            // workspace left after any repack (256-byte aligned), for the
+  size_t sk_bytes;        //   stream-K partial tiles of the CTA-pair GEMM; NULL / 0: none
 };
+
+// Workspace bytes the CTA-pair 16-bit GEMM uses to split its last partial wave of tiles
+// by K ranges (stream-K), for up to `pairs` CTA pairs (gemm_tc.cu).
+size_t pair_sk_bytes(int pairs);
+// Those bytes for an M x N x K 16-bit problem on a GPU with num_sms SMs, or 0 when its
+// schedule has no such tail (gemm_tc.cu).
+size_t pair_sk_workspace(int M, int N, int K, int num_sms);
 
 // Launch context of the current device (status word, SM count, wait limit) for `stream`;
 // LL_ERR_NO_DEVICE unless an sm_103 device is current (abi.cu).  Device addresses of the

@@ -82,6 +82,8 @@ extern "C" ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const
   a.ld_sb = 0;
   a.mx = 0;
   a.nvf4 = 0;
+  a.sk_ws = nullptr;
+  a.sk_bytes = 0;
   a.mx_sa = nullptr;
   a.ld_mx_sa = 0;
   a.mx_sb = nullptr;

@@ -170,6 +170,40 @@ __device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
+// ---------------------------------------------------------------- flags between CTAs of one grid
+
+// Publish a 64-bit flag (release at GPU scope: the calling thread's earlier writes, and
+// those ordered before them, are visible to a thread that observes the value with
+// flag_acquire).
+__device__ __forceinline__ void flag_release(unsigned long long* f, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long flag_acquire(const unsigned long long* f) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+  return v;
+}
+
+// Wait until *f == v, bounded like wait_bounded (only CTAs of the same grid, all resident,
+// set such flags).
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned long long* f, unsigned long long v,
+                                                  const WaitCtx& ctx, uint32_t role) {
+  if (flag_acquire(f) == v) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (flag_acquire(f) == v) return true;
+    if ((it & 15u) == 0) {
+      if (*ctx.abort) return false;
+      if (global_timer_ns() - t0 > ctx.timeout_ns) {
+        atomicCAS(ctx.status, 0u, kStatusTimeout | (role << 8));
+        *ctx.abort = 1u;
+        __threadfence_block();
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- cp.async (4-byte)
 
 // Asynchronous 4-byte copy global -> shared (the thread's own element; completes with
