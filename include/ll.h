@@ -89,6 +89,16 @@ typedef enum { LL_OUT_F32 = 0, LL_OUT_BF16 = 1, LL_OUT_F16 = 2 } ll_out_type;
  * (row pitch rounded up to 16 bytes) inside the same stream, and that copy is part
  * of the call.  The figure assumes 16-byte-aligned base pointers; a misaligned base
  * pointer is repacked too and needs at most ll_gemm_workspace_size(...,lda=1,ldb=1).
+ * For FP16 / BF16 inputs the figure also holds room for the partial accumulators of
+ * the stream-K tail (when a CUDA device is current and the problem leaves a partial
+ * last wave of 256 x 256 tiles): the K blocks of the last tiles are then split evenly
+ * over all SM pairs, and a pair that ends inside a tile leaves its FP32 partial and a
+ * ready flag in the workspace for the pair that finishes the tile.  That room is
+ * optional: with less workspace (or none) the call still succeeds and finishes the
+ * last wave with half-width tiles instead.  The split changes only the order in which
+ * FP32 partial sums over K are added (partials are added in a fixed order), so the
+ * result is deterministic for a given problem and workspace size.  A workspace must
+ * not be shared by calls that may run at the same time (other streams, other threads).
  */
 size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int in_type);
 
@@ -107,7 +117,8 @@ size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int
  *       written); any other overlap of D with A, B or C is rejected (LL_ERR_INVALID_ARG).
  *       Nothing outside the M x N elements of D is written (padding columns included).
  *   workspace : device scratch of ws_bytes (see ll_gemm_workspace_size); may be NULL if 0.
- *       When a repack will write it, it may overlap no operand (LL_ERR_INVALID_ARG).
+ *       The call may write any of it (repacked operands, stream-K partial tiles), so it
+ *       may overlap no operand (LL_ERR_INVALID_ARG).
  * Every product is accumulated in FP32 over the whole K; alpha * acc + beta * C is
  * evaluated in FP32 and rounded once to d_type (round to nearest even).
  * M == 0 or N == 0: nothing is done.  K == 0: D = beta * C (alpha is not used).

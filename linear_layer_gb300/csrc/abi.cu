@@ -197,7 +197,8 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
       return LL_ERR_INVALID_ARG;
   }
   // D may share bytes with no input other than itself as C (in place, checked above);
-  // a workspace that a repack will write may share bytes with nothing
+  // a workspace that a repack or the stream-K tail (16-bit inputs) may write shares
+  // bytes with nothing
   const int64_t es = in_esize(a.in_type);
   const bool c_read = a.beta != 0.0f;
   const bool in_place = c_read && static_cast<const void*>(a.C) == a.D;
@@ -220,7 +221,7 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
   if (outputs_overlap(&D, 1, ins, 5)) return LL_ERR_INVALID_ARG;
   if (a.K > 0 && ws != nullptr && ws_bytes > 0) {
     const RepackPlan plan = plan_repack(a);
-    if (plan.a || plan.b || plan.mx) {
+    if (plan.a || plan.b || plan.mx || sk_capable(a)) {
       const Extent W{ws, 1, static_cast<int64_t>(ws_bytes), static_cast<int64_t>(ws_bytes)};
       Extent all[6] = {D, ins[0], ins[1], ins[2], ins[3], ins[4]};
       if (in_place) all[3] = Extent{a.C, a.M, a.N * 4, a.ldc * 4};
@@ -302,7 +303,7 @@ ll_status gemm_common(const ll::GemmArgs& a, void* workspace, size_t ws_bytes, l
   if (workspace != nullptr)
     base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
   ll::GemmArgs b = a;
-  if (base != nullptr && !a.mx) {  // what the repacks leave: the stream-K partial tiles
+  if (base != nullptr && ll::sk_capable(a)) {  // what the repacks leave: the stream-K partial tiles
     const size_t skip = static_cast<size_t>(round_up(static_cast<int64_t>(need), 256)) +
                         (reinterpret_cast<uintptr_t>(base) - reinterpret_cast<uintptr_t>(workspace));
     if (ws_bytes > skip) {

@@ -55,6 +55,10 @@ size_t pair_sk_bytes(int pairs);
 // Those bytes for an M x N x K 16-bit problem on a GPU with num_sms SMs, or 0 when its
 // schedule has no such tail (gemm_tc.cu).
 size_t pair_sk_workspace(int M, int N, int K, int num_sms);
+// Whether the call may place stream-K partial tiles in its workspace: FP16 / BF16 inputs.
+inline bool sk_capable(const GemmArgs& a) {
+  return !a.mx && !a.nvf4 && (a.in_type == LL_IN_F16 || a.in_type == LL_IN_BF16);
+}
 
 // Launch context of the current device (status word, SM count, wait limit) for `stream`;
 // LL_ERR_NO_DEVICE unless an sm_103 device is current (abi.cu).  Device addresses of the

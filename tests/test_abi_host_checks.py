@@ -75,8 +75,8 @@ def child_results():
 
 
 def _gemm(ll, M=64, N=64, K=64, A=P, lda=64, B=P, ldb=64, beta=0.0, C=None, ldc=64, D=P + 0x100000,
-          ldd=64, d_type=0, fn="ll_gemm_f16"):
-    return getattr(ll.lib, fn)(M, N, K, 1.0, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, None, 0, None)
+          ldd=64, d_type=0, fn="ll_gemm_f16", ws=None, ws_bytes=0):
+    return getattr(ll.lib, fn)(M, N, K, 1.0, A, lda, B, ldb, beta, C, ldc, D, ldd, d_type, ws, ws_bytes, None)
 
 
 def _no_device(ll, st):
@@ -100,6 +100,17 @@ def check_gemm_rejections(ll):
     assert _gemm(ll, D=P + 0x100001, d_type=ll.OUT_BF16) == MIS           # nor a 2-byte one
     assert _gemm(ll, beta=0.5, C=P + 0x200002) == MIS                     # C read: 4-byte aligned
     assert _gemm(ll, fn="ll_gemm_bf16", ldb=10) == E
+
+
+@check
+def check_gemm_workspace_may_not_overlap(ll):
+    """A 16-bit GEMM may write its workspace (stream-K partial tiles) even when nothing is
+    repacked, so a workspace that shares bytes with D or an input is rejected."""
+    E = ll.LL_ERR_INVALID_ARG
+    D = P + 0x100000
+    assert _gemm(ll, ws=D + 0x800, ws_bytes=1 << 20) == E                    # inside D
+    assert _gemm(ll, ws=P + 0x40, ws_bytes=1 << 20, fn="ll_gemm_bf16") == E  # inside A and B
+    assert _no_device(ll, _gemm(ll, ws=P + 0x400000, ws_bytes=1 << 20))     # disjoint: accepted
 
 
 @check
