@@ -17,12 +17,14 @@ namespace ll {
 // the two aligned 16-byte words that cover its 16 source bytes and funnel-shifts them
 // into place, so every global access is a full 16-byte vector.  A word is read only if
 // it holds at least one byte of the row, and an aligned 16-byte word never crosses a
-// page, so no read leaves the source allocation's pages.  The kernel lets the
-// programmatically launched GEMM behind it start its prologue at once; the GEMM's
-// dependency wait still covers every write made here.
+// page, so no read leaves the source allocation's pages.  The kernel is itself launched
+// programmatically: its blocks may be scheduled while the previous kernel of the stream
+// finishes, and touch memory only after the dependency wait.  It lets the GEMM behind it
+// start its prologue at once; the GEMM's dependency wait still covers every write made here.
 __global__ void repack_kernel(const uint8_t* __restrict__ src, int64_t ld_src, uint8_t* __restrict__ dst,
                               int64_t ld_dst, int rows, int64_t row_bytes) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t vec_per_row = ld_dst / 16;
   const int64_t total = static_cast<int64_t>(rows) * vec_per_row;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -72,10 +74,19 @@ ll_status launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_d
   const int64_t vecs = static_cast<int64_t>(rows) * (ld_dst * esize / 16);
   int64_t blocks = (vecs + threads - 1) / threads;
   if (blocks > 8 * ctx.num_sms) blocks = 8 * ctx.num_sms;
-  repack_kernel<<<static_cast<int>(blocks), threads, 0, ctx.stream>>>(
-      static_cast<const uint8_t*>(src), ld_src * esize, static_cast<uint8_t*>(dst), ld_dst * esize, rows,
-      static_cast<int64_t>(cols) * esize);
-  return cudaGetLastError() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, repack_kernel, static_cast<const uint8_t*>(src), ld_src * esize,
+                         static_cast<uint8_t*>(dst), ld_dst * esize, rows, static_cast<int64_t>(cols) * esize);
+  return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
 __global__ void scale_c_kernel(int M, int N, float beta, const float* __restrict__ C, int64_t ldc,

@@ -569,17 +569,22 @@ struct PairSched {
   unsigned long long epoch;
 };
 
-// FP32 C and D whose rows do not start on 16-byte boundaries, as four row classes: class k
-// holds rows k, k + 4, k + 8, ..., 16 * ld bytes apart (a pitch a tensor map can describe),
-// its map starting at the first 16-byte boundary of row k, off_k = 0..3 elements in; all rows
-// of a class then have the same offset.  Column c of a row of class k is element c - off_k of
-// that map's row.  Boxes: C 36 x 8 (loaded from x = n - 4, which covers columns n .. n + 31
-// whatever off_k is), D 32 x 8 when off_k = 0 and 28 x 8 otherwise (stored at x = n: columns
-// n + off_k .. n + off_k + 27, the other 4 columns of the chunk by the lanes).
+// FP32 C whose rows do not start on 16-byte boundaries, as four row classes: class k holds
+// rows k, k + 4, k + 8, ..., 16 * ldc bytes apart (a pitch a tensor map can describe), its
+// map starting at the first 16-byte boundary of row k, off_k = 0..3 elements in; all rows of
+// a class then have the same offset.  Column c of a row of class k is element c - off_k of
+// that map's row.  Boxes of 36 x 8, loaded from x = n - 4, cover columns n .. n + 31 whatever
+// off_k is.  (D of such rows is stored by the lanes in whole 32-byte sectors, see the kernel.)
 struct EpiResMaps {
   CUtensorMap c[4];
-  CUtensorMap d[4];
 };
+
+// 32 bytes to a 32-byte-aligned global address in one store, with an L2 cache policy.
+__device__ __forceinline__ void st_global_v8_hint(float* p, const float* v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "f"(v[0]),
+               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "l"(pol)
+               : "memory");
+}
 
 template <class Cfg, uint32_t AB_FMT>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
@@ -997,19 +1002,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       }
       __syncwarp();
     } else if (p.epi_res) {
-      // FP32 D rows (and C rows) that do not start on 16-byte boundaries, through TMA by
-      // row classes (EpiResMaps).  Each lane keeps its own accumulator row (no transpose):
-      // lane l is row m_w + l, of class l & 3, row l >> 2 of that class's 8-row box.  C
-      // arrives two chunks ahead in a ring of two slots of four 36 x 8 boxes; the lane reads
-      // its row's 32 values at box column 4 - off + t (columns left of the map's first
-      // element, only in the chunk at column 0, are read by the lane itself).  D goes to
-      // four staging boxes (the lane's values shifted by its class's offset) and out with
-      // four TMA stores; the at most 4 columns of the chunk outside its class's box are
-      // stored by the lane.  Every value is fma(beta, C, alpha * acc) in FP32, as on the
-      // other paths.
+      // FP32 D rows that do not start on 16-byte boundaries.  Each lane keeps its own
+      // accumulator row (no transpose): lane l is row m_w + l.  C arrives by TMA by row
+      // classes (EpiResMaps) two chunks ahead, in a ring of two slots of four 36 x 8 boxes
+      // (box k holds the warp's rows of class k); the lane reads its row's 32 values at box
+      // column 4 - off + t (the columns left of a map's first element, only in the chunk at
+      // column 0, are read by the lane itself).  D is stored by the lanes in whole 32-byte
+      // sectors: a store that covers only part of a sector makes the memory system read
+      // the rest of it first, which with rows off the sector grid would happen at every
+      // chunk edge.  With od = 0..7 the offset of the row's first 32-byte boundary at or
+      // after the tile's first column n0, chunk c writes the four sectors that start at
+      // columns n0 + 32 c - 8 + od, ..., n0 + 32 c + 16 + od: the window of 32 values that
+      // starts od values into (previous chunk's last 8 values, this chunk's 32).  Only the
+      // sectors cut by the tile's edges or by column N are written element by element.
+      // Every value is fma(beta, C, alpha * acc) in FP32, as on the other paths.
       constexpr int CBOX = 8 * 36 * 4;
       constexpr int CSLOT = 4 * CBOX;
-      uint8_t* dstage = ebuf + 2 * CSLOT;  // four D boxes of up to 8 x 32 FP32, 1 KB apart
       const bool use_c = p.beta != 0.0f;
       const uint64_t pol_once = l2_evict_first_policy();  // C read once, D written once
       const int rc = lane & 3, jr = lane >> 2;
@@ -1051,10 +1059,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           issue_c();
         }
       }
-      if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tma_prefetch_desc(&rm.d[k]);
-      }
       uint32_t acc_it = 0, g = 0;
       bool ok = true;
       for (int u = pair; u < sc.num_units && ok; u += num_pairs) {
@@ -1067,13 +1071,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tc_fence_after();
         const int m_w = m0 + row_off;
         const int m = m_w + lane;
-        // this lane's row: its class's offset to the first 16-byte boundary (the address is
-        // only formed, never read, for rows past M)
+        const bool row_ok = m < p.M;
+        // this lane's row (the addresses are only formed, never used, for rows past M)
         const float* crow = p.C + static_cast<int64_t>(m) * p.ldc;
-        float* drow = static_cast<float*>(p.D) + static_cast<int64_t>(m) * p.ldd;
+        float* dtile = static_cast<float*>(p.D) + static_cast<int64_t>(m) * p.ldd + n0;
         const int off_c = use_c ? static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(crow) >> 2) & 3u)) & 3u) : 0;
-        const int off_d = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(drow) >> 2) & 3u)) & 3u);
-        const int wd = off_d ? 28 : 32;
+        const int od = static_cast<int>((8u - ((reinterpret_cast<uintptr_t>(dtile) >> 2) & 7u)) & 7u);
+        const int len = min(ncols, p.N - n0);  // valid columns of the unit
+        // one sector of the window: columns a .. a + 7 of the unit, whole when it lies in
+        // [0, len), element by element where it is cut
+        auto put_sector = [&](int a, const float* v) {
+          if (a >= 0 && a + 8 <= len) {
+            st_global_v8_hint(dtile + a, v, pol_once);
+          } else if (a < len && a + 8 > 0) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (a + t >= 0 && a + t < len) dtile[a + t] = v[t];
+          }
+        };
+        float carry[8];  // the previous chunk's last 8 values
+#pragma unroll
+        for (int t = 0; t < 8; ++t) carry[t] = 0.0f;
         const int chunks = ncols / 32;
 #pragma unroll 1
         for (int c = 0; c < chunks; ++c, ++g) {
@@ -1098,7 +1116,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
               break;
             }
             const float* cb = reinterpret_cast<const float*>(ebuf + b * CSLOT + rc * CBOX) + jr * 36 + 4 - off_c;
-            const bool lead = n == 0 && m < p.M;  // columns left of the class map's first element
+            const bool lead = n == 0 && row_ok;  // columns left of the class map's first element
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
               const float cv = (t < 3 && lead && t < off_c) ? crow[t] : cb[t];
@@ -1108,52 +1126,43 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             __syncwarp();
             if (lane == 0 && static_cast<int>(issued - g) < 3) issue_c();  // chunk g + 2 into this slot
           }
-          if (n < p.N && n + 32 > p.N) {
-            // the chunk that crosses column N: a TMA store writes the whole 16-byte unit that
-            // holds column N - 1, which with tight rows reaches into the next row, so each
-            // lane stores its row's valid columns itself
-            if (m < p.M) {
+          // window w[i] = (carry, o)[od + i]: three fixed-distance selections on od's bits
+          float w1[39], w2[37], wv[32];
 #pragma unroll
-              for (int t = 0; t < 32; ++t)
-                if (n + t < p.N) drow[n + t] = o[t];
-            }
-          } else if (n < p.N) {
-            // s[k] = o[k + off_d] through two fixed-index selections
-            float s1[32], s2[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) s1[k] = (off_d & 1) ? (k + 1 < 32 ? o[k + 1] : 0.0f) : o[k];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) s2[k] = (off_d & 2) ? (k + 2 < 32 ? s1[k + 2] : 0.0f) : s1[k];
-            if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the staging
-            __syncwarp();
-            float4* ds = reinterpret_cast<float4*>(dstage + rc * 1024 + jr * wd * 4);
-#pragma unroll
-            for (int i = 0; i < 7; ++i) ds[i] = make_float4(s2[4 * i], s2[4 * i + 1], s2[4 * i + 2], s2[4 * i + 3]);
-            if (wd == 32) ds[7] = make_float4(s2[28], s2[29], s2[30], s2[31]);
-            if (m < p.M) {  // the chunk's columns outside this class's box
-#pragma unroll
-              for (int t = 0; t < 3; ++t)
-                if (t < off_d && n + t < p.N) drow[n + t] = o[t];
-#pragma unroll
-              for (int t = 29; t < 32; ++t)
-                if (off_d > 0 && t >= off_d + 28 && n + t < p.N) drow[n + t] = o[t];
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && m_w < p.M) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k) tma_store_2d_hint(&rm.d[k], smem_addr(dstage + k * 1024), n, m_w / 4, pol_once);
-              bulk_commit_group();
-            }
+          for (int i = 0; i < 39; ++i) {
+            const float x0 = i < 8 ? carry[i] : o[i - 8];
+            const float x1 = i + 1 < 8 ? carry[i + 1] : o[i - 7];
+            w1[i] = (od & 1) ? x1 : x0;
           }
+#pragma unroll
+          for (int i = 0; i < 37; ++i) w2[i] = (od & 2) ? w1[i + 2] : w1[i];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) wv[i] = (od & 4) ? w2[i + 4] : w2[i];
+          if (row_ok && 32 * c - 8 + od < len) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) put_sector(32 * c - 8 + od + 8 * k, wv + 8 * k);
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t) carry[t] = o[24 + t];
+        }
+        if (!ok) break;
+        // the unit's last sector: columns 32 * chunks - 8 + od .. of the last chunk's values
+        if (row_ok) {
+          float last[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            float v = carry[t];
+#pragma unroll
+            for (int k = 1; k < 8; ++k)
+              if (od == k) v = t + k < 8 ? carry[t + k] : 0.0f;
+            last[t] = v;
+          }
+          put_sector(32 * chunks - 8 + od, last);
         }
         ++acc_it;
       }
-      if (lane == 0) {
-        if (!ok && use_c) {  // C loads still in flight land before the CTA may exit
-          for (uint32_t j = g; j < issued; ++j) wait_drain(cfull_bar(ew, static_cast<int>(j & 1u)), (j >> 1) & 1u, p.timeout_ns);
-        }
-        bulk_wait_all();
+      if (lane == 0 && !ok && use_c) {  // C loads still in flight land before the CTA may exit
+        for (uint32_t j = g; j < issued; ++j) wait_drain(cfull_bar(ew, static_cast<int>(j & 1u)), (j >> 1) & 1u, p.timeout_ns);
       }
       __syncwarp();
     } else {
@@ -1361,17 +1370,13 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   memset(&tmD, 0, sizeof(tmD));
   const bool o32 = a.d_type == LL_OUT_F32;
   p.epi_tma = p.d_row16 && (a.beta == 0.0f || p.c_vec);
-  // FP32 D rows not on 16-byte boundaries: TMA by row classes (EpiResMaps)
+  // FP32 D rows not on 16-byte boundaries: C through TMA by row classes (EpiResMaps), D by
+  // whole 32-byte sectors from the lanes
   EpiResMaps rm;
   memset(&rm, 0, sizeof(rm));
   p.epi_res = !p.epi_tma && o32 && a.M >= 4 && a.N >= 4;
   if (p.epi_res) {
     for (int k = 0; k < 4; ++k) {
-      const float* drow = static_cast<const float*>(a.D) + static_cast<int64_t>(k) * a.ldd;
-      const int off_d = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(drow) >> 2) & 3u)) & 3u);
-      if (!make_tensor_map_2d(&rm.d[k], drow + off_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (a.M - k + 3) / 4,
-                              a.N - off_d, 4 * a.ldd, off_d ? 28 : 32, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return LL_ERR_CUDA;
       if (a.beta != 0.0f) {
         const float* crow = a.C + static_cast<int64_t>(k) * a.ldc;
         const int off_c = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(crow) >> 2) & 3u)) & 3u);
