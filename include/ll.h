@@ -186,7 +186,10 @@ ll_status ll_gemm_fp8_blockscaled(int M, int N, int K, float alpha, const uint8_
  *   - Every call shares the one scratch array and overwrites what it reads, so calls
  *     that overlap on the GPU (for instance on different streams) race: serialise
  *     them.
- * Results equal those of ll_gemm_f16 with workspace; errors as for ll_gemm_f16.
+ * Results equal, bit for bit, those of ll_gemm_f16 given a workspace of exactly the
+ * repack bytes; it never splits the last wave of tiles by K (that needs workspace), so
+ * where ll_gemm_f16 with a larger workspace does, the FP32 partial sums are added in
+ * another order and the results may differ in rounding.  Errors as for ll_gemm_f16.
  */
 ll_status ll_gemm_f16_noalloc(int M, int N, int K, float alpha, const void* A, int64_t lda,
                               const void* B, int64_t ldb, float beta, const float* C,

@@ -6,7 +6,9 @@ allowed), checked against ll_gemm_f16 with a caller-provided workspace.
 The new entry point repacks operands whose row pitch is not a multiple of 16 bytes
 into a fixed 16 MiB scratch array inside the library instead of the caller's
 workspace, with the same layout and the same kernels, so its output must equal the
-existing entry point's bit for bit.  Two calls run in a row, with different shapes and
+existing entry point's bit for bit (these shapes are too small for the stream-K split of
+the last wave, the one schedule that needs more workspace than the repacks and that
+this entry point never uses).  Two calls run in a row, with different shapes and
 inputs; the second call's repacked A lies over the bytes where the first call's
 repacked B was, so a repack that left any earlier bytes in place would change its
 output.  This file is collected last so that a run stopping at its first failure has
