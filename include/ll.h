@@ -43,7 +43,8 @@
  *   - Every entry point is asynchronous on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream).  Argument errors are detected on the host and
  *     returned before anything is launched; nothing is written in that case.
- *   - Calls are deterministic: identical inputs give bit-identical outputs.
+ *   - Calls are deterministic: identical arguments (sizes, data and, for the FP16 /
+ *     BF16 GEMMs, workspace size) on the same GPU give bit-identical outputs.
  *   - A wait inside a kernel that exceeds its time limit does not hang the GPU: the
  *     kernel records LL_ERR_DEVICE_TIMEOUT in the status word and exits.
  *
