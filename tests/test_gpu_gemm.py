@@ -229,6 +229,33 @@ def test_pair_in_place_c_equals_d(orc, ld_pad):
                                                         C.ravel(), ld, rows=r), M, N, K, "f32", "bf16", "pair in place")
 
 
+@pytest.mark.parametrize("ldc,c_off", [(2001, 0), (2009, 8), (2003, 0), (2001, 1)])
+def test_pair_fp32_rows_off_grid_c_pitches_and_offsets(orc, ldc, c_off):
+    """FP32 D with 2001-float rows (off the 16- and 32-byte grids) on CTA pairs, C read
+    through TMA by row classes with its own pitch and base offset (the same sector grid
+    as D's rows, or another), D stored by whole sectors.  Every element, padding columns
+    and rows past M untouched."""
+    import linear_layer_gb300 as ll
+    M, N, K, ldd = 1500, 1992, 200, 2001
+    A = wl.operand("bf16", M, K, 71)
+    B = wl.operand("bf16", K, N, 72)
+    C = wl.f32_normal(M, N, 73, ld=ldc)
+    buf = torch.full((M * ldc + 8,), float("nan"), dtype=torch.float32, device="cuda")
+    buf[c_off:c_off + M * ldc] = up(C.ravel())
+    tC = buf[c_off:c_off + M * ldc]
+    guard = 9
+    tD = out_tensor(M + guard, ldd, "f32")
+    ll.gemm_bf16(M, N, K, 0.75, up(A), K, up(B), N, -1.25, tC, ldc, tD, ldd, ll.OUT_F32)
+    st, word = ll.get_device_status()
+    assert st == ll.LL_OK, "device status %s (word %#x)" % (ll.status_string(st), word)
+    D = tD.cpu().numpy()
+    assert np.isnan(D[M:]).all(), "rows past M were written"
+    assert np.isnan(D[:M, N:]).all(), "padding columns were written"
+    assert_fully_written(tD, M, N, "C pitch %d offset %d" % (ldc, c_off))
+    check_all_rows(D, lambda r: orc.gemm("bf16", M, N, K, 0.75, A.ravel(), K, B.ravel(), N, -1.25, C.ravel(), ldc,
+                                         rows=r), M, N, K, "f32", "bf16", "C pitch %d offset %d" % (ldc, c_off))
+
+
 @pytest.mark.parametrize("ld_pad", [0, 8, 3])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_pair_writes_nothing_outside_d(orc, ld_pad, out):
