@@ -100,6 +100,13 @@ typedef enum { LL_OUT_F32 = 0, LL_OUT_BF16 = 1, LL_OUT_F16 = 2 } ll_out_type;
  * FP32 partial sums over K are added (partials are added in a fixed order), so the
  * result is deterministic for a given problem and workspace size.  A workspace must
  * not be shared by calls that may run at the same time (other streams, other threads).
+ * The pair that finishes a split tile waits (bounded) for pairs of lower index, which
+ * the hardware starts no later than it; if kernels on other streams keep part of the
+ * grid from starting for longer than the wait limit (ll_set_wait_timeout_ns), the call
+ * reports LL_ERR_DEVICE_TIMEOUT rather than hang.  A caller that runs other kernels
+ * concurrently with large GEMMs can turn the split off by passing one byte less than
+ * ll_gemm_workspace_size reports (the repacks still fit): the split runs exactly when
+ * ws_bytes reaches that figure.
  */
 size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int in_type);
 

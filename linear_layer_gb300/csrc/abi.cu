@@ -303,12 +303,14 @@ ll_status gemm_common(const ll::GemmArgs& a, void* workspace, size_t ws_bytes, l
   if (workspace != nullptr)
     base = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~static_cast<uintptr_t>(255));
   ll::GemmArgs b = a;
-  if (base != nullptr && ll::sk_capable(a)) {  // what the repacks leave: the stream-K partial tiles
-    const size_t skip = static_cast<size_t>(round_up(static_cast<int64_t>(need), 256)) +
-                        (reinterpret_cast<uintptr_t>(base) - reinterpret_cast<uintptr_t>(workspace));
-    if (ws_bytes > skip) {
-      b.sk_ws = static_cast<unsigned char*>(workspace) + skip;
-      b.sk_bytes = ws_bytes - skip;
+  if (base != nullptr && ll::sk_capable(a)) {
+    // what the repacks leave, past the 256 bytes ll_gemm_workspace_size reserves for
+    // alignment: the stream-K partial tiles, so the split runs exactly when ws_bytes
+    // reaches the figure ll_gemm_workspace_size reports
+    const size_t rep = static_cast<size_t>(round_up(static_cast<int64_t>(need), 256));
+    if (ws_bytes > rep + 256) {
+      b.sk_ws = static_cast<unsigned char*>(base) + rep;
+      b.sk_bytes = ws_bytes - rep - 256;
     }
   }
   return ll::launch_gemm_planned(b, plan, base, ctx);

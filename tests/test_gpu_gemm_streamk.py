@@ -59,3 +59,24 @@ def test_streamk_deterministic(orc):
 def test_without_streamk_workspace(orc):
     # no workspace: the same problem with the last wave as halves, also within tolerance
     _run(orc, "bf16", 4096, 4096, 4096, 1.0, 1.0, "bf16", with_ws=False)
+
+
+def test_one_byte_less_turns_the_split_off():
+    """The split runs exactly when the workspace reaches the size ll_gemm_workspace_size
+    reports: with one byte less the call schedules the last wave as halves, so its output
+    equals the no-workspace call's bit for bit."""
+    import linear_layer_gb300 as ll
+    M = N = K = 4096
+    A = up(wl.operand("bf16", M, K, 91))
+    B = up(wl.operand("bf16", K, N, 92))
+    C = up(wl.f32_normal(M, N, 93))
+    need = ll.gemm_workspace_size(M, N, K, K, N, ll.IN_BF16)
+    assert need > 0
+    outs = []
+    for ws in (None, torch.empty(need - 1, dtype=torch.uint8, device="cuda")):
+        tD = out_tensor(M, N, "f32")
+        ll.gemm_bf16(M, N, K, 1.0, A, K, B, N, 1.0, C, N, tD, N, ll.OUT_F32, workspace=ws)
+        st, word = ll.get_device_status()
+        assert st == ll.LL_OK, "device status %s (word %#x)" % (ll.status_string(st), word)
+        outs.append(tD)
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
