@@ -640,11 +640,14 @@ def bench_fp8(args, dev, stream, peaks, peak_src):
     sets.append((tA.clone(), tsA.clone(), tB.clone(), tsB.clone(),
                  torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
     KB, NB = sA.shape[1], sB.shape[1]
+    # the workspace the library asks for (here: the partial tiles of its stream-K tail)
+    ws_bytes = ll.gemm_workspace_size(M, N, K, K, N, ll.IN_E4M3)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
 
     def call(i):
         a, sa, b, sb, d = sets[i % 2]
         ll.gemm_fp8_blockscaled(M, N, K, 1.0, a, K, sa, KB, b, N, sb, NB, 0.0, None, N, d, N,
-                                ll.OUT_BF16, stream=stream)
+                                ll.OUT_BF16, workspace=ws, stream=stream)
 
     for i in range(3):
         call(i)
@@ -670,6 +673,7 @@ def bench_fp8(args, dev, stream, peaks, peak_src):
                          "algorithmic_bytes_per_launch": M * K + K * N + M * KB * 4 + KB * NB * 4 + M * N * 2},
             "timing": "median of 5 groups of %d back-to-back launches alternating 2 input sets "
                       "(A+B 128 MB each)" % steps,
+            "workspace_bytes": ws_bytes,
             "status": ll.status_string(st)}
 
 

@@ -44,7 +44,8 @@
  *     legacy default stream).  Argument errors are detected on the host and
  *     returned before anything is launched; nothing is written in that case.
  *   - Calls are deterministic: identical arguments (sizes, data and, for the FP16 /
- *     BF16 GEMMs, workspace size) on the same GPU give bit-identical outputs.
+ *     BF16 and FP8 block-scaled GEMMs, workspace size) on the same GPU give
+ *     bit-identical outputs.
  *   - A wait inside a kernel that exceeds its time limit does not hang the GPU: the
  *     kernel records LL_ERR_DEVICE_TIMEOUT in the status word and exits.
  *
@@ -90,17 +91,19 @@ typedef enum { LL_OUT_F32 = 0, LL_OUT_BF16 = 1, LL_OUT_F16 = 2 } ll_out_type;
  * (row pitch rounded up to 16 bytes) inside the same stream, and that copy is part
  * of the call.  The figure assumes 16-byte-aligned base pointers; a misaligned base
  * pointer is repacked too and needs at most ll_gemm_workspace_size(...,lda=1,ldb=1).
- * For FP16 / BF16 inputs the figure also holds room for the partial accumulators of
- * the stream-K tail (when a CUDA device is current and the problem leaves a partial
- * last wave of 256 x 256 tiles): the K blocks of the last tiles are then split evenly
- * over all SM pairs, and a pair that ends inside a tile leaves its FP32 partial and a
- * ready flag in the workspace for the pair that finishes the tile.  That room is
- * optional: with less workspace (or none) the call still succeeds and finishes the
- * last wave with half-width tiles instead.  The split changes only the order in which
- * FP32 partial sums over K are added (partials are added in a fixed order), so the
+ * The figure also holds room for the partial accumulators of the stream-K tail (when a
+ * CUDA device is current and the problem leaves a partial last wave of tiles: 256 x 256
+ * tiles on SM pairs for FP16 / BF16 inputs, 128 x 256 tiles on single SMs for 8-bit
+ * inputs with FP32 block scales): the K blocks of the last tiles are then split evenly
+ * over all workers (SM pairs or SMs), and a worker whose range ends inside a tile leaves
+ * its FP32 partial (for 8-bit inputs: block scales applied) and a ready flag in the
+ * workspace for the worker that finishes the tile.  That room is optional: with less
+ * workspace (or none) the call still succeeds and finishes the last wave with half-width
+ * tiles (16-bit) or whole tiles (8-bit) instead.  The split changes only the order in
+ * which FP32 partial sums over K are added (partials are added in a fixed order), so the
  * result is deterministic for a given problem and workspace size.  A workspace must
  * not be shared by calls that may run at the same time (other streams, other threads).
- * The pair that finishes a split tile waits (bounded) for pairs of lower index, which
+ * The worker that finishes a split tile waits (bounded) for workers of lower index, which
  * the hardware starts no later than it; if kernels on other streams keep part of the
  * grid from starting for longer than the wait limit (ll_set_wait_timeout_ns), the call
  * reports LL_ERR_DEVICE_TIMEOUT rather than hang.  A caller that runs other kernels

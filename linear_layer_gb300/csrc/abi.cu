@@ -197,8 +197,8 @@ ll_status ll::validate_gemm(const GemmArgs& a, const void* ws, size_t ws_bytes) 
       return LL_ERR_INVALID_ARG;
   }
   // D may share bytes with no input other than itself as C (in place, checked above);
-  // a workspace that a repack or the stream-K tail (16-bit inputs) may write shares
-  // bytes with nothing
+  // a workspace that a repack or the stream-K tail (16-bit inputs, 8-bit inputs with
+  // FP32 block scales) may write shares bytes with nothing
   const int64_t es = in_esize(a.in_type);
   const bool c_read = a.beta != 0.0f;
   const bool in_place = c_read && static_cast<const void*>(a.C) == a.D;
@@ -347,29 +347,34 @@ bool gemv_outputs_overlap(int N, int K, const void* x, int x_esize, const float*
 
 extern "C" {
 
-size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int in_type) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
+// operand repacks only
+static size_t gemm_repack_need(int M, int N, int K, int64_t lda, int64_t ldb, int in_type) {
   const int es = in_esize(in_type);
   size_t need = 0;
   if ((lda * es) % 16 != 0) need += repack_bytes(M, K, es);
   if ((ldb * es) % 16 != 0) need += repack_bytes(K, N, es);
-  if (in_type == LL_IN_F16 || in_type == LL_IN_BF16) {  // the optional stream-K tail
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
-      const size_t sk = ll::pair_sk_workspace(M, N, K, sms);
-      if (sk) need = static_cast<size_t>(round_up(static_cast<int64_t>(need), 256)) + 256 + sk;
-    } else {
-      cudaGetLastError();
-    }
+  return need;
+}
+
+size_t ll_gemm_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb, int in_type) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  size_t need = gemm_repack_need(M, N, K, lda, ldb, in_type);
+  // the optional stream-K tail of the CTA-pair 16-bit kernel or the one-CTA FP8 kernel
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+    const bool f16 = in_type == LL_IN_F16 || in_type == LL_IN_BF16;
+    const size_t sk = f16 ? ll::pair_sk_workspace(M, N, K, sms) : ll::fp8_sk_workspace(M, N, K, sms);
+    if (sk) need = static_cast<size_t>(round_up(static_cast<int64_t>(need), 256)) + 256 + sk;
+  } else {
+    cudaGetLastError();
   }
   return need;
 }
 
 size_t ll_gemm_mxf8_workspace_size(int M, int N, int K, int64_t lda, int64_t ldb) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
-  return ll_gemm_workspace_size(M, N, K, lda, ldb, LL_IN_E4M3) + ll::mx_scale_block_bytes(M, N, K, false, nullptr) +
-         512;
+  return gemm_repack_need(M, N, K, lda, ldb, LL_IN_E4M3) + ll::mx_scale_block_bytes(M, N, K, false, nullptr) + 512;
 }
 
 size_t ll_gemm_nvf4_workspace_size(int M, int N, int K, int64_t lda, int64_t ldbt) {

@@ -21,7 +21,7 @@ struct GemmParams {
   int c_vec, d_vec;  // rows of C / D may be accessed with 4-element vectors
   int d_row16;       // rows of D start on 16-byte boundaries
   int epi_tma;       // CTA-pair 16-bit epilogue through TMA (C and D rows 16-byte aligned)
-  int epi_res;       // CTA-pair epilogue through TMA by row classes (FP32 D rows not 16-byte aligned)
+  int epi_res;       // CTA-pair epilogue for FP32 D rows not 16-byte aligned: C by TMA row classes, D by sectors
   const float* sA;
   int64_t ld_sa;
   const float* sB;

@@ -66,7 +66,7 @@ struct TileCfg {
   static constexpr int EPI_WARP0 = 2;  // first epilogue warp
   static constexpr int THREADS = 32 * EPI_WARP0 + EPI_THREADS;
   static constexpr int EPI_STAGE_BYTES = FP8 ? 0 : EPI_WARPS * 32 * 32 * 4;  // 32x32 FP32 per warp
-  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 256 + 1024;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_STAGE_BYTES + 512 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(B_BOXES >= 1 && BN % B_BOX_N == 0, "tile N must cover whole swizzle rows");
   static_assert(STAGE_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
@@ -231,10 +231,25 @@ __device__ __forceinline__ void store_rows(const GemmParams& p, const float* st,
   }
 }
 
+// Schedule of the one-CTA kernel: whole tiles t = cta, cta + grid, ... below full_tiles;
+// with an FP8 stream-K tail (sk_tiles > 0) the sk_tiles tiles after them are done by K
+// ranges, one contiguous range of their K blocks per CTA.  A CTA whose range ends inside a
+// tile writes that piece's promoted FP32 partial to its slot of sk_part (128 rows x 256
+// columns) and sets its promotion warps' flags (sk_flag[cta * 8 + warp]) to `epoch`; the
+// CTA whose range ends at a tile's end adds the partials of the CTAs before it, in CTA
+// order, and stores the tile.
+struct TileSched {
+  int full_tiles;
+  int sk_tiles;
+  float* sk_part;
+  unsigned long long* sk_flag;
+  unsigned long long epoch;
+};
+
 template <class Cfg, uint32_t AB_FMT>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const GemmParams p, const TileSched ts) {
   constexpr int S = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
   constexpr uint32_t IDESC = make_idesc(AB_FMT, BN, 128);
@@ -248,6 +263,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   // bars: full[S], empty[S], tfull[NA], tempty[NA], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NA + 1);
   uint32_t* abort_flag = tmem_slot + 1;
+  // this CTA's stream-K items (at most two: a range of fewer K blocks than a tile meets at
+  // most two tiles), written once by thread 0 and read by every role
+  int4* sk_items = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(abort_flag + 1) + 15) & ~static_cast<uintptr_t>(15));
+  int* sk_count = reinterpret_cast<int*>(sk_items + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -283,16 +302,74 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   WaitCtx wctx{p.status, p.timeout_ns, abort_flag};
   const int num_m = (p.M + 127) / 128;
   const int num_n = (p.N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
   const int KB = (p.K + Cfg::BK - 1) / Cfg::BK;
+  // This CTA's work items, in order: its stream-K pieces first (the piece that ends inside
+  // a tile, kind kSkPart; then the piece that ends at a tile's end, kSkOwner when CTAs
+  // before this one hold the tile's first K blocks, otherwise kWhole), then its whole
+  // tiles t = cta, cta + grid, ... below ts.full_tiles, as in the CTA-pair kernel.  The
+  // stream-K items live in shared memory, so the roles' loops carry no extra state.
+  enum { kWhole = 0, kSkPart = 1, kSkOwner = 2 };
+  struct Item {
+    int t, kb0, kb1, kind, pfirst;
+  };
+  if (threadIdx.x == 0) {
+    const int cta = blockIdx.x, P = gridDim.x;
+    const int64_t sk_total = static_cast<int64_t>(ts.sk_tiles) * KB;
+    auto sk_begin = [&](int c2) { return static_cast<int64_t>(c2) * sk_total / P; };
+    const int64_t sk_a = sk_begin(cta), sk_b = sk_begin(cta + 1);
+    // the tiles the range [sk_a, sk_b) meets: the piece that ends inside a tile first
+    const int t_first = static_cast<int>(sk_a / KB);
+    const int t_last = sk_b > sk_a ? static_cast<int>((sk_b - 1) / KB) : t_first - 1;
+    int n = 0;
+    for (int pass = 0; pass < 2; ++pass)
+      for (int t = t_first; t <= t_last && n < 2; ++t) {
+        const int64_t t0 = static_cast<int64_t>(t) * KB;
+        const int kb0 = static_cast<int>((sk_a > t0 ? sk_a : t0) - t0);
+        const int kb1 = static_cast<int>((sk_b < t0 + KB ? sk_b : t0 + KB) - t0);
+        const bool part = kb1 < KB;
+        if (part != (pass == 0)) continue;
+        const int kind = part ? kSkPart : (kb0 > 0 ? kSkOwner : kWhole);
+        int pf = cta;
+        if (kind == kSkOwner)  // the CTAs whose ranges end inside this tile
+          while (pf > 0 && sk_begin(pf) > t0) --pf;
+        sk_items[n] = make_int4(ts.full_tiles + t, kb0 | (kb1 << 16), kind, pf);
+        ++n;
+      }
+    *sk_count = n;
+  }
+  __syncthreads();
+  const int n_sk = *sk_count;
+  const int n_items =
+      n_sk + (static_cast<int>(blockIdx.x) < ts.full_tiles
+                  ? (ts.full_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                  : 0);
+  auto item = [&](int i) {
+    Item it;
+    if (i < n_sk) {
+      const int4 v = sk_items[i];
+      it.t = v.x;
+      it.kb0 = v.y & 0xFFFF;
+      it.kb1 = v.y >> 16;
+      it.kind = v.z;
+      it.pfirst = v.w;
+    } else {
+      it.t = static_cast<int>(blockIdx.x) + (i - n_sk) * static_cast<int>(gridDim.x);
+      it.kb0 = 0;
+      it.kb1 = KB;
+      it.kind = kWhole;
+      it.pfirst = blockIdx.x;
+    }
+    return it;
+  };
 
   // programmatic dependent launch (as in the pair kernel): L2 prefetch of the first
   // ring of operand tiles, then the wait for the previous kernel of the stream
-  if (warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < num_tiles) {
+  if (warp == 0 && lane == 0 && n_items > 0) {
+    const Item it0 = item(0);
     int mb, nb;
-    tile_coords(blockIdx.x, num_m, num_n, p.group_m, mb, nb);
-    const int pre = KB < S ? KB : S;
-    for (int kb = 0; kb < pre; ++kb) {
+    tile_coords(it0.t, num_m, num_n, p.group_m, mb, nb);
+    const int pre = it0.kb1 - it0.kb0 < S ? it0.kb1 - it0.kb0 : S;
+    for (int kb = it0.kb0; kb < it0.kb0 + pre; ++kb) {
       tma_prefetch_l2(&tmA, kb * Cfg::BK, mb * 128);
       for (int j = 0; j < Cfg::B_BOXES; ++j) tma_prefetch_l2(&tmB, nb * BN + j * Cfg::B_BOX_N, kb * Cfg::BK);
     }
@@ -306,10 +383,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       tma_prefetch_desc(&tmB);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int i = 0; i < n_items && ok; ++i) {
+        const Item w = item(i);
         int mb, nb;
-        tile_coords(t, num_m, num_n, p.group_m, mb, nb);
-        for (int kb = 0; kb < KB; ++kb) {
+        tile_coords(w.t, num_m, num_n, p.group_m, mb, nb);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1u;
           if (!wait_bounded(empty_bar(s), ph ^ 1u, wctx, kRoleProducer)) {
@@ -338,7 +416,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int i = 0; i < n_items && ok; ++i) {
+        const Item w = item(i);
         uint32_t d_tmem = 0;
         if (!Cfg::FP8) {
           const uint32_t ab = acc_it % NA;
@@ -349,7 +428,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           tc_fence_after();
           d_tmem = tmem_base + ab * BN;
         }
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (Cfg::FP8) {  // one TMEM partial buffer per 128-K block, alternating
             const uint32_t pb = acc_it % NA;
             if (!wait_bounded(tempty_bar(pb), ((acc_it / NA) & 1u) ^ 1u, wctx, kRoleMma)) {
@@ -372,7 +451,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc =
                 smem_desc_sw128(b_base + kk * Cfg::UMMA_K * 128, Cfg::B_BOX_BYTES, 1024);
-            const uint32_t accum = Cfg::FP8 ? (kk > 0) : (kb > 0 || kk > 0);
+            const uint32_t accum = Cfg::FP8 ? (kk > 0) : (kb > w.kb0 || kk > 0);
             if (Cfg::FP8)
               mma_f8(d_tmem, adesc, bdesc, IDESC, accum);
             else
@@ -401,9 +480,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     float* st = epi_stage + (warp - 2) * 32 * 32;
     uint32_t acc_it = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int i = 0; i < n_items; ++i) {  // whole tiles only (no stream-K for 16-bit here)
       int mb, nb;
-      tile_coords(t, num_m, num_n, p.group_m, mb, nb);
+      tile_coords(item(i).t, num_m, num_n, p.group_m, mb, nb);
       const uint32_t ab = acc_it % NA;
       bool ok = wait_bounded(tfull_bar(ab), (acc_it / NA) & 1u, wctx, kRoleEpilogue);
       ok = __all_sync(0xffffffffu, ok);
@@ -438,9 +517,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     uint32_t pit = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    // a stream-K slot holds the CTA's 128 rows x 256 columns as [warp][chunk][4-column
+    // group][row within the warp's 32][4]: a warp's 32 lanes access 512 contiguous bytes
+    auto sk_vec = [&](int slot, int c, int j) {
+      return reinterpret_cast<float4*>(ts.sk_part + static_cast<size_t>(slot) * (128 * 256)) +
+             (((ew * CH + c) * 8 + j) * 32 + lane);
+    };
+    auto sk_flag = [&](int slot) { return ts.sk_flag + static_cast<size_t>(slot) * 8 + ew; };
+    for (int i = 0; i < n_items && ok; ++i) {
+      const Item w = item(i);
       int mb, nb;
-      tile_coords(t, num_m, num_n, p.group_m, mb, nb);
+      tile_coords(w.t, num_m, num_n, p.group_m, mb, nb);
       const int m = mb * 128 + q * 32 + lane;
       const bool row_ok = m < p.M;
       const int ncol0 = nb * BN + h * HALF;
@@ -452,11 +539,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       for (int c = 0; c < CH; ++c)
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[c][j] = 0.0f;
-      float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
-      float sb_next = col_ok ? __ldg(p.sB + nblk) : 0.0f;
-      for (int kb = 0; kb < KB; ++kb) {
+      float sa_next = row_ok ? __ldg(sa_row + w.kb0) : 0.0f;
+      float sb_next = col_ok ? __ldg(p.sB + static_cast<int64_t>(w.kb0) * p.ld_sb + nblk) : 0.0f;
+      for (int kb = w.kb0; kb < w.kb1; ++kb) {
         const float s = sa_next * sb_next;
-        if (kb + 1 < KB) {  // next block's scales travel while this block is promoted
+        if (kb + 1 < w.kb1) {  // next block's scales travel while this block is promoted
           sa_next = row_ok ? __ldg(sa_row + kb + 1) : 0.0f;
           sb_next = col_ok ? __ldg(p.sB + static_cast<int64_t>(kb + 1) * p.ld_sb + nblk) : 0.0f;
         }
@@ -487,6 +574,44 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         ++pit;
       }
       if (!ok) break;
+      const Item wk = item(i);  // (shared memory) kind and first CTA of this item
+      if (wk.kind == kSkPart) {
+        // a piece that ends inside its tile: the promoted partial goes to this CTA's slot,
+        // then the flag tells the CTA that completes the tile
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *sk_vec(blockIdx.x, c, j) = make_float4(acc[c][4 * j], acc[c][4 * j + 1], acc[c][4 * j + 2], acc[c][4 * j + 3]);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) flag_release(sk_flag(blockIdx.x), ts.epoch);
+        continue;
+      }
+      if (wk.kind == kSkOwner) {  // add the partials of the CTAs before this one, in order
+        const int cta = blockIdx.x;
+        bool fw = true;
+        if (lane == 0)
+          for (int c2 = wk.pfirst; c2 < cta && fw; ++c2) fw = flag_wait_bounded(sk_flag(c2), ts.epoch, wctx, kRoleEpilogue);
+        fw = __shfl_sync(0xffffffffu, fw ? 1 : 0, 0) != 0;
+        __syncwarp();  // lane 0's acquire, before every lane's reads of the partials
+        if (!fw) {
+          ok = false;
+          break;
+        }
+        for (int c2 = wk.pfirst; c2 < cta; ++c2) {
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 v = __ldcg(sk_vec(c2, c, j));
+              acc[c][4 * j] += v.x;
+              acc[c][4 * j + 1] += v.y;
+              acc[c][4 * j + 2] += v.z;
+              acc[c][4 * j + 3] += v.w;
+            }
+        }
+      }
       epilogue_rows<CH>(p, m, ncol0, acc);
     }
   }
@@ -1275,6 +1400,64 @@ bool make_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType 
 }
 
 
+// stream-K tail: one 256 x 256 FP32 partial slot (two CTAs x 128 rows) and 8 flags per pair
+size_t pair_sk_bytes(int pairs) {
+  return static_cast<size_t>(pairs) * (2 * 128 * 256 * sizeof(float) + 8 * sizeof(unsigned long long));
+}
+
+// The schedule's tail: W whole waves of P workers (CTA pairs, or CTAs of the one-CTA FP8
+// kernel) and R more tiles.  The R tiles are split by K ranges across all P workers when
+// there are at least P / 4 of them and at least 8 K blocks a tile (so that no tile has
+// more than ~5 pieces); otherwise the 16-bit pair kernel runs them as 256 x 128 halves and
+// the FP8 kernel as whole tiles.
+static bool sk_tail(int T, int P, int KB, int& W, int& R) {
+  W = T / P;
+  R = T - W * P;
+  return W >= 1 && R > 0 && 4 * R >= P && KB >= 8;
+}
+
+size_t pair_sk_workspace(int M, int N, int K, int num_sms) {
+  const int P = num_sms / 2;
+  if (P <= 0) return 0;
+  const int T = ((M + 255) / 256) * ((N + 255) / 256);
+  const int KB = (K + PairCfg<256>::BK - 1) / PairCfg<256>::BK;
+  int W, R;
+  return sk_tail(T, P, KB, W, R) ? pair_sk_bytes(P) : 0;
+}
+
+// A value no flag of an earlier call holds: a per-process random high word over a call count.
+static unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> seq{0};
+  static const unsigned long long salt = [] {
+    unsigned long long x = static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                           static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(&seq));
+    x += 0x9E3779B97F4A7C15ull;  // splitmix64 finaliser
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    x ^= x >> 31;
+    return (x | 1ull) << 32;
+  }();
+  return salt | ((seq.fetch_add(1) + 1) & 0xFFFFFFFFull);
+}
+
+// FP8 stream-K tail: one 128 x 256 FP32 partial slot and 8 flags (one per promotion
+// warp) per CTA
+size_t fp8_sk_bytes(int ctas) {
+  return static_cast<size_t>(ctas) * (128 * 256 * sizeof(float) + 8 * sizeof(unsigned long long));
+}
+
+size_t fp8_sk_workspace(int M, int N, int K, int num_sms) {
+  if (num_sms <= 0 || M <= 0 || N <= 0 || K <= 0) return 0;
+  // the tile width run_fp8 picks
+  const int tiles128 = ((M + 127) / 128) * ((N + 127) / 128);
+  const int BN = (N > 128 && tiles128 > num_sms) ? 256 : 128;
+  const int T = ((M + 127) / 128) * ((N + BN - 1) / BN);
+  const int P = T < num_sms ? T : num_sms;
+  const int KB = (K + 127) / 128;
+  int W, R;
+  return KB < 32768 && sk_tail(T, P, KB, W, R) ? fp8_sk_bytes(P) : 0;
+}
+
 constexpr int kMaxDev = 64;
 
 template <class Cfg, uint32_t AB_FMT>
@@ -1295,6 +1478,25 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
 
   const int num_tiles = ((a.M + 127) / 128) * ((a.N + Cfg::BN - 1) / Cfg::BN);
   const int grid = num_tiles < ctx.num_sms ? num_tiles : ctx.num_sms;
+  TileSched ts;
+  ts.full_tiles = num_tiles;
+  ts.sk_tiles = 0;
+  ts.sk_part = nullptr;
+  ts.sk_flag = nullptr;
+  ts.epoch = 0;
+  if (Cfg::FP8) {  // stream-K tail, when the caller's workspace has room for it
+    const int KB = (a.K + Cfg::BK - 1) / Cfg::BK;
+    int W, R;
+    // (K block indices are packed into 16 bits in the kernel's item table)
+    if (KB < 32768 && sk_tail(num_tiles, grid, KB, W, R) && a.sk_ws != nullptr && a.sk_bytes >= fp8_sk_bytes(grid)) {
+      ts.full_tiles = W * grid;
+      ts.sk_tiles = R;
+      ts.sk_part = static_cast<float*>(a.sk_ws);
+      ts.sk_flag = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(a.sk_ws) +
+                                                         static_cast<size_t>(grid) * 128 * 256 * sizeof(float));
+      ts.epoch = next_epoch();
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(Cfg::THREADS);
@@ -1305,51 +1507,13 @@ static ll_status run(const GemmArgs& a, const LaunchCtx& ctx) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p, ts) != cudaSuccess) {
     cudaGetLastError();
     return LL_ERR_CUDA;
   }
   return LL_OK;
 }
 
-
-// stream-K tail: one 256 x 256 FP32 partial slot (two CTAs x 128 rows) and 8 flags per pair
-size_t pair_sk_bytes(int pairs) {
-  return static_cast<size_t>(pairs) * (2 * 128 * 256 * sizeof(float) + 8 * sizeof(unsigned long long));
-}
-
-// The schedule's tail: W whole waves of P pairs and R more tiles.  The R tiles are split by
-// K ranges across all P pairs when there are at least P / 4 of them and at least 8 K blocks
-// a tile (so that no tile has more than ~4 pieces); fewer run as 256 x 128 halves.
-static bool pair_sk_tail(int T, int P, int KB, int& W, int& R) {
-  W = T / P;
-  R = T - W * P;
-  return W >= 1 && R > 0 && 4 * R >= P && KB >= 8;
-}
-
-size_t pair_sk_workspace(int M, int N, int K, int num_sms) {
-  const int P = num_sms / 2;
-  if (P <= 0) return 0;
-  const int T = ((M + 255) / 256) * ((N + 255) / 256);
-  const int KB = (K + PairCfg<256>::BK - 1) / PairCfg<256>::BK;
-  int W, R;
-  return pair_sk_tail(T, P, KB, W, R) ? pair_sk_bytes(P) : 0;
-}
-
-// A value no flag of an earlier call holds: a per-process random high word over a call count.
-static unsigned long long next_epoch() {
-  static std::atomic<unsigned long long> seq{0};
-  static const unsigned long long salt = [] {
-    unsigned long long x = static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
-                           static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(&seq));
-    x += 0x9E3779B97F4A7C15ull;  // splitmix64 finaliser
-    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
-    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
-    x ^= x >> 31;
-    return (x | 1ull) << 32;
-  }();
-  return salt | ((seq.fetch_add(1) + 1) & 0xFFFFFFFFull);
-}
 
 template <uint32_t AB_FMT>
 static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
@@ -1449,7 +1613,7 @@ static ll_status run_pair(const GemmArgs& a, const LaunchCtx& ctx) {
   {  // stream-K tail (TMA epilogue only), when the caller's workspace has room for it
     const int KB = (a.K + Cfg::BK - 1) / Cfg::BK;
     int W, R;
-    if (p.epi_tma && T > max_pairs[dev] && pair_sk_tail(T, max_pairs[dev], KB, W, R) && a.sk_ws != nullptr &&
+    if (p.epi_tma && T > max_pairs[dev] && sk_tail(T, max_pairs[dev], KB, W, R) && a.sk_ws != nullptr &&
         a.sk_bytes >= pair_sk_bytes(max_pairs[dev])) {
       P = max_pairs[dev];
       sc.full_units = W * P;

@@ -55,9 +55,14 @@ size_t pair_sk_bytes(int pairs);
 // Those bytes for an M x N x K 16-bit problem on a GPU with num_sms SMs, or 0 when its
 // schedule has no such tail (gemm_tc.cu).
 size_t pair_sk_workspace(int M, int N, int K, int num_sms);
-// Whether the call may place stream-K partial tiles in its workspace: FP16 / BF16 inputs.
+// The same for the one-CTA FP8 kernel (FP32 block scales): bytes for up to `ctas` CTAs,
+// and for an M x N x K problem (0 when its schedule has no such tail) (gemm_tc.cu).
+size_t fp8_sk_bytes(int ctas);
+size_t fp8_sk_workspace(int M, int N, int K, int num_sms);
+// Whether the call may place stream-K partial tiles in its workspace: FP16 / BF16 inputs,
+// and 8-bit inputs with FP32 block scales.
 inline bool sk_capable(const GemmArgs& a) {
-  return !a.mx && !a.nvf4 && (a.in_type == LL_IN_F16 || a.in_type == LL_IN_BF16);
+  return !a.mx && !a.nvf4;
 }
 
 // Launch context of the current device (status word, SM count, wait limit) for `stream`;
