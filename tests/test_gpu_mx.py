@@ -138,3 +138,14 @@ def test_mx_k_zero_is_beta_c():
     assert st == ll.LL_OK
     want = torch.from_numpy((np.float32(2.5) * C).astype(np.float32))
     assert torch.equal(tD.cpu(), want)
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,out", [(2560, 2560, 1100, 0.5, -1.25, "f32"),
+                                                  (2500, 2400, 1024, 1.0, 0.0, "bf16")])
+def test_mx_pair_kernel_partial_wave(orc, M, N, K, alpha, beta, out):
+    """100 pair tiles on the CTA-pair kernel: more than a wave of SM pairs, then a partial
+    one, with K, M and N tails; repeat calls bit-identical."""
+    a = run_mx(orc, M, N, K, alpha, beta, out, seed=13)
+    b = run_mx(orc, M, N, K, alpha, beta, out, seed=13)
+    assert torch.equal(a.view(torch.int32 if out == "f32" else torch.int16),
+                       b.view(torch.int32 if out == "f32" else torch.int16))

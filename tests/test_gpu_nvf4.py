@@ -160,3 +160,11 @@ def test_nvf4_k_zero_is_beta_c():
     assert st == ll.LL_OK
     want = torch.from_numpy((np.float32(-0.75) * C).astype(np.float32))
     assert torch.equal(tD.cpu(), want)
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,out", [(2560, 2500, 2300, 1.0, 1.0, "f16"),
+                                                  (2500, 2560, 2048, 0.5, 0.0, "f32")])
+def test_nvf4_pair_kernel_partial_wave(orc, M, N, K, alpha, beta, out):
+    """100 pair tiles on the CTA-pair kernel: more than a wave of SM pairs, then a partial
+    one, with M, N and K tails (8 or 9 K blocks of 256)."""
+    run_nvf4(orc, M, N, K, alpha, beta, out, seed=13)
