@@ -136,8 +136,10 @@ def test_gemv_rejects_overflowing_k():
 
 
 @pytest.mark.parametrize("a_fmt,b_fmt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
-@pytest.mark.parametrize("M,N,K", [(200, 300, 389), (2048, 2048, 512)])
+@pytest.mark.parametrize("M,N,K", [(200, 300, 389), (2048, 2048, 512), (2560, 2560, 1024)])
 def test_f8_mixed_formats(orc, a_fmt, b_fmt, M, N, K):
+    """Every pairing of E4M3 / E5M2 operands; 2560 x 2560 x 1024 (200 tiles of 128 x 256 on
+    152 SMs) also splits its last wave by K ranges, the workspace query counting the slots."""
     import linear_layer_gb300 as ll
     code = {"e4m3": ll.IN_E4M3, "e5m2": ll.IN_E5M2}
     A, sA = wl.e4m3_blockquant_rowblocks(M, K, 61, fmt=a_fmt)
