@@ -8,7 +8,8 @@ other kernels of the path ("extra"): the batch-1 W8A8 GEMV 1 x 4096 . 4096 x 110
 (GB/s of HBM) and its fused FP16-activation form, the W8A8 and weight-only layers for a
 few tokens, the FP8 E4M3 block-scaled GEMM 8192^3, the MXFP8 and NVFP4 GEMMs 8192^3
 (hardware block scaling), the ragged FP16 GEMM 4093 x 5003 x 2056 and the launch-bound
-FP16 256^3.
+FP16 256^3.  Every GEMM is given the workspace ll_gemm_*workspace_size asks for, so the
+BF16 headline and the FP8 GEMM run their stream-K tails.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
